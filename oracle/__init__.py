@@ -1,0 +1,297 @@
+"""CPU oracle for the routed MoE expert FFN: numpy-facing wrappers over liboracle.so.
+
+TEST INFRASTRUCTURE ONLY. This package is imported by the test suite, by the
+smoke check and by the benchmark's CPU-baseline leg, and by nothing in the
+product path (the CUDA library and its Python binding never import it). It
+shares no code with the GPU side: only the seeded input generators are common.
+
+Every function is a direct wrapper over the C function of the same name
+without the ``orc_`` prefix; see oracle/moe_oracle.c for the definitions and
+the page sections they restate.
+
+Parity unpinned: ``glu_oai`` (the gpt-oss GLU formula of the decode path; the
+pages give its parameters only).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from ._build import LIB, build_oracle
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = build_oracle()
+        _lib = ctypes.CDLL(path)
+        _declare(_lib)
+    return _lib
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L = ctypes.c_long
+_F = ctypes.c_float
+
+
+def _declare(L):
+    sig = {
+        "orc_bf16_to_float": (_F, [ctypes.c_uint16]),
+        "orc_bf16_from_float": (ctypes.c_uint16, [_F]),
+        "orc_bf16_from_double": (ctypes.c_uint16, [ctypes.c_double]),
+        "orc_e4m3_value": (ctypes.c_double, [ctypes.c_uint8]),
+        "orc_e4m3_from_float": (ctypes.c_uint8, [_F]),
+        "orc_e2m1_value": (ctypes.c_double, [ctypes.c_uint8]),
+        "orc_ue8m0_value": (ctypes.c_double, [ctypes.c_uint8]),
+        "orc_ue8m0_ceil": (ctypes.c_uint8, [_F]),
+        "orc_exp_spec": (_F, [_F]),
+        "orc_silu_spec": (_F, [_F]),
+        "orc_sigmoid_spec": (_F, [_F]),
+        "orc_glu_oai": (_F, [_F, _F, _F, _F, _F]),
+        "orc_group_quant_row": (None, [_P, _I, _I, _P, _P]),
+        "orc_route_softmax_topk": (None, [_P, _I, _I, _I, _P, _P]),
+        "orc_route_sigmoid_bias_topk": (None, [_P, _P, _I, _I, _I, _P, _P]),
+        "orc_expert_counts": (None, [_P, _L, _I, _P]),
+        "orc_endpoints": (None, [_P, _I, _I, _P, _P]),
+        "orc_scatter": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+        "orc_grouped_gemm": (None, [_P, _P, _I, _I, _P, _I, _I, _P, _P, _I, _P]),
+        "orc_act_quant": (None, [_P, _I, _I, _P, _I, _I, _I, _F, _P, _P, _I]),
+        "orc_combine": (None, [_P, _I, _P, _P, _I, _I, _F, _P]),
+        "orc_ffn_tokens": (None, [_P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _F, _F, _P, _I, _P]),
+        "orc_ffn_dense": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _F, _F, _P]),
+        "orc_decode": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
+                              _I, _F, _F, _F, _P, _P, _P, _P]),
+        "orc_decode_dense": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                    _P, _I, _F, _F, _F, _P]),
+        "orc_num_threads": (_I, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+
+
+def _p(a):
+    """Pointer to a C-contiguous numpy array (or None)."""
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ----------------------------------------------------------------- scalars
+def bf16_to_float(h): return lib().orc_bf16_to_float(int(h))
+def bf16_from_float(f): return lib().orc_bf16_from_float(float(f))
+def bf16_from_double(d): return lib().orc_bf16_from_double(float(d))
+def e4m3_value(c): return lib().orc_e4m3_value(int(c))
+def e4m3_from_float(x): return lib().orc_e4m3_from_float(float(x))
+def e2m1_value(n): return lib().orc_e2m1_value(int(n))
+def ue8m0_value(b): return lib().orc_ue8m0_value(int(b))
+def ue8m0_ceil(s): return lib().orc_ue8m0_ceil(float(s))
+def exp_spec(x): return lib().orc_exp_spec(float(x))
+def silu_spec(x): return lib().orc_silu_spec(float(x))
+def sigmoid_spec(x): return lib().orc_sigmoid_spec(float(x))
+def glu_oai(g, u, alpha, beta, limit): return lib().orc_glu_oai(g, u, alpha, beta, limit)
+def num_threads(): return lib().orc_num_threads()
+
+
+def bf16_to_f32_array(u16):
+    """bf16 bit patterns -> fp32 values (exact)."""
+    return (np.asarray(u16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------------------------ arrays
+def group_quant_row(v, group=128):
+    v = _c(v, np.float32)
+    K = v.shape[0]
+    codes = np.zeros(K, np.uint8)
+    sf = np.zeros((K + group - 1) // group, np.uint8)
+    lib().orc_group_quant_row(_p(v), K, group, _p(codes), _p(sf))
+    return codes, sf
+
+
+def route_softmax_topk(logits, k):
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float32)
+    lib().orc_route_softmax_topk(_p(logits), T, E, k, _p(ids), _p(w))
+    return ids, w
+
+
+def route_sigmoid_bias_topk(logits, bias, k):
+    logits = _c(logits, np.float32)
+    bias = _c(bias, np.float32)
+    T, E = logits.shape
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float32)
+    lib().orc_route_sigmoid_bias_topk(_p(logits), _p(bias), T, E, k, _p(ids), _p(w))
+    return ids, w
+
+
+def expert_counts(ids, E):
+    ids = _c(ids, np.int32)
+    counts = np.zeros(E, np.int32)
+    lib().orc_expert_counts(_p(ids), ids.size, E, _p(counts))
+    return counts
+
+
+def endpoints(counts, A):
+    counts = _c(counts, np.int32)
+    E = counts.shape[0]
+    start = np.zeros(E, np.int32)
+    end = np.zeros(E, np.int32)
+    lib().orc_endpoints(_p(counts), E, A, _p(start), _p(end))
+    return start, end
+
+
+def align4(n):
+    return (n + 3) // 4 * 4
+
+
+def scatter(ids, x_bf16, E, A, cap, fp8_fill=0xAB, sf_fill=None):
+    """Returns expert_ends, src2dst, a_fp8 [cap,H], a_sf [G4, align4(cap)].
+    Non-live rows keep the fill value (the oracle only writes live rows)."""
+    ids = _c(ids, np.int32)
+    x = _c(x_bf16, np.uint16)
+    T, k = ids.shape
+    H = x.shape[1]
+    G4 = (H // 128 + 3) // 4
+    ld = align4(cap)
+    ends = np.zeros(E, np.int32)
+    s2d = np.zeros((T, k), np.int32)
+    a = np.full((cap, H), fp8_fill, np.uint8)
+    sf = np.full((G4, ld), fp8_fill * 0x01010101 if sf_fill is None else sf_fill, np.uint32).view(np.int32)
+    rc = lib().orc_scatter(_p(ids), _p(x), T, k, E, H, A, cap, ld, _p(ends), _p(s2d), _p(a), _p(sf))
+    if rc != 0:
+        raise ValueError("capacity exceeded")
+    return ends, s2d, a, sf
+
+
+def grouped_gemm(a, a_sf, expert_ends, A, w, w_sf, out=None):
+    a = _c(a, np.uint8)
+    a_sf = _c(a_sf, np.int32)
+    ends = _c(expert_ends, np.int32)
+    w = _c(w, np.uint8)
+    w_sf = _c(w_sf, np.uint8)
+    cap, K = a.shape
+    E, N = w.shape[0], w.shape[1]
+    if out is None:
+        out = np.zeros((cap, N), np.uint16)
+    lib().orc_grouped_gemm(_p(a), _p(a_sf), a_sf.shape[1], K, _p(ends), E, A, _p(w), _p(w_sf), N, _p(out))
+    return out
+
+
+def act_quant(gateup, expert_ends, A, clamp=False, limit=0.0, out=None, out_sf=None, fill=0xAB):
+    gateup = _c(gateup, np.uint16)
+    M, I2 = gateup.shape
+    I = I2 // 2
+    G4 = ((I + 127) // 128 + 3) // 4
+    ld = align4(M)
+    if out is None:
+        out = np.full((M, I), fill, np.uint8)
+    if out_sf is None:
+        out_sf = np.full((G4, ld), fill * 0x01010101, np.uint32).view(np.int32)
+    ends = None if expert_ends is None else _c(expert_ends, np.int32)
+    E = 0 if ends is None else ends.shape[0]
+    lib().orc_act_quant(_p(gateup), M, I, _p(ends), E, A, int(bool(clamp)), float(limit), _p(out), _p(out_sf), ld)
+    return out, out_sf
+
+
+def combine(down, topk_w, src2dst, rsf=1.0):
+    down = _c(down, np.uint16)
+    topk_w = _c(topk_w, np.float32)
+    s2d = _c(src2dst, np.int32)
+    T, k = s2d.shape
+    H = down.shape[1]
+    out = np.zeros((T, H), np.uint16)
+    lib().orc_combine(_p(down), H, _p(topk_w), _p(s2d), T, k, float(rsf), _p(out))
+    return out
+
+
+def ffn_tokens(x, ids, topk_w, w13, w13_sf, w2, w2_sf, tokens, clamp=False, limit=0.0, rsf=1.0):
+    x = _c(x, np.uint16)
+    ids = _c(ids, np.int32)
+    topk_w = _c(topk_w, np.float32)
+    tokens = _c(tokens, np.int32)
+    T, H = x.shape
+    k = ids.shape[1]
+    E, I2 = w13.shape[0], w13.shape[1]
+    out = np.zeros((tokens.shape[0], H), np.uint16)
+    lib().orc_ffn_tokens(_p(x), H, I2 // 2, _p(ids), _p(topk_w), k, E, _p(_c(w13, np.uint8)),
+                         _p(_c(w13_sf, np.uint8)), _p(_c(w2, np.uint8)), _p(_c(w2_sf, np.uint8)),
+                         int(bool(clamp)), float(limit), float(rsf), _p(tokens), tokens.shape[0], _p(out))
+    return out
+
+
+def ffn_dense(x, ids, topk_w, w13, w13_sf, w2, w2_sf, clamp=False, limit=0.0, rsf=1.0):
+    x = _c(x, np.uint16)
+    ids = _c(ids, np.int32)
+    topk_w = _c(topk_w, np.float32)
+    T, H = x.shape
+    k = ids.shape[1]
+    E, I2 = w13.shape[0], w13.shape[1]
+    out = np.zeros((T, H), np.uint16)
+    lib().orc_ffn_dense(_p(x), T, H, I2 // 2, _p(ids), _p(topk_w), k, E, _p(_c(w13, np.uint8)),
+                        _p(_c(w13_sf, np.uint8)), _p(_c(w2, np.uint8)), _p(_c(w2_sf, np.uint8)),
+                        int(bool(clamp)), float(limit), float(rsf), _p(out))
+    return out
+
+
+def _decode_args(w):
+    """Returns pointer tuple for a decode weight set dict."""
+    def g(key, dt):
+        return None if w.get(key) is None else _c(w[key], dt)
+    arrs = dict(w_gu=g("w_gu", np.uint8), gu_scale=g("gu_scale", np.float32), gu_sf=g("gu_sf", np.uint8),
+                b_gu=g("b_gu", np.uint16), w_d=g("w_d", np.uint8), d_scale=g("d_scale", np.float32),
+                d_sf=g("d_sf", np.uint8), b_d=g("b_d", np.uint16))
+    return arrs
+
+
+def decode(x, ids, topk_w, weights, wfmt, I, expert_start=0, n_local=None, interleaved=True,
+           alpha=1.702, beta=1.0, limit=7.0, fill=0x7FC0):
+    """Sparse decode path. Returns (y1 [T,k,2I], act [T*k,I], y2 [T,k,H], out [T,H]);
+    slots of non-local experts keep `fill` (bf16 NaN by default) in y1/act/y2."""
+    x = _c(x, np.uint16)
+    ids = _c(ids, np.int32)
+    topk_w = _c(topk_w, np.float32)
+    T, H = x.shape
+    k = ids.shape[1]
+    a = _decode_args(weights)
+    if n_local is None:
+        n_local = a["b_gu"].shape[0]
+    y1 = np.full((T, k, 2 * I), fill, np.uint16)
+    act = np.full((T * k, I), fill, np.uint16)
+    y2 = np.full((T, k, H), fill, np.uint16)
+    out = np.zeros((T, H), np.uint16)
+    lib().orc_decode(_p(x), T, H, I, _p(ids), _p(topk_w), k, expert_start, n_local, wfmt,
+                     _p(a["w_gu"]), _p(a["gu_scale"]), _p(a["gu_sf"]), _p(a["b_gu"]),
+                     _p(a["w_d"]), _p(a["d_scale"]), _p(a["d_sf"]), _p(a["b_d"]),
+                     int(bool(interleaved)), float(alpha), float(beta), float(limit),
+                     _p(y1), _p(act), _p(y2), _p(out))
+    return y1, act, y2, out
+
+
+def decode_dense(x, ids, topk_w, weights, wfmt, I, expert_start=0, n_local=None, interleaved=True,
+                 alpha=1.702, beta=1.0, limit=7.0):
+    x = _c(x, np.uint16)
+    ids = _c(ids, np.int32)
+    topk_w = _c(topk_w, np.float32)
+    T, H = x.shape
+    k = ids.shape[1]
+    a = _decode_args(weights)
+    if n_local is None:
+        n_local = a["b_gu"].shape[0]
+    out = np.zeros((T, H), np.uint16)
+    lib().orc_decode_dense(_p(x), T, H, I, _p(ids), _p(topk_w), k, expert_start, n_local, wfmt,
+                           _p(a["w_gu"]), _p(a["gu_scale"]), _p(a["gu_sf"]), _p(a["b_gu"]),
+                           _p(a["w_d"]), _p(a["d_scale"]), _p(a["d_sf"]), _p(a["b_d"]),
+                           int(bool(interleaved)), float(alpha), float(beta), float(limit), _p(out))
+    return out
