@@ -1,0 +1,366 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE expert FFN layer on GB300.
+
+One step = one pass of the whole hot path over one batch: routing + aligned
+prefix-sum endpoints + token scatter with input quantisation
+(moe_route_scatter), grouped GEMM1, live-row SiLU*mul + e4m3/UE8M0 quant,
+grouped GEMM2, top-k weighted combine, on the DeepSeek-style W4A8 layer
+(E=32 experts, top-6, T=4096 tokens, hidden 4096, intermediate 2048, MXFP4
+weights, capacity 28,672 rows). Synthetic seeded inputs; weights resident.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica of the layer on its own
+GPU (the path has no exchange step on one GPU); value = routed rows of all
+ranks / max-over-ranks time. `--impl reference` times the CPU oracle (the
+plain restatement of the method) on the host cores on bounded samples of the
+same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE FFN μs/layer & routed rows/s; act-quant μs; % of TC/HBM roofline"
+UNIT = "routed rows/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extras", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def workload_config(cfg):
+    return {"workload": cfg.name, "T": cfg.T, "E": cfg.E, "k": cfg.k, "H": cfg.H, "I": cfg.I, "A": cfg.A,
+            "cap": cfg.cap, "routing": "softmax top-k, renormalised", "weights": "MXFP4 e2m1 + UE8M0 group 32",
+            "activations": "e4m3 + UE8M0 group 128",
+            "l2": "inputs larger than L2: about 0.9 GB touched per step (weights 0.43 GB, capacity buffers)"}
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.device = device
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ CPU baseline
+def oracle_sample(cfg, inp, n_tokens, seed=0):
+    """Time the oracle (routing + the layer for n_tokens sampled tokens)."""
+    import numpy as np
+    import oracle as orc
+
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(cfg.T, n_tokens, replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    ids, w = orc.route_softmax_topk(inp.logits[toks], cfg.k)
+    full_ids = np.zeros((cfg.T, cfg.k), np.int32)
+    full_w = np.zeros((cfg.T, cfg.k), np.float32)
+    full_ids[toks], full_w[toks] = ids, w
+    orc.ffn_tokens(inp.x, full_ids, full_w, inp.w13, inp.w13_sf, inp.w2, inp.w2_sf, toks)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, inp, budget_s=15.0):
+    import oracle as orc
+
+    t1 = oracle_sample(cfg, inp, 2, seed=1)
+    n = int(max(2, min(cfg.T, budget_s / max(t1 / 2, 1e-6))))
+    t = oracle_sample(cfg, inp, n, seed=2)
+    return {"value": n * cfg.k / t, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
+            "sample": "%d of %d tokens (%d routed rows) of the same layer: oracle routing + per-token "
+                      "FFN (fp64 GEMMs) in %.2f s" % (n, cfg.T, n * cfg.k, t)}
+
+
+# --------------------------------------------------------------- reference
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from moe_expert_ffn_scatter_gb300 import synth
+    import oracle as orc
+
+    cfg = synth.DEEPSEEK
+    inp = synth.ffn_inputs(cfg)
+    t1 = oracle_sample(cfg, inp, 2, seed=1)
+    per_tok = t1 / 2
+    n = int(max(1, min(64, 4.0 / max(per_tok, 1e-6))))  # about 4 s of CPU work per step
+    for i in range(args.warmup):
+        oracle_sample(cfg, inp, n, seed=100 + i)
+    times = [oracle_sample(cfg, inp, n, seed=1000 + i) for i in range(args.steps)]
+    total = sum(times)
+    value = args.steps * n * cfg.k / total
+    conf = workload_config(cfg)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": conf,
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
+                             "sample": "%d tokens (%d routed rows) of %d per step" % (n, n * cfg.k, cfg.T)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- ours
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from moe_expert_ffn_scatter_gb300 import binding as B
+    from moe_expert_ffn_scatter_gb300 import synth
+    from moe_expert_ffn_scatter_gb300.layer import MoEFFNLayer
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+
+    cfg = synth.DEEPSEEK
+    inp = synth.ffn_inputs(cfg)
+    ctx = B.Context(local)
+    layer = MoEFFNLayer(ctx, T=cfg.T, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I, A=cfg.A, cap=cfg.cap)
+    layer.load_weights(inp.w13, inp.w13_sf, inp.w2, inp.w2_sf)
+    x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).cuda()
+    logits = torch.from_numpy(inp.logits).cuda()
+    stream = torch.cuda.current_stream()
+    L = layer
+    ld = synth.align4(cfg.cap)
+
+    def step(ev=None):
+        if ev is not None: ev[0].record(stream)
+        L.route_scatter(x, logits, stream=stream)
+        if ev is not None: ev[1].record(stream)
+        B.moe_grouped_gemm(ctx, L.a_fp8, L.a_sf, ld, L.expert_ends, cfg.E, cfg.A, cfg.cap, L.w13, L.w13_sf,
+                           L.w_format, 2 * cfg.I, cfg.H, L.gateup, stream=stream)
+        if ev is not None: ev[2].record(stream)
+        B.moe_act_quant(ctx, L.gateup, L.act_fp8, L.act_sf, L.expert_ends, cfg.E, cfg.A, cfg.cap, cfg.I,
+                        stream=stream)
+        if ev is not None: ev[3].record(stream)
+        B.moe_grouped_gemm(ctx, L.act_fp8, L.act_sf, ld, L.expert_ends, cfg.E, cfg.A, cfg.cap, L.w2, L.w2_sf,
+                           L.w_format, cfg.H, cfg.I, L.down, stream=stream)
+        if ev is not None: ev[4].record(stream)
+        B.moe_combine(ctx, L.down, cfg.H, L.topk_w, L.src2dst, cfg.T, cfg.k, cfg.rsf, L.out, stream=stream)
+        if ev is not None: ev[5].record(stream)
+
+    kernels_per_step = 3 + 1 + 1 + 1 + 1
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if B.moe_get_device_error(ctx) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if pg: pg.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if pg: pg.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if pg:
+        tt = torch.tensor([total_ms], device="cuda")
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    if B.moe_get_device_error(ctx) != 0:
+        raise RuntimeError("device error during the timed region")
+    names = ["route_scatter", "gemm1", "act_quant", "gemm2", "combine"]
+    per = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)) / args.steps
+           for j, n in enumerate(names)}
+    ms_step = total_ms / args.steps
+    R = cfg.R
+    value = world * R * args.steps / (total_ms / 1e3)
+
+    pk, pk_kind = peaks()
+    fp8_peak = 2.0 * pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+    hbm = pk["hbm_gbs"]
+    g1_flop = 2.0 * R * (2 * cfg.I) * cfg.H
+    g2_flop = 2.0 * R * cfg.H * cfg.I
+    g1_tf = g1_flop / (per["gemm1"] * 1e-3) / 1e12
+    g2_tf = g2_flop / (per["gemm2"] * 1e-3) / 1e12
+    # algorithmic bytes of the HBM-bound steps (live rows only)
+    G_H = cfg.H // 128
+    rs_bytes = cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4 + R * (cfg.H + 4 * ((G_H + 3) // 4)) + R * 8 + cfg.T * cfg.k * 8
+    aq_bytes = R * (2 * cfg.I * 2 + cfg.I + 4 * ((cfg.I // 128 + 3) // 4))
+    cb_bytes = R * cfg.H * 2 + cfg.T * cfg.H * 2 + cfg.T * cfg.k * 8
+    kern = {
+        "route_scatter": {"us": 1e3 * per["route_scatter"], "gbs": rs_bytes / (per["route_scatter"] * 1e-3) / 1e9},
+        "gemm1": {"us": 1e3 * per["gemm1"], "tflops": g1_tf, "frac_of_fp8_peak": g1_tf / fp8_peak},
+        "act_quant": {"us": 1e3 * per["act_quant"], "gbs": aq_bytes / (per["act_quant"] * 1e-3) / 1e9},
+        "gemm2": {"us": 1e3 * per["gemm2"], "tflops": g2_tf, "frac_of_fp8_peak": g2_tf / fp8_peak},
+        "combine": {"us": 1e3 * per["combine"], "gbs": cb_bytes / (per["combine"] * 1e-3) / 1e9},
+    }
+    roofline = {"bound": "tensor", "kernel": "gemm1 (grouped_gemm_kernel, tcgen05 mxf8f6f4 block-scaled)",
+                "achieved": g1_tf, "peak": fp8_peak, "unit": "TFLOP/s", "frac": g1_tf / fp8_peak,
+                "traffic": None,
+                "peak_note": "%s sustained bf16 x 2 (dense FP8/FP6/FP4-in-mxf8f6f4 rate is twice bf16)" % pk_kind,
+                "algorithmic": "2*R*2I*H = %.1f GFLOP per launch over live rows only" % (g1_flop / 1e9)}
+
+    # ---------------------------------------------- end to end (host buffers)
+    e2e = None
+    if True:
+        xh = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+        lh = torch.from_numpy(inp.logits).pin_memory()
+        oh = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+        xd = torch.empty_like(x)
+        lgd = torch.empty_like(logits)
+
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
+            lgd.copy_(lh, non_blocking=True)
+            out = layer.forward(xd, lgd, stream=stream)
+            oh.copy_(out, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        if pg: pg.barrier()
+        torch.cuda.synchronize()
+        a0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a0.elapsed_time(a1)
+        if pg:
+            tt = torch.tensor([e_ms], device="cuda")
+            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": world * R * args.steps / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": xh.numel() * 2 + lh.numel() * 4, "d2h_bytes_per_step": oh.numel() * 2,
+               "ms_per_step": e_ms / args.steps,
+               "api": "MoEFFNLayer.forward: moe_route_scatter + moe_ffn_forward, pinned host x/logits in, out back"}
+
+    extras = {}
+    if not args.no_extras:
+        extras["act_quant_microbench"] = actq_microbench(ctx, B, synth, torch, np, hbm)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "us_per_layer": 1e3 * ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e2m1 (fp32 accumulate)", "data": "synthetic",
+            "config": workload_config(cfg), "roofline": roofline, "kernels": kern, "clocks": clk, "e2e": e2e,
+            "gpu_launches": kernels_per_step * args.steps}
+    line.update(extras)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def actq_microbench(ctx, B, synth, torch, np, hbm, reps=50):
+    """Live-row act-quant at 3,072 live / 28,672 allocated rows (I = 2,048),
+    the all-live full buffer through the endpoint path, and the dense launch."""
+    rows, I, E = synth.ACTQ_ROWS, synth.ACTQ_I, synth.ACTQ_E
+    res = {}
+    for name, full in (("live", False), ("full", True)):
+        gu, counts = synth.actq_inputs(full=full)
+        g = torch.from_numpy(gu.view(np.int16)).view(torch.bfloat16).cuda()
+        out = torch.empty((rows, I), dtype=torch.uint8, device="cuda")
+        sf = torch.empty((I // 512, rows), dtype=torch.int32, device="cuda")
+        ends = torch.empty((E,), dtype=torch.int32, device="cuda")
+        B.moe_expert_ends_from_counts(ctx, torch.from_numpy(counts).cuda(), 128, ends)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        variants = [(name, ends)] + ([("dense", None)] if full else [])
+        for vname, e in variants:
+            ts = []
+            for i in range(reps + 3):
+                flush.fill_(i & 0xFF)  # evict the inputs from L2 between launches
+                s0 = torch.cuda.Event(enable_timing=True)
+                s1 = torch.cuda.Event(enable_timing=True)
+                s0.record()
+                B.moe_act_quant(ctx, g, out, sf, e, E, 128, rows, I)
+                s1.record()
+                torch.cuda.synchronize()
+                if i >= 3:
+                    ts.append(s0.elapsed_time(s1))
+            live_rows = int(counts.sum()) if e is not None else rows
+            nbytes = live_rows * (2 * I * 2 + I + 4 * (I // 512))
+            us = 1e3 * statistics.median(ts)
+            res[vname] = {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9, "frac_of_hbm": nbytes / (us * 1e-6) / 1e9 / hbm,
+                          "live_rows": live_rows}
+    if "full" in res and "dense" in res:
+        res["full_over_dense"] = res["full"]["us"] / res["dense"]["us"]
+    return res
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

@@ -1,0 +1,311 @@
+/*
+ * moe_gb300.h -- C ABI of the GB300 (sm_103a) routed MoE expert FFN library.
+ *
+ * The hot path: top-k routing -> token scatter that writes aligned prefix-sum
+ * expert endpoints -> grouped GEMM1 (w13, gate/up) -> SiLU*mul with e4m3
+ * quantisation and packed UE8M0 scales over live rows only -> grouped GEMM2
+ * (w2, down) -> top-k weighted combine; plus the small-batch sparse GEMV
+ * decode variant.
+ *
+ * Sources, cited by tag and the page's own section:
+ *  [LR] "Blackwell FP4 MoE：把 live-row 边界贯穿整个 FFN"
+ *  [DG] "Blackwell 上的 DeepGEMM FusedMoE（sglang）"
+ *  [SD] "Phase 20: Sparse MoE Decode — 只算被路由到的专家"
+ *  [KM] "kimi3_pro6000_sglang_sm120_flashinfer_mxfp4" experiment log
+ *
+ * Conventions (all entry points)
+ *  - Plain C: pointers and sizes only. Pointers named in argument structs are
+ *    DEVICE pointers unless marked "host". Row-major unless stated.
+ *  - Ownership: the caller allocates and owns every buffer, including the
+ *    capacity workspaces; the library never allocates on the hot path, keeps
+ *    no pointer after a call returns and never returns aliases. (Only
+ *    moe_ctx_create allocates: the context and its 4-byte device error word.)
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and enqueue a fixed launch structure that depends on the
+ *    sizes only, never on routing counts: every call may be captured into a
+ *    CUDA graph and replayed while the device contents change ([LR] §3).
+ *  - Status: 0 on success; a negative MOE_ERR_* code otherwise. Arguments are
+ *    validated on the host before anything is enqueued; an invalid argument
+ *    enqueues nothing. Anomalies that only the device can see (an expert id
+ *    out of range, a capacity overflow, a pipeline wait that ran out) set bits
+ *    in the context's device error word (moe_get_device_error); nothing traps.
+ *  - Number formats: bf16 as uint16 bit patterns; e4m3 codes as uint8 (OCP
+ *    FP8 E4M3, largest finite 448); e2m1 packed two per byte with the LOW
+ *    nibble holding the even index; UE8M0 scale bytes b meaning 2^(b-127).
+ *  - "Packed activation scales" (ASF): int32 array [ceil(G/4)][ld] with
+ *    ld = align4(rows) ("MN-major"): byte (g % 4) of word [g/4][row] is the
+ *    scale of the row's 128-column group g; unused bytes of the last word of a
+ *    written row are 0 ([DG] §2.4.1 and 附录 A: 4 uint8 per int32 along K,
+ *    MN-major).
+ *  - Endpoints: expert_ends[e] is the real (unaligned) end of expert e's rows;
+ *    start[0] = 0, start[e] = align_up(expert_ends[e-1], A) ([LR] §2). Rows
+ *    outside [start[e], expert_ends[e]) are padding: no kernel writes them.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef struct moe_ctx moe_ctx;
+typedef void* moe_stream_t; /* cudaStream_t */
+
+/* status codes */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)
+#define MOE_ERR_CAPACITY (-2)
+#define MOE_ERR_UNSUPPORTED (-3)
+#define MOE_ERR_CUDA (-4)
+#define MOE_ERR_DEVICE (-5)
+
+/* device error bits */
+#define MOE_DEVERR_EXPERT_ID 0x1u      /* an expert id outside [0, E) reached a kernel that needs it */
+#define MOE_DEVERR_CAPACITY 0x2u       /* expert_ends[E-1] > cap seen on the device */
+#define MOE_DEVERR_WAIT_TIMEOUT 0x4u   /* a bounded pipeline wait in a GEMM ran out */
+#define MOE_DEVERR_ENDPOINTS 0x8u      /* expert_ends not non-decreasing / beyond capacity */
+
+/* routing modes */
+#define MOE_ROUTE_SOFTMAX_TOPK 0       /* softmax -> top-k -> renormalise */
+#define MOE_ROUTE_SIGMOID_BIAS_TOPK 1  /* select on sigmoid + bias, weights from unbiased sigmoid */
+#define MOE_ROUTE_PRECOMPUTED 2        /* topk_ids given by the caller */
+
+/* activation kinds between the GEMMs */
+#define MOE_ACT_SILU 0                 /* h = silu(gate) * up */
+#define MOE_ACT_SILU_CLAMP 1           /* gate = min(gate, L); up = clamp(up, -L, L) first */
+
+/* decode weight formats */
+#define MOE_WFMT_FP8_PER_EXPERT 0      /* e4m3 [E,N,K] + fp32 scale [E] */
+#define MOE_WFMT_MXFP4_G32 1           /* e2m1 [E,N,K/2] + UE8M0 [E,N,K/32] */
+
+/* decode GLU layouts of the gate_up output */
+#define MOE_GLU_HALVES 0               /* [gate_0..gate_{I-1}, up_0..up_{I-1}] */
+#define MOE_GLU_INTERLEAVED 1          /* [gate_0, up_0, gate_1, up_1, ...] */
+
+/* ------------------------------------------------------------- context
+ * moe_ctx_create: binds `device`, reads its SM count, allocates the 4-byte
+ *   device error word. Returns MOE_ERR_CUDA if the device is unusable.
+ * moe_ctx_destroy: frees the context (NULL is ignored).
+ * moe_get_device_error: synchronises `stream`, reads the error word into
+ *   *bits (host) and clears it. */
+MOE_API int moe_ctx_create(moe_ctx** out, int device);
+MOE_API int moe_ctx_destroy(moe_ctx* ctx);
+MOE_API int moe_get_device_error(moe_ctx* ctx, uint32_t* bits, moe_stream_t stream);
+MOE_API const char* moe_status_string(int status);
+MOE_API int moe_version(void);
+
+/* ---------------------------------------------------- endpoints alone
+ * expert_ends[e] from per-expert live-row counts[e] (both int32 [E], device):
+ * start[0] = 0, start[e] = align_up(end[e-1], A), end[e] = start[e] + count[e]
+ * ([LR] §2, "概念伪代码"). One block; E <= 65536. */
+MOE_API int moe_expert_ends_from_counts(moe_ctx* ctx, const int32_t* counts, int E, int A,
+                                        int32_t* expert_ends, moe_stream_t stream);
+
+/* ------------------------------------------------------ route + scatter
+ * [LR] §2 ("scatter 在现有步骤内写出 int32 endpoint"), [DG] §2.2.4 (compact
+ * layout: per-token-group quantisation then ep_scatter into expert
+ * segments), [DG] 附录 C (ep_scatter, src2dst).
+ *
+ * 1. Routing (unless PRECOMPUTED): per token, the k experts with the largest
+ *    score, ties to the lower expert index, in descending order.
+ *    SOFTMAX_TOPK: score = logit; weight_j = exp(l_j - l_max) / sum over the
+ *    selected slots ([DG] §2.2.1). SIGMOID_BIAS_TOPK: score = sigmoid(l) +
+ *    corr_bias; weight_j = sigmoid(l_j) / sum of the selected sigmoids
+ *    ([KM] Phase 1, topk.py row). exp is the library's exp specification
+ *    (Cody & Waite reduction plus a degree-7 Taylor series in fixed fp32
+ *    steps, written out in csrc/common.cuh).
+ * 2. Endpoints from the per-expert route counts (ids outside [0,E) skipped).
+ * 3. Route (t, j) of expert e gets row start[e] + number of earlier routes
+ *    (row-major (t, j) order) to e; src2dst[t,j] = that row, or -1.
+ * 4. Each token row x[t] is quantised once (group 128, UE8M0, e4m3) and its
+ *    codes/scales copied to each of its rows of a_fp8 / a_sf.
+ *
+ * Arguments (device pointers):
+ *  logits [T,E] fp32 (ignored if PRECOMPUTED); corr_bias [E] fp32
+ *  (SIGMOID_BIAS only, else NULL); topk_ids [T,k] int32 (written; read if
+ *  PRECOMPUTED); topk_w [T,k] fp32 (written; ignored if PRECOMPUTED);
+ *  x [T,H] bf16; a_fp8 [cap,H] e4m3; a_sf ASF [ceil(H/512)][align4(cap)];
+ *  expert_ends [E] int32 (written); src2dst [T,k] int32 (written);
+ *  workspace: moe_route_scatter_workspace_size(T,E,k) bytes of scratch,
+ *  16-byte aligned, contents need not be initialised.
+ * Sizes: T >= 0 (T == 0 writes expert_ends = 0 and nothing else),
+ *  1 <= E <= 4096 (E <= 1024 for the two routing modes), 1 <= k <= min(E, 32),
+ *  H % 128 == 0, A >= 1, cap >= T*k + E*(A-1). Logits must be finite.
+ * Errors: MOE_ERR_INVALID_ARG (null pointer, bad size), MOE_ERR_CAPACITY
+ *  (cap below the bound above). */
+typedef struct moe_route_args {
+    int32_t routing_mode;
+    const float* logits;
+    const float* corr_bias;
+    int32_t* topk_ids;
+    float* topk_w;
+    const uint16_t* x;
+    uint8_t* a_fp8;
+    int32_t* a_sf;
+    int32_t* expert_ends;
+    int32_t* src2dst;
+    void* workspace;
+    size_t workspace_bytes;
+    int32_t T, E, k, H, A, cap;
+} moe_route_args;
+
+MOE_API size_t moe_route_scatter_workspace_size(int T, int E, int k);
+MOE_API int moe_route_scatter(moe_ctx* ctx, const moe_route_args* args, moe_stream_t stream);
+
+/* ------------------------------------------------------- weight prepare
+ * Load-time (not on the hot path) re-layout of MXFP4 weights for the grouped
+ * GEMM ([DG] §2.1.2 path A: weight scales are transformed once at load into
+ * the layout the GEMM consumes). Input: packed e2m1 w_in [E][N][K/2] and
+ * canonical UE8M0 bytes sf_in [E][N][K/32]. Output scales: uint32 words
+ * sf_out [E][K/128][N], word (e, c, n) holding the four scales of k-blocks
+ * 4c..4c+3 of row n, block 4c in the low byte. Output weights w_out:
+ *   MOE_GEMM_W_E2M1: packed e2m1 [E][N][K/2] (a copy; w_out may equal w_in)
+ *   MOE_GEMM_W_E4M3: the same values re-encoded exactly as e4m3 [E][N][K]
+ *                    (twice the bytes; [DG] §2.1.2 path B does the same
+ *                    lossless widening of e2m1 to e4m3)
+ * Requires K % 128 == 0; w_out must not overlap sf_out. */
+#define MOE_GEMM_W_E2M1 0
+#define MOE_GEMM_W_E4M3 1
+MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t* sf_in, int E, int N,
+                                int K, int w_format, uint8_t* w_out, uint32_t* sf_out,
+                                moe_stream_t stream);
+
+/* ------------------------------------------------------- grouped GEMM
+ * One block-scaled grouped GEMM over live rows ([LR] §2: FC1/FC2 take the
+ * endpoint layout; [DG] §2.3.1, recipes (1,128) for the e4m3 activations and
+ * (1,32) for the MXFP4 weights):
+ *   out[r, n] = bf16( sum_k e4m3(a[r,k]) 2^(sa(r,k/128)-127)
+ *                           * e2m1(w[e,n,k]) 2^(sw(e,n,k/32)-127) )
+ * for r in [start[e], expert_ends[e]) only; fp32 accumulation in tensor
+ * memory (tcgen05, sm_103a). a [cap,K] e4m3; a_sf ASF [ceil(K/512)][ld_sf];
+ * w, w_sf prepared by moe_prepare_weights in format w_format ([E][N][K/2]
+ * packed e2m1 or [E][N][K] e4m3; scales [E][K/128][N]); out [cap,N] bf16.
+ * Requires K % 128 == 0, N % 256 == 0, cap % 128 == 0, A == 128,
+ * ld_sf >= cap, ld_sf % 4 == 0, 32-byte aligned w, 16-byte aligned a. */
+MOE_API int moe_grouped_gemm(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf, int ld_sf,
+                             const int32_t* expert_ends, int E, int A, int cap, const uint8_t* w,
+                             const uint32_t* w_sf, int w_format, int N, int K, uint16_t* out,
+                             moe_stream_t stream);
+
+/* ---------------------------------------------------- activation quant
+ * [LR] §2-3 (live-row activation kernel: 3-D grid with the expert on axis z,
+ * grid-stride loop over [start[e], end[e]), padding left unwritten; a dense
+ * launch over all rows when no endpoints are given), [DG] §2.4.1 (fused
+ * SiLU*mul + per-token-group quant, UE8M0 packed MN-major output;
+ * silu_mul_keep_fp32: SiLU result kept in fp32).
+ *   gate = gateup[r, j], up = gateup[r, I + j]
+ *   SILU_CLAMP: gate = min(gate, L), up = clamp(up, -L, L) ([DG] §2.4.1)
+ *   h = silu(gate) * up in fp32 (silu(g) = g / (1 + exp(-g)), the library's
+ *   exp specification); per 128 columns: amax, b = ceil_pow2(amax / 448),
+ *   code = e4m3_rne_satfinite(h * 2^(127-b)); amax infinite -> b = 0xFE.
+ * gateup [M_alloc, 2I] bf16; out [M_alloc, I] e4m3; out_sf ASF
+ * [ceil(I/512)][align4(M_alloc)]; expert_ends [E] or NULL (dense fallback:
+ * every row of [0, M_alloc)). Requires I % 128 == 0, A >= 1. */
+typedef struct moe_act_params {
+    int32_t kind;  /* MOE_ACT_* */
+    float limit;   /* L for SILU_CLAMP */
+} moe_act_params;
+
+MOE_API int moe_act_quant(moe_ctx* ctx, const uint16_t* gateup, uint8_t* out, int32_t* out_sf,
+                          const int32_t* expert_ends, int E, int A, int M_alloc, int I,
+                          const moe_act_params* act, moe_stream_t stream);
+
+/* ------------------------------------------------------------- combine
+ * [DG] §2.6.1 (post_reorder): out[t] = bf16( rsf * sum over j = 0..k-1 with
+ * src2dst[t,j] >= 0 of topk_w[t,j] * down[src2dst[t,j]] ), accumulated in
+ * fp32, one fused multiply-add per slot in slot order. down [rows,H] bf16
+ * (rows referenced by src2dst only); topk_w/src2dst [T,k]; out [T,H] bf16.
+ * Requires H % 8 == 0. */
+MOE_API int moe_combine(moe_ctx* ctx, const uint16_t* down, int H, const float* topk_w,
+                        const int32_t* src2dst, int T, int k, float rsf, uint16_t* out,
+                        moe_stream_t stream);
+
+/* ----------------------------------------------------------- FFN forward
+ * GEMM1 -> act-quant -> GEMM2 -> combine on one stream, all driven by the
+ * device-side expert_ends ([LR] §2 "FC1(endpoint) → SiLU+mul+quant(endpoint)
+ * → FC2(endpoint)"). Inputs: a_fp8/a_sf/expert_ends/src2dst as written by
+ * moe_route_scatter; topk_w [T,k]; w13 [E][2I][H/2] and w2 [E][H][I/2]
+ * prepared with their scales by moe_prepare_weights. Workspaces (caller
+ * owned, fixed capacity, contents need not be initialised): gateup
+ * [cap,2I] bf16, act_fp8 [cap,I], act_sf ASF [ceil(I/512)][align4(cap)],
+ * down [cap,H] bf16. Output out [T,H] bf16. Requires H % 256 == 0,
+ * I % 128 == 0, 2I % 256 == 0, A == 128, cap % 128 == 0. */
+typedef struct moe_ffn_args {
+    const uint8_t* a_fp8;
+    const int32_t* a_sf;
+    const int32_t* expert_ends;
+    const uint8_t* w13;
+    const uint32_t* w13_sf;
+    const uint8_t* w2;
+    const uint32_t* w2_sf;
+    uint16_t* gateup;
+    uint8_t* act_fp8;
+    int32_t* act_sf;
+    uint16_t* down;
+    const float* topk_w;
+    const int32_t* src2dst;
+    uint16_t* out;
+    int32_t T, E, k, H, I, A, cap;
+    int32_t w_format; /* MOE_GEMM_W_*, the format both w13 and w2 were prepared in */
+    moe_act_params act;
+    float rsf;
+} moe_ffn_args;
+
+MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* args, moe_stream_t stream);
+
+/* ------------------------------------------------ sparse decode GEMV
+ * [SD] §3: per (token, slot) whose expert e is local (expert_start <= e <
+ * expert_start + num_local_experts), block-uniformly read from topk_ids on
+ * the device:
+ *   y1[t,j] = W_gu[e] x[t] (* scale) + b_gu[e]            bf16 [T,k,2I]
+ *   act[t*k+j] = GLU(y1[t,j])                             bf16 [T*k, I]
+ *   y2[t,j] = W_d[e] act[t*k+j] (* scale) + b_d[e]        bf16 [T,k,H]
+ *   out[t] = bf16( sum over local slots, in slot order, of topk_w * y2 )
+ * Slots of non-local experts are never written and are skipped in the sum,
+ * never multiplied by zero ([SD] §3 "两个容易写错的安全点").
+ * GLU: g = min(g, L), u = clamp(u, -L, L) (L <= 0: no clamp),
+ *   act = (g * sigmoid(alpha g)) * (u + beta); layout HALVES or INTERLEAVED.
+ * Weights (local expert index lid = e - expert_start):
+ *   FP8_PER_EXPERT: w_gu [n_local][2I][H] e4m3, w_gu_scale [n_local] fp32,
+ *                   w_d [n_local][H][I], w_d_scale [n_local]
+ *   MXFP4_G32:      w_gu [n_local][2I][H/2], w_gu_sf [n_local][2I][H/32],
+ *                   w_d [n_local][H][I/2], w_d_sf [n_local][H][I/32]
+ *   b_gu [n_local][2I] bf16, b_d [n_local][H] bf16.
+ * Requires H % 32 == 0, I % 32 == 0, T <= 64, k <= 32. */
+typedef struct moe_decode_args {
+    const uint16_t* x;
+    const int32_t* topk_ids;
+    const float* topk_w;
+    int32_t expert_start, num_local_experts, wfmt;
+    const uint8_t* w_gu;
+    const float* w_gu_scale;
+    const uint8_t* w_gu_sf;
+    const uint16_t* b_gu;
+    const uint8_t* w_d;
+    const float* w_d_scale;
+    const uint8_t* w_d_sf;
+    const uint16_t* b_d;
+    int32_t glu_layout;
+    float glu_alpha, glu_beta, glu_limit;
+    uint16_t* y1;
+    uint16_t* act;
+    uint16_t* y2;
+    uint16_t* out;
+    int32_t T, H, I, k;
+} moe_decode_args;
+
+MOE_API int moe_sparse_gemv_decode(moe_ctx* ctx, const moe_decode_args* args, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

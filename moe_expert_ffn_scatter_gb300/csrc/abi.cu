@@ -1,0 +1,255 @@
+// abi.cu -- the exported C entry points: context, argument validation and
+// the launch sequence of each call. See include/moe_gb300.h for the contract.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include "../../include/moe_gb300.h"
+#include "kernels.h"
+
+struct moe_ctx {
+  int device;
+  int num_sms;
+  uint32_t* d_err;
+  moe::EncodeTiledFn encode;
+};
+
+namespace {
+
+inline cudaStream_t S(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+inline bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+inline long align4l(long n) { return (n + 3) / 4 * 4; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Every call runs on the context's device.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+MOE_API int moe_version(void) { return 10000; }
+
+MOE_API const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_CAPACITY: return "capacity below the routed rows plus alignment gaps";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size or device";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE: return "device-side error";
+    default: return "unknown status";
+  }
+}
+
+MOE_API int moe_ctx_create(moe_ctx** out, int device) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return MOE_ERR_CUDA;
+  DeviceGuard g(device);
+  if (!g.ok) return MOE_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MOE_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
+  moe_ctx* c = static_cast<moe_ctx*>(calloc(1, sizeof(moe_ctx)));
+  if (!c) return MOE_ERR_CUDA;
+  c->device = device;
+  c->num_sms = prop.multiProcessorCount;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    free(c);
+    return MOE_ERR_CUDA;
+  }
+  c->encode = reinterpret_cast<moe::EncodeTiledFn>(fn);
+  if (cudaMalloc(&c->d_err, sizeof(uint32_t)) != cudaSuccess) {
+    free(c);
+    return MOE_ERR_CUDA;
+  }
+  if (moe::init_grouped_gemm() != cudaSuccess || cudaMemset(c->d_err, 0, sizeof(uint32_t)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(c->d_err);
+    free(c);
+    return MOE_ERR_CUDA;
+  }
+  *out = c;
+  return MOE_OK;
+}
+
+MOE_API int moe_ctx_destroy(moe_ctx* ctx) {
+  if (!ctx) return MOE_OK;
+  DeviceGuard g(ctx->device);
+  cudaFree(ctx->d_err);
+  free(ctx);
+  return MOE_OK;
+}
+
+MOE_API int moe_get_device_error(moe_ctx* ctx, uint32_t* bits, moe_stream_t stream) {
+  if (!ctx || !bits) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  uint32_t h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, ctx->d_err, sizeof(uint32_t), cudaMemcpyDeviceToHost, S(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(S(stream));
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d_err, 0, sizeof(uint32_t), S(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(S(stream));
+  *bits = h;
+  return cuda_status(e);
+}
+
+MOE_API int moe_expert_ends_from_counts(moe_ctx* ctx, const int32_t* counts, int E, int A,
+                                        int32_t* expert_ends, moe_stream_t stream) {
+  if (!ctx || !counts || !expert_ends || E < 1 || E > 65536 || A < 1) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  return cuda_status(moe::launch_expert_ends(counts, E, A, expert_ends, ctx->d_err, S(stream)));
+}
+
+MOE_API size_t moe_route_scatter_workspace_size(int T, int E, int k) {
+  if (T < 0 || E < 1 || k < 1) return 0;
+  return moe::route_scatter_ws_bytes(T, E, k);
+}
+
+MOE_API int moe_route_scatter(moe_ctx* ctx, const moe_route_args* a, moe_stream_t stream) {
+  if (!ctx || !a) return MOE_ERR_INVALID_ARG;
+  if (a->T < 0 || a->E < 1 || a->E > 4096 || a->k < 1 || a->k > 32 || a->k > a->E || a->H < 128 ||
+      a->H % 128 != 0 || a->A < 1 || a->cap < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (a->routing_mode != MOE_ROUTE_SOFTMAX_TOPK && a->routing_mode != MOE_ROUTE_SIGMOID_BIAS_TOPK &&
+      a->routing_mode != MOE_ROUTE_PRECOMPUTED)
+    return MOE_ERR_INVALID_ARG;
+  if (a->routing_mode != MOE_ROUTE_PRECOMPUTED && (a->E > 1024 || !a->logits || !a->topk_w))
+    return MOE_ERR_INVALID_ARG;
+  if (a->routing_mode == MOE_ROUTE_SIGMOID_BIAS_TOPK && !a->corr_bias) return MOE_ERR_INVALID_ARG;
+  if (!a->topk_ids || !a->expert_ends || !a->workspace) return MOE_ERR_INVALID_ARG;
+  if (a->T > 0 && (!a->x || !a->a_fp8 || !a->a_sf || !a->src2dst)) return MOE_ERR_INVALID_ARG;
+  if (a->workspace_bytes < moe::route_scatter_ws_bytes(a->T, a->E, a->k) || !al(a->workspace, 16))
+    return MOE_ERR_INVALID_ARG;
+  if (a->T > 0 && (!al(a->x, 16) || !al(a->a_fp8, 8) || !al(a->a_sf, 4))) return MOE_ERR_INVALID_ARG;
+  if ((long)a->cap < (long)a->T * a->k + (long)a->E * (a->A - 1)) return MOE_ERR_CAPACITY;
+  if ((long)a->cap * a->H > 0x7FFFFFFFFFFFL) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return MOE_ERR_CUDA;
+  return cuda_status(moe::launch_route_scatter(*a, ctx->num_sms, ctx->d_err, S(stream)));
+}
+
+MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t* sf_in, int E, int N,
+                                int K, int w_format, uint8_t* w_out, uint32_t* sf_out, moe_stream_t stream) {
+  if (!ctx || !w_in || !sf_in || !w_out || !sf_out || E < 1 || N < 1 || K < 128 || K % 128 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (w_format != MOE_GEMM_W_E2M1 && w_format != MOE_GEMM_W_E4M3) return MOE_ERR_INVALID_ARG;
+  if (w_format == MOE_GEMM_W_E4M3 && w_out == w_in) return MOE_ERR_INVALID_ARG;
+  if (!al(sf_out, 4) || (w_format == MOE_GEMM_W_E4M3 && !al(w_out, 2))) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  return cuda_status(moe::launch_prepare_weights(w_in, sf_in, E, N, K, w_format, w_out, sf_out, S(stream)));
+}
+
+static int check_gemm(const moe::GemmArgs& g) {
+  if (!g.a || !g.a_sf || !g.expert_ends || !g.w || !g.w_sf || !g.out) return MOE_ERR_INVALID_ARG;
+  if (g.E < 1 || g.N < 256 || g.N % 256 != 0 || g.K < 128 || g.K % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (g.cap < 0 || g.cap % 128 != 0 || g.ld_sf < g.cap || g.ld_sf % 4 != 0) return MOE_ERR_INVALID_ARG;
+  if (g.w_format != MOE_GEMM_W_E2M1 && g.w_format != MOE_GEMM_W_E4M3) return MOE_ERR_INVALID_ARG;
+  if (!al(g.a, 16) || !al(g.w, 32) || !al(g.out, 16) || !al(g.a_sf, 4) || !al(g.w_sf, 4))
+    return MOE_ERR_INVALID_ARG;
+  if ((long)g.E * g.N >= (1L << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+MOE_API int moe_grouped_gemm(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf, int ld_sf,
+                             const int32_t* expert_ends, int E, int A, int cap, const uint8_t* w,
+                             const uint32_t* w_sf, int w_format, int N, int K, uint16_t* out,
+                             moe_stream_t stream) {
+  if (!ctx || A != 128) return MOE_ERR_INVALID_ARG;
+  moe::GemmArgs g{a, a_sf, ld_sf, expert_ends, E, cap, w, w_sf, w_format, N, K, out};
+  int rc = check_gemm(g);
+  if (rc != MOE_OK) return rc;
+  if (cap == 0) return MOE_OK;
+  DeviceGuard dg(ctx->device);
+  return moe::launch_grouped_gemm(g, ctx->encode, ctx->num_sms, ctx->d_err, S(stream));
+}
+
+MOE_API int moe_act_quant(moe_ctx* ctx, const uint16_t* gateup, uint8_t* out, int32_t* out_sf,
+                          const int32_t* expert_ends, int E, int A, int M_alloc, int I,
+                          const moe_act_params* act, moe_stream_t stream) {
+  if (!ctx || !act || M_alloc < 0 || I < 128 || I % 128 != 0 || A < 1) return MOE_ERR_INVALID_ARG;
+  if (M_alloc > 0 && (!gateup || !out || !out_sf)) return MOE_ERR_INVALID_ARG;
+  if (expert_ends && (E < 1 || E > 65535)) return MOE_ERR_INVALID_ARG;
+  if (act->kind != MOE_ACT_SILU && act->kind != MOE_ACT_SILU_CLAMP) return MOE_ERR_INVALID_ARG;
+  if (!al(gateup, 16) || !al(out, 16) || !al(out_sf, 4)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  return cuda_status(moe::launch_act_quant(gateup, out, out_sf, expert_ends, E, A, M_alloc, I, act->kind,
+                                           act->limit, ctx->num_sms, ctx->d_err, S(stream)));
+}
+
+MOE_API int moe_combine(moe_ctx* ctx, const uint16_t* down, int H, const float* topk_w,
+                        const int32_t* src2dst, int T, int k, float rsf, uint16_t* out, moe_stream_t stream) {
+  if (!ctx || T < 0 || k < 1 || H < 8 || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!down || !topk_w || !src2dst || !out)) return MOE_ERR_INVALID_ARG;
+  if (!al(down, 16) || !al(out, 16)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  return cuda_status(moe::launch_combine(down, H, topk_w, src2dst, T, k, rsf, out, ctx->num_sms, S(stream)));
+}
+
+MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* a, moe_stream_t stream) {
+  if (!ctx || !a) return MOE_ERR_INVALID_ARG;
+  if (a->T < 0 || a->k < 1 || a->A != 128 || a->H % 256 != 0 || a->I % 128 != 0 || (2 * a->I) % 256 != 0 ||
+      a->cap % 128 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (!a->gateup || !a->act_fp8 || !a->act_sf || !a->down || !a->topk_w || !a->src2dst || !a->out)
+    return MOE_ERR_INVALID_ARG;
+  if (a->act.kind != MOE_ACT_SILU && a->act.kind != MOE_ACT_SILU_CLAMP) return MOE_ERR_INVALID_ARG;
+  const int ld = (int)align4l(a->cap);
+  moe::GemmArgs g1{a->a_fp8, a->a_sf, ld, a->expert_ends, a->E, a->cap, a->w13, a->w13_sf, a->w_format,
+                   2 * a->I, a->H, a->gateup};
+  moe::GemmArgs g2{a->act_fp8, a->act_sf, ld, a->expert_ends, a->E, a->cap, a->w2, a->w2_sf, a->w_format,
+                   a->H, a->I, a->down};
+  int rc;
+  if ((rc = check_gemm(g1)) != MOE_OK || (rc = check_gemm(g2)) != MOE_OK) return rc;
+  if (!al(a->gateup, 16) || !al(a->act_fp8, 16) || !al(a->down, 16) || !al(a->out, 16))
+    return MOE_ERR_INVALID_ARG;
+  DeviceGuard dg(ctx->device);
+  if (a->cap > 0) {
+    if ((rc = moe::launch_grouped_gemm(g1, ctx->encode, ctx->num_sms, ctx->d_err, S(stream))) != MOE_OK) return rc;
+    if ((rc = cuda_status(moe::launch_act_quant(a->gateup, a->act_fp8, a->act_sf, a->expert_ends, a->E, a->A,
+                                                a->cap, a->I, a->act.kind, a->act.limit, ctx->num_sms,
+                                                ctx->d_err, S(stream)))) != MOE_OK)
+      return rc;
+    if ((rc = moe::launch_grouped_gemm(g2, ctx->encode, ctx->num_sms, ctx->d_err, S(stream))) != MOE_OK) return rc;
+  }
+  return cuda_status(moe::launch_combine(a->down, a->H, a->topk_w, a->src2dst, a->T, a->k, a->rsf, a->out,
+                                         ctx->num_sms, S(stream)));
+}
+
+MOE_API int moe_sparse_gemv_decode(moe_ctx* ctx, const moe_decode_args* a, moe_stream_t stream) {
+  if (!ctx || !a) return MOE_ERR_INVALID_ARG;
+  if (a->T < 0 || a->T > 64 || a->k < 1 || a->k > 32 || a->H < 32 || a->H % 32 != 0 || a->I < 32 ||
+      a->I % 32 != 0 || a->num_local_experts < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (a->wfmt != MOE_WFMT_FP8_PER_EXPERT && a->wfmt != MOE_WFMT_MXFP4_G32) return MOE_ERR_INVALID_ARG;
+  if (a->glu_layout != MOE_GLU_HALVES && a->glu_layout != MOE_GLU_INTERLEAVED) return MOE_ERR_INVALID_ARG;
+  if (a->T > 0) {
+    if (!a->x || !a->topk_ids || !a->topk_w || !a->w_gu || !a->b_gu || !a->w_d || !a->b_d || !a->y1 ||
+        !a->act || !a->y2 || !a->out)
+      return MOE_ERR_INVALID_ARG;
+    if (a->wfmt == MOE_WFMT_FP8_PER_EXPERT && (!a->w_gu_scale || !a->w_d_scale)) return MOE_ERR_INVALID_ARG;
+    if (a->wfmt == MOE_WFMT_MXFP4_G32 && (!a->w_gu_sf || !a->w_d_sf)) return MOE_ERR_INVALID_ARG;
+    if (!al(a->w_gu, 16) || !al(a->w_d, 16) || !al(a->x, 8) || !al(a->act, 8)) return MOE_ERR_INVALID_ARG;
+  }
+  DeviceGuard g(ctx->device);
+  return cuda_status(moe::launch_decode(*a, S(stream)));
+}
+
+}  // extern "C"

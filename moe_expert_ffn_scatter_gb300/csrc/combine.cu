@@ -1,0 +1,118 @@
+// combine.cu -- top-k weighted combine and load-time weight preparation.
+//
+// Combine ([DG] §2.6.1, post_reorder): out[t] = bf16(rsf * sum_j w[t,j] *
+// down[src2dst[t,j]]) over the slots with src2dst >= 0, fp32 accumulation,
+// one fused multiply-add per slot in slot order. One thread per (token, 8
+// columns): uint4 gathers from the k grouped rows, a uint4 store; the token's
+// src2dst / weights are warp-broadcast loads.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ down, int H,
+                                                      const float* __restrict__ topk_w,
+                                                      const int32_t* __restrict__ s2d, int T, int k,
+                                                      float rsf, uint16_t* __restrict__ out) {
+  const int chunks = H / 8;
+  const long total = (long)T * chunks;
+  for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long)gridDim.x * blockDim.x) {
+    const int t = (int)(idx / chunks);
+    const int c = (int)(idx % chunks);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j0 = 0; j0 < k; j0 += 4) {
+      int dst[4];
+      float wt[4];
+      uint4 v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = j0 + q;
+        dst[q] = (j < k) ? s2d[(size_t)t * k + j] : -1;
+        wt[q] = (j < k) ? topk_w[(size_t)t * k + j] : 0.0f;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        v[q] = (dst[q] >= 0) ? __ldg(reinterpret_cast<const uint4*>(down + (size_t)dst[q] * H) + c)
+                             : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (dst[q] < 0) continue;
+        const uint32_t* pv = &v[q].x;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = __fmaf_rn(wt[q], bf16_lo(pv[i]), acc[2 * i]);
+          acc[2 * i + 1] = __fmaf_rn(wt[q], bf16_hi(pv[i]), acc[2 * i + 1]);
+        }
+      }
+    }
+    uint4 o;
+    uint32_t* po = &o.x;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      po[i] = pack_bf16x2(__fmul_rn(acc[2 * i], rsf), __fmul_rn(acc[2 * i + 1], rsf));
+    reinterpret_cast<uint4*>(out + (size_t)t * H)[c] = o;
+  }
+}
+
+// Scales [E][N][K/32] bytes -> words [E][K/128][N]: word (e, c, n) = the
+// four bytes sf[e][n][4c .. 4c+3], byte 4c lowest.
+__global__ void prepare_scales_kernel(const uint8_t* __restrict__ sf_in, int E, int N, int K,
+                                      uint32_t* __restrict__ sf_out) {
+  const int KC = K / 128;
+  const long total = (long)E * KC * N;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int n = (int)(i % N);
+    const long ec = i / N;
+    const int c = (int)(ec % KC);
+    const int e = (int)(ec / KC);
+    const uint8_t* p = sf_in + ((size_t)e * N + n) * (K / 32) + 4 * c;
+    sf_out[i] = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+  }
+}
+
+// Packed e2m1 byte pairs -> e4m3 codes (exact: every e2m1 value is an e4m3
+// value). One thread per input byte, two output bytes.
+__global__ void widen_e2m1_kernel(const uint8_t* __restrict__ w_in, long nbytes, uint16_t* __restrict__ w_out) {
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nbytes; i += (long)gridDim.x * blockDim.x) {
+    const uint32_t b = w_in[i];
+    const float lo = e2m1_to_f32(b & 0xFu), hi = e2m1_to_f32(b >> 4);
+    w_out[i] = (uint16_t)e4m3x2_satfinite(lo, hi);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t* down, int H, const float* topk_w, const int32_t* src2dst,
+                           int T, int k, float rsf, uint16_t* out, int num_sms, cudaStream_t st) {
+  const long total = (long)T * (H / 8);
+  if (total == 0) return cudaSuccess;
+  const int blocks = (int)lmin((total + 255) / 256, (long)num_sms * 8);
+  combine_kernel<<<blocks, 256, 0, st>>>(down, H, topk_w, src2dst, T, k, rsf, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepare_weights(const uint8_t* w_in, const uint8_t* sf_in, int E, int N, int K,
+                                   int w_format, uint8_t* w_out, uint32_t* sf_out, cudaStream_t st) {
+  const long words = (long)E * (K / 128) * N;
+  if (words > 0) {
+    prepare_scales_kernel<<<(int)lmin((words + 255) / 256, 65535), 256, 0, st>>>(sf_in, E, N, K, sf_out);
+    cudaError_t ce = cudaGetLastError();
+    if (ce != cudaSuccess) return ce;
+  }
+  const long nbytes = (long)E * N * (K / 2);
+  if (nbytes == 0) return cudaSuccess;
+  if (w_format == MOE_GEMM_W_E4M3) {
+    widen_e2m1_kernel<<<(int)lmin((nbytes + 255) / 256, 65535), 256, 0, st>>>(
+        w_in, nbytes, reinterpret_cast<uint16_t*>(w_out));
+    return cudaGetLastError();
+  }
+  if (w_out != w_in) return cudaMemcpyAsync(w_out, w_in, (size_t)nbytes, cudaMemcpyDeviceToDevice, st);
+  return cudaSuccess;
+}
+
+}  // namespace moe

@@ -1,0 +1,161 @@
+// common.cuh -- device helpers shared by the sm_103a kernels of this library.
+//
+// Number formats (e4m3, e2m1, UE8M0, bf16), the exp/SiLU specification that
+// makes the activation quantisation reproducible bit for bit, warp helpers and
+// the device error word. Everything here is written for sm_103a; every float
+// operation whose rounding matters uses an explicit _rn intrinsic so that the
+// compiler cannot contract it into an fma.
+//
+// Sources cited by tag and section:
+//  [LR] "Blackwell FP4 MoE：把 live-row 边界贯穿整个 FFN"
+//  [DG] "Blackwell 上的 DeepGEMM FusedMoE（sglang）"
+//  [SD] "Phase 20: Sparse MoE Decode — 只算被路由到的专家"
+//  [KM] "kimi3_pro6000_sglang_sm120_flashinfer_mxfp4" experiment log
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_gb300.h"
+
+namespace moe {
+
+// ----------------------------------------------------------------- errors
+// Device-side anomalies set bits in a context-owned word; nothing traps.
+__device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// ------------------------------------------------------------------ bf16
+__device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+// fp32 -> bf16 bits, round to nearest even, NaN kept quiet.
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x7FFFFFu)) return (u >> 16) | 0x40u;
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return f32_to_bf16_bits(lo) | (f32_to_bf16_bits(hi) << 16);
+}
+
+// ------------------------------------------------------------------- e4m3
+// Two fp32 values -> two e4m3 codes with the hardware's round-to-nearest-even
+// and saturation to the largest finite value (+-448); `lo` lands in bits 0-7.
+__device__ __forceinline__ uint32_t e4m3x2_satfinite(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
+// e4m3 pair (bits 0-7 and 8-15) -> two fp32 values (exact, through f16).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)(two_codes & 0xFFFFu)));
+  float2 out;
+  asm("{.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;}"
+      : "=f"(out.x), "=f"(out.y) : "r"(h2));
+  return out;
+}
+
+// ------------------------------------------------------------------ UE8M0
+// Smallest power of two not below s (s >= 0, finite), as a biased exponent
+// byte: the fp32 exponent field, plus one when the mantissa is non-zero,
+// except at exponent 0xFE and for subnormals not above 2^-127
+// ([DG] 附录 A, rounding-up cast).
+__device__ __forceinline__ uint32_t ue8m0_ceil(float s) {
+  uint32_t bits = __float_as_uint(s);
+  uint32_t e = (bits >> 23) & 0xFFu;
+  uint32_t m = bits & 0x7FFFFFu;
+  uint32_t ru = (m > 0u && e != 0xFEu) && !(e == 0u && m <= 0x400000u);
+  return (e + ru) & 0xFFu;
+}
+
+// 2^k for k in [-127, 127] (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float pow2_f32(int k) {
+  return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Scale byte for a group with absolute maximum `amax` (NaN never reaches it:
+// the callers reduce with fmaxf, which drops NaN). A non-finite amax keeps the
+// scale finite at 0xFE ([KM] NaN/Inf decision: E8M0 must never be 0xFF).
+__device__ __forceinline__ uint32_t group_scale_byte(float amax) {
+  if (isinf(amax)) return 0xFEu;
+  return ue8m0_ceil(__fdiv_rn(amax, 448.0f));
+}
+
+// ----------------------------------------------------- exp specification
+// The pages leave exp unspecified; this library fixes one definition so that
+// SiLU and the routing weights are reproducible bit for bit:
+//   n = rint(x * fl(log2 e)); r = fma(-n, L_hi, x); r = fma(-n, L_lo, r)
+//   with L_hi = fl(ln 2) with its 12 low significand bits cleared (exact
+//   products n * L_hi for |n| < 4096) and L_lo = fl(ln 2 - L_hi);
+//   p = Taylor series of e^r to degree 7 by Horner, coefficients fl(1/k!),
+//   one fma per step (Cody & Waite reduction, textbook series);
+//   e^x = (p * 2^(n/2)) * 2^(n - n/2), n/2 truncated toward zero;
+//   x >= 128 -> +inf, x <= -150 -> +0, NaN -> NaN.
+// Constants as fp32 bit patterns:
+//   fl(log2 e) 0x3fb8aa3b, L_hi 0x3f317000, L_lo 0x3805fdf4,
+//   1/3! 0x3e2aaaab, 1/4! 0x3d2aaaab, 1/5! 0x3c088889, 1/6! 0x3ab60b61,
+//   1/7! 0x39500d01.
+__device__ __forceinline__ float spec_exp(float x) {
+  if (isnan(x)) return x;
+  if (x >= 128.0f) return __uint_as_float(0x7F800000u);
+  if (x <= -150.0f) return 0.0f;
+  const float t = __fmul_rn(x, __uint_as_float(0x3fb8aa3bu));
+  const float fn = rintf(t);
+  const int n = (int)fn;
+  float r = __fmaf_rn(-fn, __uint_as_float(0x3f317000u), x);
+  r = __fmaf_rn(-fn, __uint_as_float(0x3805fdf4u), r);
+  float p = __uint_as_float(0x39500d01u);
+  p = __fmaf_rn(p, r, __uint_as_float(0x3ab60b61u));
+  p = __fmaf_rn(p, r, __uint_as_float(0x3c088889u));
+  p = __fmaf_rn(p, r, __uint_as_float(0x3d2aaaabu));
+  p = __fmaf_rn(p, r, __uint_as_float(0x3e2aaaabu));
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  const int n1 = n / 2;
+  const int n2 = n - n1;
+  return __fmul_rn(__fmul_rn(p, pow2_f32(n1)), pow2_f32(n2));
+}
+
+// silu(g) = g / (1 + exp(-g)), one add and one IEEE division.
+__device__ __forceinline__ float spec_silu(float g) {
+  return __fdiv_rn(g, __fadd_rn(1.0f, spec_exp(-g)));
+}
+__device__ __forceinline__ float spec_sigmoid(float x) {
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, spec_exp(-x)));
+}
+
+// ------------------------------------------------------------------- e2m1
+// e2m1 nibble -> fp32: 1 sign, 2 exponent (bias 1), 1 mantissa bit.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t nib) {
+  const uint32_t e = (nib >> 1) & 3u, m = nib & 1u;
+  float mag = (e == 0u) ? (m ? 0.5f : 0.0f)
+                        : __uint_as_float(((e - 1u + 127u) << 23) | (m << 22));
+  return (nib & 8u) ? -mag : mag;
+}
+
+// Two e2m1 values in one byte (low nibble first) -> two fp32 values (exact).
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
+  uint32_t h2;
+  asm("{.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;}" : "=r"(h2) : "h"((uint16_t)byte));
+  float2 out;
+  asm("{.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;}"
+      : "=f"(out.x), "=f"(out.y) : "r"(h2));
+  return out;
+}
+
+// ------------------------------------------------------------------ warps
+__device__ __forceinline__ float warp_max_xor(float v, int width_log2) {
+  for (int o = 1 << (width_log2 - 1); o > 0; o >>= 1)
+    v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+__host__ __device__ __forceinline__ int64_t align_up64(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace moe

@@ -1,0 +1,435 @@
+// grouped_gemm.cu -- block-scaled grouped GEMM over live rows on the sm_103a
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+//   out[r, n] = bf16( sum_k e4m3(a[r,k]) 2^(sa(r, k/128) - 127)
+//                           * w(e, n, k) 2^(sw(e, n, k/32) - 127) )
+// for the live rows r in [start[e], end[e]) of every expert e; A = 128-row
+// aligned segments ([LR] §2: FC1 and FC2 take the same endpoint layout, and
+// padding rows are never computed; [DG] §2.3.1 recipes (1,128) activations,
+// (1,32) MXFP4 weights).
+//
+// Kernel structure (one persistent CTA per SM, 256 threads):
+//   warp 0    TMA producer: 128x128 e4m3 A tile and 256x128 B tile per stage
+//             (B e2m1 is expanded by TMA to one byte per element, the layout
+//             kind::mxf8f6f4 reads for 4-bit operands; the transaction count
+//             of such a copy is its packed global size), 128B swizzle.
+//   warp 1    TMEM owner and MMA issuer: tcgen05.cp moves the stage's scale
+//             factors from shared to tensor memory, then 4 x
+//             tcgen05.mma.kind::mxf8f6f4.block_scale (M128 N256 K32) into a
+//             128x256 fp32 accumulator; tcgen05.commit frees the stage.
+//   warp 2    scale-factor loader: activation scale words (one int32 holds 4
+//             groups of 128 = the packed MN-major activation scales, used as
+//             they are: the MMA's scale-factor-A id picks the byte) and the
+//             prepared weight scale words (4 x 32-K blocks per int32, picked by
+//             the scale-factor-B id), written to shared memory in the
+//             32-row x 16-byte layout of tcgen05.cp 32x128b.warpx4.
+//   warps 4-7 epilogue: tcgen05.ld of the accumulator (each warp its 32-lane
+//             quarter), bf16 conversion into registers, accumulator released,
+//             then row-masked 16-byte stores (rows >= end[e] are skipped).
+// The tile list is (live 128-row tile, 256-column tile); the number of live
+// tiles, align_up(end[E-1], 128) / 128, and each tile's expert come from the
+// device-side endpoint tensor, so the grid never depends on routing counts.
+// Every mbarrier wait is bounded (about one second); a wait that runs out sets
+// MOE_DEVERR_WAIT_TIMEOUT, makes every role leave its loop, drains the issued
+// tensor-core work and frees tensor memory before the CTA exits.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int kThreads = 256;
+constexpr uint32_t A_BYTES = BM * BK;
+constexpr uint32_t B_BYTES = BN * BK;
+constexpr uint32_t SFA_BYTES = BM * 4;
+constexpr uint32_t SFB_BYTES = BN * 4;
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
+constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+constexpr uint32_t NUM_BARS = 2 * STAGES + 3;
+constexpr uint32_t OFF_TMEM_PTR = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t OFF_ABORT = OFF_TMEM_PTR + 4;
+constexpr uint32_t SMEM_USED = OFF_ABORT + 4;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_SF_BASE = 256;             // stage s: SFA cols 256+16s, SFB cols 264+16s
+constexpr unsigned long long kWaitNs = 1000000000ull;
+
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale:
+// A format e4m3 (0), B format e2m1 (5) or e4m3 (0), both K-major, N >> 3 at
+// bit 17, UE8M0 scale type at bit 23, M >> 4 at bit 24; the scale-factor ids
+// (B at bit 4, A at bit 29) are or-ed in per instruction.
+__host__ __device__ constexpr uint32_t idesc_base(bool b_fp4) {
+  return (0u << 7) | ((b_fp4 ? 5u : 0u) << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128
+// bytes, 8-row atoms 1024 bytes apart (stride byte offset), version 1.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                 // leading byte offset (unused with swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// Descriptor of a 32-row x 16-byte scale-factor block (no swizzle: 8-row x
+// 16-byte core matrices stored contiguously, 128 bytes apart).
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for phase `parity` of `bar`. Returns false when the wait ran
+// out (error bit set, abort raised) or another role already aborted.
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                        uint32_t* err, bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (honour_abort && *abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitNs) {
+      *abort_flag = 1;
+      raise_error(err, MOE_DEVERR_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Expert of the live 128-row tile starting at m0: the smallest e with
+// align_up(end[e], 128) > m0 (start[e] <= m0 < end[e] follows).
+__device__ __forceinline__ int expert_of_tile(const int32_t* __restrict__ ends, int E, int m0) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((int)align_up64(__ldg(ends + mid), BM) > m0) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
+template <bool kBfp4>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
+    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    const int32_t* __restrict__ a_sf, int ld_sf, const int32_t* __restrict__ ends, int E, int cap,
+    const uint32_t* __restrict__ w_sf, int N, int K, uint16_t* __restrict__ out, uint32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM_PTR);
+  const uint32_t bar0 = sbase + OFF_BAR;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  const uint32_t tmem_full_bar = bar0 + 8u * (2 * STAGES);
+  const uint32_t tmem_empty_bar = bar0 + 8u * (2 * STAGES + 1);
+  const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 2);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 2);   // producer's expect_tx arrive + scale loader's arrive
+      mbar_init(empty_bar(s), 1);  // tcgen05.commit
+    }
+    mbar_init(tmem_full_bar, 1);
+    mbar_init(tmem_empty_bar, 4);  // one arrive per epilogue warp
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int KC = K / BK;
+  const int n_tiles = N / BN;
+  int rows_aligned = (int)align_up64(__ldg(ends + E - 1), BM);
+  if (rows_aligned > cap || rows_aligned < 0) {
+    if (threadIdx.x == 0) raise_error(err, MOE_DEVERR_ENDPOINTS);
+    rows_aligned = 0;
+  }
+  const int num_tiles = (rows_aligned / BM) * n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+      int s = 0;
+      uint32_t ph = 0;
+      int issued[STAGES];
+      for (int i = 0; i < STAGES; ++i) issued[i] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+        const int e = expert_of_tile(ends, E, m0);
+        for (int kc = 0; kc < KC; ++kc) {
+          if (!(ok = wait_phase(empty_bar(s), ph ^ 1u, abort_flag, err))) break;
+          mbar_arrive_expect_tx(full_bar(s), A_BYTES + (kBfp4 ? B_BYTES / 2 : B_BYTES));
+          tma_load_2d(sbase + OFF_A + s * A_BYTES, &tmA, kc * BK, m0, full_bar(s));
+          tma_load_2d(sbase + OFF_B + s * B_BYTES, &tmB, kc * BK, e * N + n0, full_bar(s));
+          issued[s] = (int)ph;
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA can exit: their
+        // transaction bytes complete the full barriers' tx counts whether or
+        // not the scale loader arrived, so wait with a short bound only.
+        for (int i = 0; i < STAGES; ++i)
+          if (issued[i] >= 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(full_bar(i), (uint32_t)issued[i]) && globaltimer_ns() - t0 < 2000000ull) {}
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      int s = 0;
+      uint32_t ph = 0, acc_ph = 0;
+      const uint32_t ibase = idesc_base(kBfp4);
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!(ok = wait_phase(tmem_empty_bar, acc_ph ^ 1u, abort_flag, err))) break;
+        tc_fence_after();
+        for (int kc = 0; kc < KC; ++kc) {
+          if (!(ok = wait_phase(full_bar(s), ph, abort_flag, err))) break;
+          tc_fence_after();
+          const uint32_t tsfa = tmem + TMEM_SF_BASE + 16u * s;
+          const uint32_t tsfb = tsfa + 8u;
+          tc_cp_sf(tsfa, desc_sf(sbase + OFF_SFA + s * SFA_BYTES));
+          tc_cp_sf(tsfb, desc_sf(sbase + OFF_SFB + s * SFB_BYTES));
+          tc_cp_sf(tsfb + 4u, desc_sf(sbase + OFF_SFB + s * SFB_BYTES + 512u));
+          const uint32_t a_addr = sbase + OFF_A + s * A_BYTES;
+          const uint32_t b_addr = sbase + OFF_B + s * B_BYTES;
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const uint32_t idesc = ibase | ((uint32_t)k4 << 4) | ((uint32_t)(kc & 3) << 29);
+            tc_mma(tmem, desc_sw128(a_addr + 32u * k4), desc_sw128(b_addr + 32u * k4), idesc, tsfa, tsfb,
+                   (kc | k4) != 0);
+          }
+          tc_commit(empty_bar(s));
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(tmem_full_bar);
+        acc_ph ^= 1u;
+      }
+      // Drain: every tcgen05 operation issued above completes before the
+      // tensor memory is released.
+      tc_commit(done_bar);
+      wait_phase(done_bar, 0, abort_flag, err, false);
+    }
+  } else if (warp == 2) {
+    // -------------------------------------------------- scale loader
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+      const int e = expert_of_tile(ends, E, m0);
+      for (int kc = 0; kc < KC; ++kc) {
+        if (!(ok = wait_phase(empty_bar(s), ph ^ 1u, abort_flag, err))) break;
+        const int32_t* asf = a_sf + (size_t)(kc >> 2) * ld_sf + m0 + lane;
+        uint4 va;
+        va.x = (uint32_t)__ldg(asf);
+        va.y = (uint32_t)__ldg(asf + 32);
+        va.z = (uint32_t)__ldg(asf + 64);
+        va.w = (uint32_t)__ldg(asf + 96);
+        *reinterpret_cast<uint4*>(smem + OFF_SFA + s * SFA_BYTES + 16 * lane) = va;
+        const uint32_t* bsf = w_sf + ((size_t)e * KC + kc) * N + n0 + lane;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint4 vb;
+          vb.x = __ldg(bsf + 128 * h);
+          vb.y = __ldg(bsf + 128 * h + 32);
+          vb.z = __ldg(bsf + 128 * h + 64);
+          vb.w = __ldg(bsf + 128 * h + 96);
+          *reinterpret_cast<uint4*>(smem + OFF_SFB + s * SFB_BYTES + 512 * h + 16 * lane) = vb;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full_bar(s));
+        if (++s == STAGES) { s = 0; ph ^= 1u; }
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    uint32_t acc_ph = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+      const int e = expert_of_tile(ends, E, m0);
+      const int row_end = __ldg(ends + e);
+      if (!wait_phase(tmem_full_bar, acc_ph, abort_flag, err)) break;
+      tc_fence_after();
+      uint32_t packed[BN / 2];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + 32u * c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          packed[16 * c + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty_bar);
+      const int row = m0 + 32 * q + lane;
+      if (row < row_end) {
+        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * N + n0);
+#pragma unroll
+        for (int i = 0; i < BN / 8; ++i)
+          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      }
+      acc_ph ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+bool encode_2d(EncodeTiledFn encode, CUtensorMap* map, CUtensorMapDataType dt, const void* base,
+               uint64_t inner, uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+               uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kBfp4>
+int launch_impl(const GemmArgs& g, EncodeTiledFn encode, int num_sms, uint32_t* err, cudaStream_t st) {
+  CUtensorMap tmA, tmB;
+  if (!encode_2d(encode, &tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a, (uint64_t)g.K, (uint64_t)g.cap,
+                 (uint64_t)g.K, BK, BM))
+    return MOE_ERR_INVALID_ARG;
+  const uint64_t wrows = (uint64_t)g.E * (uint64_t)g.N;
+  const bool ok = kBfp4 ? encode_2d(encode, &tmB, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w, (uint64_t)g.K,
+                                    wrows, (uint64_t)g.K / 2, BK, BN)
+                        : encode_2d(encode, &tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.w, (uint64_t)g.K, wrows,
+                                    (uint64_t)g.K, BK, BN);
+  if (!ok) return MOE_ERR_INVALID_ARG;
+  const long max_tiles = (long)(g.cap / BM) * (g.N / BN);
+  const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
+  if (grid <= 0) return MOE_OK;
+  grouped_gemm_kernel<kBfp4><<<grid, kThreads, SMEM_BYTES, st>>>(tmA, tmB, g.a_sf, g.ld_sf, g.expert_ends, g.E,
+                                                                  g.cap, g.w_sf, g.N, g.K, g.out, err);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+cudaError_t init_grouped_gemm() {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(grouped_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)SMEM_BYTES);
+}
+
+int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, uint32_t* err, cudaStream_t st) {
+  if (g.w_format == MOE_GEMM_W_E4M3) return launch_impl<false>(g, encode, num_sms, err, st);
+  return launch_impl<true>(g, encode, num_sms, err, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,55 @@
+// kernels.h -- internal launchers of the library (host side, not exported).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_gb300.h"
+
+namespace moe {
+
+inline long lmin(long a, long b) { return a < b ? a : b; }
+inline long lmax(long a, long b) { return a > b ? a : b; }
+
+// Tokens per scatter chunk: the unit of the per-chunk expert histogram.
+constexpr int kScatterChunk = 64;
+
+size_t route_scatter_ws_bytes(int T, int E, int k);
+cudaError_t launch_expert_ends(const int32_t* counts, int E, int A, int32_t* ends, uint32_t* err,
+                               cudaStream_t st);
+cudaError_t launch_route_scatter(const moe_route_args& a, int num_sms, uint32_t* err, cudaStream_t st);
+cudaError_t launch_act_quant(const uint16_t* gateup, uint8_t* out, int32_t* out_sf,
+                             const int32_t* expert_ends, int E, int A, int M_alloc, int I, int kind,
+                             float limit, int num_sms, uint32_t* err, cudaStream_t st);
+cudaError_t launch_combine(const uint16_t* down, int H, const float* topk_w, const int32_t* src2dst,
+                           int T, int k, float rsf, uint16_t* out, int num_sms, cudaStream_t st);
+cudaError_t launch_prepare_weights(const uint8_t* w_in, const uint8_t* sf_in, int E, int N, int K,
+                                   int w_format, uint8_t* w_out, uint32_t* sf_out, cudaStream_t st);
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct GemmArgs {
+  const uint8_t* a;
+  const int32_t* a_sf;
+  int ld_sf;
+  const int32_t* expert_ends;
+  int E, cap;
+  const uint8_t* w;
+  const uint32_t* w_sf;
+  int w_format;
+  int N, K;
+  uint16_t* out;
+};
+// Per-device set-up (shared-memory opt-in); called once per context.
+cudaError_t init_grouped_gemm();
+// Returns MOE_OK or a MOE_ERR_* code.
+int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, uint32_t* err,
+                        cudaStream_t st);
+
+cudaError_t launch_decode(const moe_decode_args& a, cudaStream_t st);
+
+}  // namespace moe

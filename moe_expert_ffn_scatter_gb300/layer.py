@@ -1,0 +1,86 @@
+"""One routed MoE FFN layer on one GPU: fixed-capacity buffers plus the two
+C-ABI calls of the hot path (moe_route_scatter, moe_ffn_forward).
+
+PyTorch only allocates device memory and supplies the stream; all arithmetic
+runs in the library's kernels. Every buffer is allocated once at capacity and
+keeps its address, so `forward` can be captured into a CUDA graph and replayed
+with new routing (the endpoint tensor's contents change, its address does not).
+"""
+import torch
+
+from . import binding as B
+from .synth import align4
+
+
+def ceil_div(a, b):
+    return (a + b - 1) // b
+
+
+class MoEFFNLayer:
+    def __init__(self, ctx, *, T, E, k, H, I, A=128, cap=None, routing=B.MOE_ROUTE_SOFTMAX_TOPK,
+                 act_kind=B.MOE_ACT_SILU, limit=0.0, rsf=1.0, w_format=B.MOE_GEMM_W_E2M1, device="cuda"):
+        self.ctx = ctx
+        self.T, self.E, self.k, self.H, self.I, self.A = T, E, k, H, I, A
+        if cap is None:
+            cap = ceil_div(T * k + E * (A - 1), A) * A
+        self.cap = cap
+        self.routing = routing
+        self.act_kind, self.limit, self.rsf = act_kind, limit, rsf
+        self.w_format = w_format
+        dev = torch.device(device)
+        u8, i32, f32, bf16 = torch.uint8, torch.int32, torch.float32, torch.bfloat16
+        self.topk_ids = torch.empty((T, k), dtype=i32, device=dev)
+        self.topk_w = torch.empty((T, k), dtype=f32, device=dev)
+        self.src2dst = torch.empty((T, k), dtype=i32, device=dev)
+        self.expert_ends = torch.zeros((E,), dtype=i32, device=dev)
+        self.a_fp8 = torch.empty((cap, H), dtype=u8, device=dev)
+        self.a_sf = torch.empty((ceil_div(H, 512), align4(cap)), dtype=i32, device=dev)
+        self.ws = torch.empty((max(16, B.moe_route_scatter_workspace_size(T, E, k)),), dtype=u8, device=dev)
+        self.gateup = torch.empty((cap, 2 * I), dtype=bf16, device=dev)
+        self.act_fp8 = torch.empty((cap, I), dtype=u8, device=dev)
+        self.act_sf = torch.empty((ceil_div(I, 512), align4(cap)), dtype=i32, device=dev)
+        self.down = torch.empty((cap, H), dtype=bf16, device=dev)
+        self.out = torch.empty((T, H), dtype=bf16, device=dev)
+        self.w13 = self.w13_sf = self.w2 = self.w2_sf = None
+
+    # ---------------------------------------------------------------- weights
+    def load_weights(self, w13, w13_sf, w2, w2_sf, stream=None):
+        """Upload canonical MXFP4 weights (packed e2m1 [E,N,K/2], UE8M0 [E,N,K/32])
+        and prepare them for the grouped GEMM (scale re-layout, optional e4m3)."""
+        dev = self.out.device
+        E, H, I = self.E, self.H, self.I
+
+        def prep(w, sf, N, K):
+            w_in = torch.as_tensor(w).to(dev).contiguous()
+            sf_in = torch.as_tensor(sf).to(dev).contiguous()
+            if self.w_format == B.MOE_GEMM_W_E4M3:
+                w_out = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
+            else:
+                w_out = w_in
+            sf_out = torch.empty((E, K // 128, N), dtype=torch.int32, device=dev)
+            B.moe_prepare_weights(self.ctx, w_in, sf_in, E, N, K, self.w_format, w_out, sf_out, stream=stream)
+            return w_out, sf_out
+
+        self.w13, self.w13_sf = prep(w13, w13_sf, 2 * I, H)
+        self.w2, self.w2_sf = prep(w2, w2_sf, H, I)
+
+    # ------------------------------------------------------------------ steps
+    def route_scatter(self, x, logits=None, bias=None, stream=None):
+        B.moe_route_scatter(self.ctx, routing_mode=self.routing, x=x, logits=logits, corr_bias=bias,
+                            topk_ids=self.topk_ids, topk_w=self.topk_w, expert_ends=self.expert_ends,
+                            src2dst=self.src2dst, a_fp8=self.a_fp8, a_sf=self.a_sf, workspace=self.ws,
+                            T=self.T, E=self.E, k=self.k, H=self.H, A=self.A, cap=self.cap, stream=stream)
+
+    def ffn(self, stream=None):
+        B.moe_ffn_forward(self.ctx, a_fp8=self.a_fp8, a_sf=self.a_sf, expert_ends=self.expert_ends, w13=self.w13,
+                          w13_sf=self.w13_sf, w2=self.w2, w2_sf=self.w2_sf, gateup=self.gateup,
+                          act_fp8=self.act_fp8, act_sf=self.act_sf, down=self.down, topk_w=self.topk_w,
+                          src2dst=self.src2dst, out=self.out, T=self.T, E=self.E, k=self.k, H=self.H, I=self.I,
+                          A=self.A, cap=self.cap, w_format=self.w_format, act_kind=self.act_kind,
+                          limit=self.limit, rsf=self.rsf, stream=stream)
+
+    def forward(self, x, logits=None, bias=None, stream=None):
+        """x [T,H] bf16, logits [T,E] fp32 (device) -> self.out [T,H] bf16."""
+        self.route_scatter(x, logits, bias, stream=stream)
+        self.ffn(stream=stream)
+        return self.out

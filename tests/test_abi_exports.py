@@ -1,0 +1,73 @@
+"""The C ABI library loads on a machine without a GPU, exports every symbol
+that include/*.h declares, and rejects invalid arguments on the host before
+touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from moe_expert_ffn_scatter_gb300 import binding as B
+from moe_expert_ffn_scatter_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names |= set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 12
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+
+
+def test_exports_only_declared_symbols():
+    out = os.popen("nm -D --defined-only %s" % build_mod.LIB).read()
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert exported == declared_symbols()
+
+
+def test_binding_names_match_abi():
+    for n in declared_symbols():
+        if n in ("moe_ctx_create", "moe_ctx_destroy", "moe_status_string"):
+            continue
+        assert hasattr(B, n), n
+
+
+def test_host_validation_without_device(lib):
+    """Invalid arguments are rejected before any CUDA call (so this runs on
+    CPU-only machines): NULL context, NULL args, bad sizes."""
+    assert lib.moe_version() == 10000
+    assert lib.moe_status_string(-1) == b"invalid argument"
+    assert lib.moe_route_scatter(None, None, None) == -1
+    assert lib.moe_ffn_forward(None, None, None) == -1
+    assert lib.moe_sparse_gemv_decode(None, None, None) == -1
+    assert lib.moe_grouped_gemm(None, None, None, 0, None, 1, 128, 128, None, None, 0, 256, 128, None, None) == -1
+    p = B.moe_act_params(0, 0.0)
+    assert lib.moe_act_quant(None, None, None, None, None, 1, 128, 10, 128, ctypes.byref(p), None) == -1
+    assert lib.moe_combine(None, None, 8, None, None, 1, 1, 1.0, None, None) == -1
+    assert lib.moe_expert_ends_from_counts(None, None, 4, 128, None, None) == -1
+    assert lib.moe_route_scatter_workspace_size(4096, 32, 6) == 64 * 32 * 4
+    assert lib.moe_route_scatter_workspace_size(-1, 32, 6) == 0
+
+
+def test_struct_layouts_match_header():
+    """ctypes mirrors of the argument structs have the C sizes (LP64)."""
+    assert ctypes.sizeof(B.moe_route_args) == 120
+    assert ctypes.sizeof(B.moe_act_params) == 8
+    assert ctypes.sizeof(B.moe_ffn_args) == 14 * 8 + 8 * 4 + 8 + 4 + 4
+    assert B.moe_decode_args.T.offset > B.moe_decode_args.out.offset

@@ -1,0 +1,208 @@
+"""Grouped block-scaled GEMM, combine and the whole layer on the GPU against
+the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from moe_expert_ffn_scatter_gb300 import binding as B
+from moe_expert_ffn_scatter_gb300 import synth
+from moe_expert_ffn_scatter_gb300.layer import MoEFFNLayer
+from tests.gpu_util import check_ffn_tolerance, dev, dev_bf16, filled, host, host_u16
+from tests.refs import bf16_bits_to_f64, bf16_ulp
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx(cuda_lib):
+    return B.Context(0)
+
+
+def prepared(ctx, w, w_sf, fmt):
+    E, N, K2 = w.shape
+    K = 2 * K2
+    w_in = dev(w)
+    w_out = torch.empty((E, N, K), dtype=torch.uint8, device="cuda") if fmt == B.MOE_GEMM_W_E4M3 else w_in
+    sf_out = torch.empty((E, K // 128, N), dtype=torch.int32, device="cuda")
+    B.moe_prepare_weights(ctx, w_in, dev(w_sf), E, N, K, fmt, w_out, sf_out)
+    return w_out, sf_out
+
+
+def gemm_case(ctx, orc, counts, N, K, fmt, seed=0, cap=None):
+    g = np.random.default_rng(seed)
+    E = len(counts)
+    counts = np.array(counts, np.int32)
+    _, ends = orc.endpoints(counts, 128)
+    cap = cap or synth.align_up(max(int(ends[-1]), 128), 128)
+    ld = synth.align4(cap)
+    a = synth.e4m3_codes(g, (cap, K), exp_lo=1, exp_hi=14)
+    sfb = synth.ue8m0_bytes(g, (cap, K // 128), -3, 3)
+    a_sf = synth.pack_scale_words(sfb, ld)
+    w = synth.e2m1_packed(g, (E, N, K // 2))
+    w_sf = synth.ue8m0_bytes(g, (E, N, K // 32))
+    wd, wsfd = prepared(ctx, w, w_sf, fmt)
+    out = filled((cap, N), 0xAB, torch.int16)
+    B.moe_grouped_gemm(ctx, dev(a), dev(a_sf), ld, dev(ends), E, 128, cap, wd, wsfd, fmt, N, K, out)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_error(ctx) == 0
+    got = host_u16(out)
+    ref = orc.grouped_gemm(a, a_sf, ends, 128, w, w_sf, out=np.full((cap, N), 0xABAB, np.uint16))
+    return got, ref, ends
+
+
+def assert_gemm_close(got, ref, ends):
+    start = np.concatenate([[0], (ends[:-1] + 127) // 128 * 128])
+    live = np.zeros(got.shape[0], bool)
+    for s, e in zip(start, ends):
+        live[s:e] = True
+    assert np.all(got[~live] == 0xABAB), "padding rows written"
+    g = bf16_bits_to_f64(got[live])
+    r = bf16_bits_to_f64(ref[live])
+    # fp32 tensor-core accumulation vs one fp64 sum: at most one bf16 step apart
+    bad = np.abs(g - r) > bf16_ulp(r) * 1.0001 + 1e-30
+    assert not bad.any(), "%d of %d elements differ by more than one bf16 step" % (bad.sum(), bad.size)
+    return np.mean(got[live] == ref[live])
+
+
+@pytest.mark.parametrize("fmt", [B.MOE_GEMM_W_E2M1, B.MOE_GEMM_W_E4M3], ids=["e2m1", "e4m3"])
+def test_gemm_single_tile(ctx, orc, fmt):
+    got, ref, ends = gemm_case(ctx, orc, [128], 256, 128, fmt)
+    assert assert_gemm_close(got, ref, ends) > 0.99
+
+
+@pytest.mark.parametrize("fmt", [B.MOE_GEMM_W_E2M1, B.MOE_GEMM_W_E4M3], ids=["e2m1", "e4m3"])
+def test_gemm_ragged_experts(ctx, orc, fmt):
+    # several M tiles per expert, an empty expert, ragged tails, K with a
+    # partial group of four 128-blocks (K=640 -> scale words 0 and 1)
+    got, ref, ends = gemm_case(ctx, orc, [5, 0, 300, 129, 1], 512, 640, fmt, seed=1)
+    assert assert_gemm_close(got, ref, ends) > 0.99
+
+
+def test_gemm_formats_agree_bitwise(ctx, orc):
+    g1, _, _ = gemm_case(ctx, orc, [200, 77], 256, 384, B.MOE_GEMM_W_E2M1, seed=3)
+    g2, _, _ = gemm_case(ctx, orc, [200, 77], 256, 384, B.MOE_GEMM_W_E4M3, seed=3)
+    assert np.array_equal(g1, g2)
+
+
+def test_gemm_many_tiles_persistent(ctx, orc):
+    """More tiles than SMs: every CTA loops over several tiles."""
+    counts = [700, 650, 0, 900, 810, 333]
+    got, ref, ends = gemm_case(ctx, orc, counts, 1024, 256, B.MOE_GEMM_W_E2M1, seed=4)
+    assert assert_gemm_close(got, ref, ends) > 0.99
+
+
+def test_gemm_no_live_rows(ctx, orc):
+    got, ref, ends = gemm_case(ctx, orc, [0, 0], 256, 128, B.MOE_GEMM_W_E2M1, cap=256)
+    assert np.all(got == 0xABAB)
+
+
+def test_combine_bit_exact(ctx, orc):
+    g = np.random.default_rng(6)
+    T, k, H, rows = 333, 6, 4096, 2500
+    down = synth.bf16_normal(g, (rows, H))
+    s2d = g.permutation(rows)[:T * k].reshape(T, k).astype(np.int32)
+    s2d[g.random((T, k)) < 0.05] = -1
+    w = g.random((T, k)).astype(np.float32)
+    down[s2d.max() + 1:] = 0x7FC0  # rows that no slot references are NaN
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    B.moe_combine(ctx, dev_bf16(down), H, dev(w), dev(s2d), T, k, 1.25, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_u16(out), orc.combine(down, w, s2d, rsf=1.25))
+
+
+# ------------------------------------------------------------ whole layer
+def make_layer(ctx, cfg, inp, fmt=B.MOE_GEMM_W_E2M1):
+    routing = B.MOE_ROUTE_SIGMOID_BIAS_TOPK if cfg.routing == "sigmoid_bias" else B.MOE_ROUTE_SOFTMAX_TOPK
+    layer = MoEFFNLayer(ctx, T=cfg.T, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I, A=cfg.A, cap=cfg.cap, routing=routing,
+                        act_kind=B.MOE_ACT_SILU_CLAMP if cfg.clamp else B.MOE_ACT_SILU, limit=cfg.limit,
+                        rsf=cfg.rsf, w_format=fmt)
+    layer.load_weights(inp.w13, inp.w13_sf, inp.w2, inp.w2_sf)
+    return layer
+
+
+def oracle_layer(orc, cfg, inp):
+    if cfg.routing == "sigmoid_bias":
+        ids, w = orc.route_sigmoid_bias_topk(inp.logits, inp.bias, cfg.k)
+    else:
+        ids, w = orc.route_softmax_topk(inp.logits, cfg.k)
+    return ids, w
+
+
+def test_tiny_layer_vs_oracle(ctx, orc):
+    cfg = synth.TINY
+    inp = synth.ffn_inputs(cfg)
+    layer = make_layer(ctx, cfg, inp)
+    out = layer.forward(dev_bf16(inp.x), dev(inp.logits))
+    torch.cuda.synchronize()
+    assert B.moe_get_device_error(ctx) == 0
+    ids, w = oracle_layer(orc, cfg, inp)
+    ends, s2d, a, a_sf = orc.scatter(ids, inp.x, cfg.E, cfg.A, cfg.cap)
+    assert np.array_equal(host(layer.expert_ends), ends)
+    assert np.array_equal(host(layer.src2dst), s2d)
+    gu = orc.grouped_gemm(a, a_sf, ends, cfg.A, inp.w13, inp.w13_sf)
+    act, act_sf = orc.act_quant(gu, ends, cfg.A)
+    down = orc.grouped_gemm(act, act_sf, ends, cfg.A, inp.w2, inp.w2_sf)
+    ref = orc.combine(down, w, s2d, rsf=cfg.rsf)
+    assert_gemm_close(host_u16(layer.gateup), gu, ends)
+    check_ffn_tolerance(host_u16(out), ref)
+
+
+def test_deepseek_layer_sampled_tokens(ctx, orc):
+    cfg = synth.DEEPSEEK
+    inp = synth.ffn_inputs(cfg)
+    layer = make_layer(ctx, cfg, inp)
+    out = layer.forward(dev_bf16(inp.x), dev(inp.logits))
+    torch.cuda.synchronize()
+    assert B.moe_get_device_error(ctx) == 0
+    ids, w = oracle_layer(orc, cfg, inp)
+    assert np.array_equal(host(layer.topk_ids), ids)
+    toks = np.random.default_rng(11).choice(cfg.T, 48, replace=False).astype(np.int32)
+    ref = orc.ffn_tokens(inp.x, ids, w, inp.w13, inp.w13_sf, inp.w2, inp.w2_sf, toks)
+    check_ffn_tolerance(host_u16(out)[toks], ref)
+
+
+def test_layer_graph_replay_permuted_routing_deterministic(ctx, orc):
+    """Capture route+scatter+FFN once; replay with the logit columns permuted
+    (new counts each time): equal to an eager run bit for bit."""
+    cfg = synth.FFNConfig("graph", T=512, E=8, k=2, H=512, I=256, seed=12)
+    inp = synth.ffn_inputs(cfg)
+    layer = make_layer(ctx, cfg, inp)
+    x = dev_bf16(inp.x)
+    logits = dev(inp.logits)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        layer.forward(x, logits, stream=s)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        layer.forward(x, logits, stream=s)
+    rng = np.random.default_rng(100)
+    for i in range(3):
+        perm = rng.permutation(cfg.E)
+        logits.copy_(dev(inp.logits[:, perm]))
+        graph.replay()
+        torch.cuda.synchronize()
+        replayed = host_u16(layer.out).copy()
+        ends_replayed = host(layer.expert_ends).copy()
+        layer.forward(x, logits)
+        torch.cuda.synchronize()
+        assert np.array_equal(replayed, host_u16(layer.out))
+        ids, w = orc.route_softmax_topk(inp.logits[:, perm], cfg.k)
+        ends, _, _, _ = orc.scatter(ids, inp.x, cfg.E, cfg.A, cfg.cap)
+        assert np.array_equal(ends_replayed, ends)
+        toks = np.arange(0, cfg.T, 37, dtype=np.int32)
+        ref = orc.ffn_tokens(inp.x, ids, w, inp.w13, inp.w13_sf, inp.w2, inp.w2_sf, toks)
+        check_ffn_tolerance(replayed[toks], ref)
+    assert B.moe_get_device_error(ctx) == 0
+
+
+def test_layer_three_runs_bitwise_identical(ctx):
+    cfg = synth.FFNConfig("det", T=256, E=8, k=4, H=256, I=256, seed=13)
+    inp = synth.ffn_inputs(cfg)
+    layer = make_layer(ctx, cfg, inp)
+    outs = []
+    for _ in range(3):
+        layer.forward(dev_bf16(inp.x), dev(inp.logits))
+        torch.cuda.synchronize()
+        outs.append(host_u16(layer.out).copy())
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])

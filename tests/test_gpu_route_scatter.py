@@ -1,0 +1,118 @@
+"""Routing, endpoints and the token scatter on the GPU against the oracle:
+ids and weights, expert_ends, src2dst, e4m3 rows and packed scales bit-exact;
+padding rows untouched."""
+import numpy as np
+import pytest
+import torch
+
+from moe_expert_ffn_scatter_gb300 import binding as B
+from moe_expert_ffn_scatter_gb300 import synth
+from tests.gpu_util import dev, dev_bf16, filled, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx(cuda_lib):
+    return B.Context(0)
+
+
+def gpu_route_scatter(ctx, x, E, k, A, cap, mode, logits=None, bias=None, ids=None):
+    T, H = x.shape
+    ids_d = dev(ids) if ids is not None else torch.full((T, k), -9, dtype=torch.int32, device="cuda")
+    w_d = torch.full((T, k), -1.0, dtype=torch.float32, device="cuda")
+    ends = torch.full((E,), -9, dtype=torch.int32, device="cuda")
+    s2d = torch.full((T, k), -9, dtype=torch.int32, device="cuda")
+    a = filled((cap, H), 0xAB)
+    a_sf = filled(((H // 128 + 3) // 4, synth.align4(cap)), 0xAB, torch.int32)
+    ws = torch.empty((B.moe_route_scatter_workspace_size(T, E, k),), dtype=torch.uint8, device="cuda")
+    B.moe_route_scatter(ctx, routing_mode=mode, x=dev_bf16(x), logits=None if logits is None else dev(logits),
+                        corr_bias=None if bias is None else dev(bias), topk_ids=ids_d,
+                        topk_w=w_d if mode != B.MOE_ROUTE_PRECOMPUTED else None, expert_ends=ends, src2dst=s2d,
+                        a_fp8=a, a_sf=a_sf, workspace=ws, T=T, E=E, k=k, H=H, A=A, cap=cap)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_error(ctx) == 0
+    return host(ids_d), host(w_d), host(ends), host(s2d), host(a), host(a_sf)
+
+
+def check_against_oracle(orc, res, ids_ref, x, E, A, cap, w_ref=None):
+    ids, w, ends, s2d, a, a_sf = res
+    assert np.array_equal(ids, ids_ref)
+    if w_ref is not None:
+        assert np.array_equal(w.view(np.uint32), w_ref.view(np.uint32))  # bit-exact weights
+    r_ends, r_s2d, r_a, r_sf = orc.scatter(ids_ref, x, E, A, cap)
+    assert np.array_equal(ends, r_ends)
+    assert np.array_equal(s2d, r_s2d)
+    assert np.array_equal(a, r_a)
+    assert np.array_equal(a_sf, r_sf)
+
+
+@pytest.mark.parametrize("cfg", [synth.TINY, synth.DEEPSEEK], ids=["tiny", "deepseek"])
+def test_softmax_routing_and_scatter(ctx, orc, cfg):
+    inp = synth.ffn_inputs(cfg, weights=False)
+    ids_ref, w_ref = orc.route_softmax_topk(inp.logits, cfg.k)
+    res = gpu_route_scatter(ctx, inp.x, cfg.E, cfg.k, cfg.A, cfg.cap, B.MOE_ROUTE_SOFTMAX_TOPK, logits=inp.logits)
+    check_against_oracle(orc, res, ids_ref, inp.x, cfg.E, cfg.A, cfg.cap, w_ref)
+
+
+def test_sigmoid_bias_routing_and_scatter_kimi_shape(ctx, orc):
+    cfg = synth.KIMI
+    inp = synth.ffn_inputs(cfg, weights=False)
+    ids_ref, w_ref = orc.route_sigmoid_bias_topk(inp.logits, inp.bias, cfg.k)
+    res = gpu_route_scatter(ctx, inp.x, cfg.E, cfg.k, cfg.A, cfg.cap, B.MOE_ROUTE_SIGMOID_BIAS_TOPK,
+                            logits=inp.logits, bias=inp.bias)
+    check_against_oracle(orc, res, ids_ref, inp.x, cfg.E, cfg.A, cfg.cap, w_ref)
+
+
+def test_precomputed_page_counts(ctx, orc):
+    """[LR] §2 worked example: A=128, counts=[96,0,129,1] -> end=[96,128,257,385]."""
+    g = np.random.default_rng(0)
+    ids = synth.ids_with_counts(g, [96, 0, 129, 1], k=2)
+    x = synth.bf16_normal(g, (ids.shape[0], 256))
+    cap = synth.align_up(ids.size + 4 * 127, 128)
+    res = gpu_route_scatter(ctx, x, 4, 2, 128, cap, B.MOE_ROUTE_PRECOMPUTED, ids=ids)
+    assert res[2].tolist() == [96, 128, 257, 385]
+    check_against_oracle(orc, res, ids, x, 4, 128, cap)
+
+
+@pytest.mark.parametrize("H", [128, 384, 3584])
+def test_precomputed_masked_slots_ragged_hidden(ctx, orc, H):
+    g = np.random.default_rng(H)
+    T, k, E = 300, 3, 7
+    ids = g.integers(-1, E, size=(T, k)).astype(np.int32)
+    ids[5] = -1
+    ids[ids == 4] = -1  # expert 4 empty
+    x = synth.bf16_normal(g, (T, H))
+    cap = synth.align_up(T * k + E * 127, 128)
+    res = gpu_route_scatter(ctx, x, E, k, 128, cap, B.MOE_ROUTE_PRECOMPUTED, ids=ids)
+    check_against_oracle(orc, res, ids, x, E, 128, cap)
+
+
+def test_all_masked_and_empty_batch(ctx, orc):
+    ids = np.full((70, 2), -1, np.int32)
+    x = synth.bf16_normal(np.random.default_rng(1), (70, 256))
+    res = gpu_route_scatter(ctx, x, 5, 2, 128, 1024, B.MOE_ROUTE_PRECOMPUTED, ids=ids)
+    assert res[2].tolist() == [0] * 5 and np.all(res[3] == -1)
+    assert np.all(res[4] == 0xAB)
+
+
+def test_skewed_routing_one_hot_expert(ctx, orc):
+    """Every token prefers expert 3: one long segment, the rest small."""
+    g = np.random.default_rng(5)
+    T, E, k = 1000, 16, 4
+    logits = synth.fp32_normal(g, (T, E))
+    logits[:, 3] += 10.0
+    x = synth.bf16_normal(g, (T, 512))
+    cap = synth.align_up(T * k + E * 127, 128)
+    ids_ref, w_ref = orc.route_softmax_topk(logits, k)
+    res = gpu_route_scatter(ctx, x, E, k, 128, cap, B.MOE_ROUTE_SOFTMAX_TOPK, logits=logits)
+    check_against_oracle(orc, res, ids_ref, x, E, 128, cap, w_ref)
+
+
+def test_capacity_checked_on_host(ctx):
+    x = torch.zeros((10, 128), dtype=torch.bfloat16, device="cuda")
+    t = torch.zeros(4096, dtype=torch.int32, device="cuda")
+    with pytest.raises(B.MoeError) as ei:
+        B.moe_route_scatter(ctx, routing_mode=B.MOE_ROUTE_PRECOMPUTED, x=x, topk_ids=t, expert_ends=t, src2dst=t,
+                            a_fp8=t, a_sf=t, workspace=t, T=10, E=2, k=1, H=128, A=128, cap=100)
+    assert ei.value.status == -2
