@@ -40,6 +40,9 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extras", action="store_true")
+    p.add_argument("--profile-kernel", choices=["route_scatter", "gemm1", "act_quant", "gemm2", "combine"],
+                   help="set up the layer, run one full step, then launch only this step's kernel "
+                        "warmup + steps times and exit (for ncu captures); prints no JSON line")
     return p.parse_args()
 
 
@@ -207,6 +210,26 @@ def run_ours(args):
         if ev is not None: ev[5].record(stream)
 
     kernels_per_step = 3 + 1 + 1 + 1 + 1
+    if args.profile_kernel:
+        step()
+        only = {
+            "route_scatter": lambda: L.route_scatter(x, logits, stream=stream),
+            "gemm1": lambda: B.moe_grouped_gemm(ctx, L.a_fp8, L.a_sf, ld, L.expert_ends, cfg.E, cfg.A, cfg.cap,
+                                                L.w13, L.w13_sf, L.w_format, 2 * cfg.I, cfg.H, L.gateup,
+                                                stream=stream),
+            "act_quant": lambda: B.moe_act_quant(ctx, L.gateup, L.act_fp8, L.act_sf, L.expert_ends, cfg.E, cfg.A,
+                                                 cfg.cap, cfg.I, stream=stream),
+            "gemm2": lambda: B.moe_grouped_gemm(ctx, L.act_fp8, L.act_sf, ld, L.expert_ends, cfg.E, cfg.A, cfg.cap,
+                                                L.w2, L.w2_sf, L.w_format, cfg.H, cfg.I, L.down, stream=stream),
+            "combine": lambda: B.moe_combine(ctx, L.down, cfg.H, L.topk_w, L.src2dst, cfg.T, cfg.k, cfg.rsf, L.out,
+                                             stream=stream),
+        }[args.profile_kernel]
+        for _ in range(args.warmup + args.steps):
+            only()
+        torch.cuda.synchronize()
+        if B.moe_get_device_error(ctx) != 0:
+            raise RuntimeError("device error")
+        return
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
