@@ -106,7 +106,7 @@ MOE_API int moe_version(void);
 /* ---------------------------------------------------- endpoints alone
  * expert_ends[e] from per-expert live-row counts[e] (both int32 [E], device):
  * start[0] = 0, start[e] = align_up(end[e-1], A), end[e] = start[e] + count[e]
- * ([LR] §2, "概念伪代码"). One block; E <= 65536. */
+ * ([LR] §2, "概念伪代码"). One block; 1 <= E <= 8192. */
 MOE_API int moe_expert_ends_from_counts(moe_ctx* ctx, const int32_t* counts, int E, int A,
                                         int32_t* expert_ends, moe_stream_t stream);
 
@@ -166,13 +166,15 @@ MOE_API int moe_route_scatter(moe_ctx* ctx, const moe_route_args* args, moe_stre
  * GEMM ([DG] §2.1.2 path A: weight scales are transformed once at load into
  * the layout the GEMM consumes). Input: packed e2m1 w_in [E][N][K/2] and
  * canonical UE8M0 bytes sf_in [E][N][K/32]. Output scales: uint32 words
- * sf_out [E][K/128][N], word (e, c, n) holding the four scales of k-blocks
- * 4c..4c+3 of row n, block 4c in the low byte. Output weights w_out:
+ * sf_out [E][K/128][N]; the word of (e, c, n) holds the four scales of
+ * k-blocks 4c..4c+3 of row n, block 4c in the low byte, and within each block
+ * of 128 rows position 4i + j holds row 32j + i (the tensor-memory scale
+ * layout the GEMM copies as is). Output weights w_out:
  *   MOE_GEMM_W_E2M1: packed e2m1 [E][N][K/2] (a copy; w_out may equal w_in)
  *   MOE_GEMM_W_E4M3: the same values re-encoded exactly as e4m3 [E][N][K]
  *                    (twice the bytes; [DG] §2.1.2 path B does the same
  *                    lossless widening of e2m1 to e4m3)
- * Requires K % 128 == 0; w_out must not overlap sf_out. */
+ * Requires K % 128 == 0, N % 128 == 0; w_out must not overlap sf_out. */
 #define MOE_GEMM_W_E2M1 0
 #define MOE_GEMM_W_E4M3 1
 MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t* sf_in, int E, int N,
@@ -190,7 +192,8 @@ MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t
  * w, w_sf prepared by moe_prepare_weights in format w_format ([E][N][K/2]
  * packed e2m1 or [E][N][K] e4m3; scales [E][K/128][N]); out [cap,N] bf16.
  * Requires K % 128 == 0, N % 256 == 0, cap % 128 == 0, A == 128,
- * ld_sf >= cap, ld_sf % 4 == 0, 32-byte aligned w, 16-byte aligned a. */
+ * ld_sf >= cap, ld_sf % 4 == 0, 32-byte aligned w, 16-byte aligned a, a_sf,
+ * w_sf and out. */
 MOE_API int moe_grouped_gemm(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf, int ld_sf,
                              const int32_t* expert_ends, int E, int A, int cap, const uint8_t* w,
                              const uint32_t* w_sf, int w_format, int N, int K, uint16_t* out,

@@ -113,7 +113,7 @@ MOE_API int moe_get_device_error(moe_ctx* ctx, uint32_t* bits, moe_stream_t stre
 
 MOE_API int moe_expert_ends_from_counts(moe_ctx* ctx, const int32_t* counts, int E, int A,
                                         int32_t* expert_ends, moe_stream_t stream) {
-  if (!ctx || !counts || !expert_ends || E < 1 || E > 65536 || A < 1) return MOE_ERR_INVALID_ARG;
+  if (!ctx || !counts || !expert_ends || E < 1 || E > 8192 || A < 1) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
   return cuda_status(moe::launch_expert_ends(counts, E, A, expert_ends, ctx->d_err, S(stream)));
 }
@@ -148,7 +148,8 @@ MOE_API int moe_route_scatter(moe_ctx* ctx, const moe_route_args* a, moe_stream_
 
 MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t* sf_in, int E, int N,
                                 int K, int w_format, uint8_t* w_out, uint32_t* sf_out, moe_stream_t stream) {
-  if (!ctx || !w_in || !sf_in || !w_out || !sf_out || E < 1 || N < 1 || K < 128 || K % 128 != 0)
+  if (!ctx || !w_in || !sf_in || !w_out || !sf_out || E < 1 || N < 128 || N % 128 != 0 || K < 128 ||
+      K % 128 != 0)
     return MOE_ERR_INVALID_ARG;
   if (w_format != MOE_GEMM_W_E2M1 && w_format != MOE_GEMM_W_E4M3) return MOE_ERR_INVALID_ARG;
   if (w_format == MOE_GEMM_W_E4M3 && w_out == w_in) return MOE_ERR_INVALID_ARG;
@@ -162,7 +163,7 @@ static int check_gemm(const moe::GemmArgs& g) {
   if (g.E < 1 || g.N < 256 || g.N % 256 != 0 || g.K < 128 || g.K % 128 != 0) return MOE_ERR_INVALID_ARG;
   if (g.cap < 0 || g.cap % 128 != 0 || g.ld_sf < g.cap || g.ld_sf % 4 != 0) return MOE_ERR_INVALID_ARG;
   if (g.w_format != MOE_GEMM_W_E2M1 && g.w_format != MOE_GEMM_W_E4M3) return MOE_ERR_INVALID_ARG;
-  if (!al(g.a, 16) || !al(g.w, 32) || !al(g.out, 16) || !al(g.a_sf, 4) || !al(g.w_sf, 4))
+  if (!al(g.a, 16) || !al(g.w, 32) || !al(g.out, 16) || !al(g.a_sf, 16) || !al(g.w_sf, 16))
     return MOE_ERR_INVALID_ARG;
   if ((long)g.E * g.N >= (1L << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;

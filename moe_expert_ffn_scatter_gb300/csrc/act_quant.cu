@@ -70,9 +70,10 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
           ua = fminf(fmaxf(ua, -limit), limit);
           ub = fminf(fmaxf(ub, -limit), limit);
         }
-        h[2 * i] = __fmul_rn(spec_silu(ga), ua);
-        h[2 * i + 1] = __fmul_rn(spec_silu(gb), ub);
-        amax = fmaxf(amax, fmaxf(fabsf(h[2 * i]), fabsf(h[2 * i + 1])));
+        const float2 hh = mul2(spec_silu2(make_float2(ga, gb)), make_float2(ua, ub));
+        h[2 * i] = hh.x;
+        h[2 * i + 1] = hh.y;
+        amax = fmaxf(amax, fmaxf(fabsf(hh.x), fabsf(hh.y)));
       }
     }
 #pragma unroll

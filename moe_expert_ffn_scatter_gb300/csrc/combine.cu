@@ -59,14 +59,18 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   }
 }
 
-// Scales [E][N][K/32] bytes -> words [E][K/128][N]: word (e, c, n) = the
-// four bytes sf[e][n][4c .. 4c+3], byte 4c lowest.
+// Scales [E][N][K/32] bytes -> words [E][K/128][N]: the word of (e, c, n)
+// holds the four bytes sf[e][n][4c .. 4c+3], byte 4c lowest; inside every
+// block of 128 rows, position 4 i + j holds row 32 j + i (the source layout of
+// tcgen05.cp 32x128b.warpx4, so the GEMM copies it without rearranging).
 __global__ void prepare_scales_kernel(const uint8_t* __restrict__ sf_in, int E, int N, int K,
                                       uint32_t* __restrict__ sf_out) {
   const int KC = K / 128;
   const long total = (long)E * KC * N;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
-    const int n = (int)(i % N);
+    const int pos = (int)(i % N);
+    const int q = pos & 127;
+    const int n = (pos & ~127) + 32 * (q & 3) + (q >> 2);
     const long ec = i / N;
     const int c = (int)(ec % KC);
     const int e = (int)(ec / KC);

@@ -130,6 +130,71 @@ __device__ __forceinline__ float spec_sigmoid(float x) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, spec_exp(-x)));
 }
 
+// ------------------------------------------------ packed pairs (f32x2)
+// Blackwell executes fp32 add / mul / fma on register pairs; each half is the
+// ordinary IEEE round-to-nearest operation, so results are bitwise those of
+// the scalar forms.
+__device__ __forceinline__ uint64_t pk(float2 a) {
+  return ((uint64_t)__float_as_uint(a.y) << 32) | __float_as_uint(a.x);
+}
+__device__ __forceinline__ float2 upk(uint64_t r) {
+  return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)), "l"(pk(c)));
+  return upk(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)));
+  return upk(d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)));
+  return upk(d);
+}
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+
+// The exp specification on a pair, bitwise equal to spec_exp on each half.
+// rint(t) is taken as (t + 1.5*2^23) - 1.5*2^23, exact round-to-nearest-even
+// for |t| < 2^22; 2^n is applied as 2^(n>>1) * 2^(n - (n>>1)): the first
+// product is exact (normal range) for every n this range produces, so the
+// result equals the n/2 split of the definition.
+__device__ __forceinline__ float2 spec_exp2(float2 x) {
+  const float kMagic = 12582912.0f;  // 1.5 * 2^23
+  const float2 t = mul2(x, splat2(__uint_as_float(0x3fb8aa3bu)));
+  const float2 y = add2(t, splat2(kMagic));
+  const float2 fn = add2(y, splat2(-kMagic));
+  const int n0 = __float_as_int(y.x) - 0x4B400000, n1 = __float_as_int(y.y) - 0x4B400000;
+  float2 r = fma2(make_float2(-fn.x, -fn.y), splat2(__uint_as_float(0x3f317000u)), x);
+  r = fma2(make_float2(-fn.x, -fn.y), splat2(__uint_as_float(0x3805fdf4u)), r);
+  float2 p = splat2(__uint_as_float(0x39500d01u));
+  p = fma2(p, r, splat2(__uint_as_float(0x3ab60b61u)));
+  p = fma2(p, r, splat2(__uint_as_float(0x3c088889u)));
+  p = fma2(p, r, splat2(__uint_as_float(0x3d2aaaabu)));
+  p = fma2(p, r, splat2(__uint_as_float(0x3e2aaaabu)));
+  p = fma2(p, r, splat2(0.5f));
+  p = fma2(p, r, splat2(1.0f));
+  p = fma2(p, r, splat2(1.0f));
+  const int h0 = n0 >> 1, h1 = n1 >> 1;
+  const float2 s1 = make_float2(__uint_as_float((uint32_t)(h0 + 127) << 23), __uint_as_float((uint32_t)(h1 + 127) << 23));
+  const float2 s2 = make_float2(__uint_as_float((uint32_t)(n0 - h0 + 127) << 23),
+                                __uint_as_float((uint32_t)(n1 - h1 + 127) << 23));
+  float2 res = mul2(mul2(p, s1), s2);
+  // out-of-range and NaN inputs, as in the scalar definition
+  if (!(x.x > -150.0f && x.x < 128.0f)) res.x = isnan(x.x) ? x.x : (x.x >= 128.0f ? __uint_as_float(0x7F800000u) : 0.0f);
+  if (!(x.y > -150.0f && x.y < 128.0f)) res.y = isnan(x.y) ? x.y : (x.y >= 128.0f ? __uint_as_float(0x7F800000u) : 0.0f);
+  return res;
+}
+
+// silu on a pair, bitwise equal to spec_silu on each half.
+__device__ __forceinline__ float2 spec_silu2(float2 g) {
+  const float2 d = add2(splat2(1.0f), spec_exp2(make_float2(-g.x, -g.y)));
+  return make_float2(__fdiv_rn(g.x, d.x), __fdiv_rn(g.y, d.y));
+}
+
 // ------------------------------------------------------------------- e2m1
 // e2m1 nibble -> fp32: 1 sign, 2 exponent (bias 1), 1 mantissa bit.
 __device__ __forceinline__ float e2m1_to_f32(uint32_t nib) {

@@ -17,12 +17,16 @@
 //             factors from shared to tensor memory, then 4 x
 //             tcgen05.mma.kind::mxf8f6f4.block_scale (M128 N256 K32) into a
 //             128x256 fp32 accumulator; tcgen05.commit frees the stage.
-//   warp 2    scale-factor loader: activation scale words (one int32 holds 4
-//             groups of 128 = the packed MN-major activation scales, used as
-//             they are: the MMA's scale-factor-A id picks the byte) and the
-//             prepared weight scale words (4 x 32-K blocks per int32, picked by
-//             the scale-factor-B id), written to shared memory in the
-//             32-row x 16-byte layout of tcgen05.cp 32x128b.warpx4.
+//             The same thread bulk-copies the stage's scale words: the
+//             activation scales (one int32 holds 4 groups of 128 of the packed
+//             MN-major array, used as stored: the MMA's scale-factor-A id
+//             picks the byte) and the prepared weight scales (4 x 32-K blocks
+//             per int32, picked by the scale-factor-B id, pre-permuted at load
+//             time into the 32-row x 16-byte source layout of tcgen05.cp
+//             32x128b.warpx4).
+//   warp 2    activation-scale transposer: rearranges the 128 activation scale
+//             words of each stage into that tcgen05.cp source layout
+//             (shared -> shared), then completes the stage's full barrier.
 //   warps 4-7 epilogue: tcgen05.ld of the accumulator (each warp its 32-lane
 //             quarter), bf16 conversion into registers, accumulator released,
 //             then row-masked 16-byte stores (rows >= end[e] are skipped).
@@ -49,10 +53,11 @@ constexpr uint32_t SFA_BYTES = BM * 4;
 constexpr uint32_t SFB_BYTES = BN * 4;
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
-constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-constexpr uint32_t NUM_BARS = 2 * STAGES + 3;
+constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;          // tcgen05.cp layout
+constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;       // tcgen05.cp layout
+constexpr uint32_t OFF_SFA_IN = OFF_SFB + STAGES * SFB_BYTES;    // activation scales as stored
+constexpr uint32_t OFF_BAR = OFF_SFA_IN + STAGES * SFA_BYTES;
+constexpr uint32_t NUM_BARS = 3 * STAGES + 3;
 constexpr uint32_t OFF_TMEM_PTR = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_PTR + 4;
 constexpr uint32_t SMEM_USED = OFF_ABORT + 4;
@@ -147,6 +152,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -202,14 +215,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   const uint32_t bar0 = sbase + OFF_BAR;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  const uint32_t tmem_full_bar = bar0 + 8u * (2 * STAGES);
-  const uint32_t tmem_empty_bar = bar0 + 8u * (2 * STAGES + 1);
-  const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 2);
+  auto sfa_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  const uint32_t tmem_full_bar = bar0 + 8u * (3 * STAGES);
+  const uint32_t tmem_empty_bar = bar0 + 8u * (3 * STAGES + 1);
+  const uint32_t done_bar = bar0 + 8u * (3 * STAGES + 2);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 2);   // producer's expect_tx arrive + scale loader's arrive
+      mbar_init(full_bar(s), 2);   // producer's expect_tx arrive + scale transposer's arrive
       mbar_init(empty_bar(s), 1);  // tcgen05.commit
+      mbar_init(sfa_bar(s), 1);    // producer's expect_tx arrive for the activation scales
     }
     mbar_init(tmem_full_bar, 1);
     mbar_init(tmem_empty_bar, 4);  // one arrive per epilogue warp
@@ -253,9 +268,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
         const int e = expert_of_tile(ends, E, m0);
         for (int kc = 0; kc < KC; ++kc) {
           if (!(ok = wait_phase(empty_bar(s), ph ^ 1u, abort_flag, err))) break;
-          mbar_arrive_expect_tx(full_bar(s), A_BYTES + (kBfp4 ? B_BYTES / 2 : B_BYTES));
+          mbar_arrive_expect_tx(sfa_bar(s), SFA_BYTES);
+          bulk_load(sbase + OFF_SFA_IN + s * SFA_BYTES, a_sf + (size_t)(kc >> 2) * ld_sf + m0, SFA_BYTES,
+                    sfa_bar(s));
+          mbar_arrive_expect_tx(full_bar(s), A_BYTES + (kBfp4 ? B_BYTES / 2 : B_BYTES) + SFB_BYTES);
           tma_load_2d(sbase + OFF_A + s * A_BYTES, &tmA, kc * BK, m0, full_bar(s));
           tma_load_2d(sbase + OFF_B + s * B_BYTES, &tmB, kc * BK, e * N + n0, full_bar(s));
+          bulk_load(sbase + OFF_SFB + s * SFB_BYTES, w_sf + ((size_t)e * KC + kc) * N + n0, SFB_BYTES, full_bar(s));
           issued[s] = (int)ph;
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
@@ -310,37 +329,27 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       wait_phase(done_bar, 0, abort_flag, err, false);
     }
   } else if (warp == 2) {
-    // -------------------------------------------------- scale loader
+    // ------------------------------------------- activation-scale transposer
+    // The bulk copy lands the 128 scale words of the tile's rows in row order;
+    // tcgen05.cp 32x128b.warpx4 wants word (i, j) of its 32 x 4 source at
+    // 16 i + 4 j to hold row 32 j + i. Lane i gathers rows i, 32+i, 64+i, 96+i.
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
-      const int e = expert_of_tile(ends, E, m0);
-      for (int kc = 0; kc < KC; ++kc) {
-        if (!(ok = wait_phase(empty_bar(s), ph ^ 1u, abort_flag, err))) break;
-        const int32_t* asf = a_sf + (size_t)(kc >> 2) * ld_sf + m0 + lane;
-        uint4 va;
-        va.x = (uint32_t)__ldg(asf);
-        va.y = (uint32_t)__ldg(asf + 32);
-        va.z = (uint32_t)__ldg(asf + 64);
-        va.w = (uint32_t)__ldg(asf + 96);
-        *reinterpret_cast<uint4*>(smem + OFF_SFA + s * SFA_BYTES + 16 * lane) = va;
-        const uint32_t* bsf = w_sf + ((size_t)e * KC + kc) * N + n0 + lane;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint4 vb;
-          vb.x = __ldg(bsf + 128 * h);
-          vb.y = __ldg(bsf + 128 * h + 32);
-          vb.z = __ldg(bsf + 128 * h + 64);
-          vb.w = __ldg(bsf + 128 * h + 96);
-          *reinterpret_cast<uint4*>(smem + OFF_SFB + s * SFB_BYTES + 512 * h + 16 * lane) = vb;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full_bar(s));
-        if (++s == STAGES) { s = 0; ph ^= 1u; }
-      }
+    const int total = (num_tiles > (int)blockIdx.x) ? ((num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * KC : 0;
+    for (int it = 0; it < total; ++it) {
+      if (!(ok = wait_phase(sfa_bar(s), ph, abort_flag, err))) break;
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(smem + OFF_SFA_IN + s * SFA_BYTES);
+      uint4 v;
+      v.x = src[lane];
+      v.y = src[32 + lane];
+      v.z = src[64 + lane];
+      v.w = src[96 + lane];
+      *reinterpret_cast<uint4*>(smem + OFF_SFA + s * SFA_BYTES + 16 * lane) = v;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full_bar(s));
+      if (++s == STAGES) { s = 0; ph ^= 1u; }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------ epilogue

@@ -35,7 +35,7 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 template <int EPL, int MODE>
 __device__ __forceinline__ void route_token(const float* __restrict__ l, const float* __restrict__ bias,
                                             int E, int k, int lane, int32_t* __restrict__ ids_out,
-                                            float* __restrict__ w_out) {
+                                            float* __restrict__ w_out, int32_t* ids_smem) {
   float v[EPL];
   uint32_t removed = 0;
 #pragma unroll
@@ -86,6 +86,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ l, const f
   for (int j = 0; j < k; ++j) s = __fadd_rn(s, __shfl_sync(kFull, num, j));
   if (lane < k) {
     ids_out[lane] = my_idx;
+    ids_smem[lane] = my_idx;
     w_out[lane] = __fdiv_rn(num, s);
   }
 }
@@ -98,23 +99,30 @@ __global__ void __launch_bounds__(512) route_count_kernel(const float* __restric
                                                           int32_t* __restrict__ s2d,
                                                           int32_t* __restrict__ ws, int T, int E,
                                                           int k) {
-  extern __shared__ int32_t cnt[];
+  extern __shared__ int32_t smem_i32[];
+  int32_t* cnt = smem_i32;                 // [E] running count per expert
+  int32_t* ids_s = smem_i32 + E;           // [kScatterChunk * k] the chunk's expert ids
   const int c = blockIdx.x;
   const int t0 = c * kScatterChunk;
   const int t1 = min(T, t0 + kScatterChunk);
+  const int nr = (t1 - t0) * k;
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   if (MODE != MOE_ROUTE_PRECOMPUTED) {
     for (int t = t0 + warp; t < t1; t += nwarps)
       route_token<EPL, MODE>(logits + (size_t)t * E, bias, E, k, lane, ids + (size_t)t * k,
-                             topw + (size_t)t * k);
+                             topw + (size_t)t * k, ids_s + (t - t0) * k);
+  } else {
+    for (int r = threadIdx.x; r < nr; r += blockDim.x) ids_s[r] = ids[(size_t)t0 * k + r];
   }
   __syncthreads();
   if (warp == 0) {
-    const long r0 = (long)t0 * k, r1 = (long)t1 * k;
-    for (long base = r0; base < r1; base += 32) {
-      const long r = base + lane;
-      const int e = (r < r1) ? ids[r] : -1;
+    // Stable rank of every route inside the chunk: routes in row-major
+    // (token, slot) order, 32 at a time; peers with the same expert are ranked
+    // by lane, then the group's count is added to the expert's running count.
+    for (int base = 0; base < nr; base += 32) {
+      const int r = base + lane;
+      const int e = (r < nr) ? ids_s[r] : -1;
       const bool valid = (e >= 0 && e < E);
       const unsigned peers = __match_any_sync(kFull, valid ? e : -1);
       const int rank = __popc(peers & ((1u << lane) - 1u));
@@ -123,7 +131,7 @@ __global__ void __launch_bounds__(512) route_count_kernel(const float* __restric
       __syncwarp();
       if (valid && lane == leader) cnt[e] = before + __popc(peers);
       __syncwarp();
-      if (r < r1) s2d[r] = valid ? before + rank : -1;
+      if (r < nr) s2d[(size_t)t0 * k + r] = valid ? before + rank : -1;
     }
   }
   __syncthreads();
@@ -132,30 +140,42 @@ __global__ void __launch_bounds__(512) route_count_kernel(const float* __restric
 
 // Endpoints. With `counts` given, count[e] = counts[e]; otherwise count[e] is
 // the sum of the chunk histograms, which are replaced by per-chunk row bases
-// (start[e] + routes of e in earlier chunks).
+// (start[e] + routes of e in earlier chunks). One warp per expert scans the
+// chunk histograms (lanes over chunks); the block then scans the A-aligned
+// counts over experts.
 __global__ void __launch_bounds__(1024) endpoints_kernel(const int32_t* __restrict__ counts,
                                                          int32_t* __restrict__ ws, int nchunks, int E,
                                                          int A, int32_t* __restrict__ ends, long cap,
                                                          uint32_t* err) {
+  extern __shared__ int32_t cnt_s[];       // [E]
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   if (threadIdx.x == 0) carry = 0;
+  if (counts) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = counts[e];
+  } else {
+    for (int e = warp; e < E; e += nwarps) {
+      int run = 0;
+      for (int c0 = 0; c0 < nchunks; c0 += 32) {
+        const int c = c0 + lane;
+        const int v = (c < nchunks) ? ws[(size_t)c * E + e] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += n;
+        }
+        if (c < nchunks) ws[(size_t)c * E + e] = run + incl - v;
+        run += __shfl_sync(kFull, incl, 31);
+      }
+      if (lane == 0) cnt_s[e] = run;
+    }
+  }
   __syncthreads();
   for (int base = 0; base < E; base += 1024) {
     const int e = base + threadIdx.x;
-    int total = 0;
-    if (e < E) {
-      if (counts) {
-        total = counts[e];
-      } else {
-        for (int c = 0; c < nchunks; ++c) {
-          const int v = ws[(size_t)c * E + e];
-          ws[(size_t)c * E + e] = total;
-          total += v;
-        }
-      }
-    }
+    const int total = (e < E) ? cnt_s[e] : 0;
     const int aligned = (e < E) ? (int)align_up64(total, A) : 0;
     int v = aligned;
 #pragma unroll
@@ -178,12 +198,17 @@ __global__ void __launch_bounds__(1024) endpoints_kernel(const int32_t* __restri
     const int start = carry + (v - aligned) + (warp > 0 ? warp_sums[warp - 1] : 0);
     if (e < E) {
       ends[e] = start + total;
-      if (!counts)
-        for (int c = 0; c < nchunks; ++c) ws[(size_t)c * E + e] += start;
+      cnt_s[e] = start;  // reused below as the expert's start row
     }
     __syncthreads();
     if (threadIdx.x == 0) carry += warp_sums[31];
     __syncthreads();
+  }
+  if (!counts) {
+    for (int e = warp; e < E; e += nwarps) {
+      const int start = cnt_s[e];
+      for (int c = lane; c < nchunks; c += 32) ws[(size_t)c * E + e] += start;
+    }
   }
   if (threadIdx.x == 0 && E > 0 && cap >= 0 && (long)ends[E - 1] > cap) raise_error(err, MOE_DEVERR_CAPACITY);
 }
@@ -269,7 +294,7 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(const uint16_t* __re
 
 template <int EPL, int MODE>
 cudaError_t launch_route_count(const moe_route_args& a, int nchunks, cudaStream_t st) {
-  const size_t smem = (size_t)a.E * sizeof(int32_t);
+  const size_t smem = (size_t)(a.E + kScatterChunk * a.k) * sizeof(int32_t);
   route_count_kernel<EPL, MODE><<<nchunks, 512, smem, st>>>(
       a.logits, a.corr_bias, a.topk_ids, a.topk_w, a.src2dst, (int32_t*)a.workspace, a.T, a.E, a.k);
   return cudaGetLastError();
@@ -297,7 +322,7 @@ size_t route_scatter_ws_bytes(int T, int E, int k) {
 
 cudaError_t launch_expert_ends(const int32_t* counts, int E, int A, int32_t* ends, uint32_t* err,
                                cudaStream_t st) {
-  endpoints_kernel<<<1, 1024, 0, st>>>(counts, nullptr, 0, E, A, ends, -1, err);
+  endpoints_kernel<<<1, 1024, (size_t)E * sizeof(int32_t), st>>>(counts, nullptr, 0, E, A, ends, -1, err);
   return cudaGetLastError();
 }
 
@@ -313,8 +338,8 @@ cudaError_t launch_route_scatter(const moe_route_args& a, int num_sms, uint32_t*
       ce = launch_route_count<1, MOE_ROUTE_PRECOMPUTED>(a, nchunks, st);
     if (ce != cudaSuccess) return ce;
   }
-  endpoints_kernel<<<1, 1024, 0, st>>>(nullptr, (int32_t*)a.workspace, nchunks, a.E, a.A,
-                                      a.expert_ends, a.cap, err);
+  endpoints_kernel<<<1, 1024, (size_t)a.E * sizeof(int32_t), st>>>(nullptr, (int32_t*)a.workspace, nchunks,
+                                                                   a.E, a.A, a.expert_ends, a.cap, err);
   if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
   if (a.T > 0) {
     const int blocks = (int)lmin((a.T + 7) / 8, (long)num_sms * 16);
