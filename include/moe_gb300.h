@@ -191,9 +191,9 @@ MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t
  * memory (tcgen05, sm_103a). a [cap,K] e4m3; a_sf ASF [ceil(K/512)][ld_sf];
  * w, w_sf prepared by moe_prepare_weights in format w_format ([E][N][K/2]
  * packed e2m1 or [E][N][K] e4m3; scales [E][K/128][N]); out [cap,N] bf16.
- * Requires K % 128 == 0, N % 256 == 0, cap % 128 == 0, A == 128,
- * ld_sf >= cap, ld_sf % 4 == 0, 32-byte aligned w, 16-byte aligned a, a_sf,
- * w_sf and out. */
+ * Requires 1 <= E <= 4096, K % 128 == 0, N % 256 == 0, cap % 128 == 0,
+ * A == 128, ld_sf >= cap, ld_sf % 4 == 0, 32-byte aligned w, 16-byte
+ * aligned a, a_sf, w_sf and out. */
 MOE_API int moe_grouped_gemm(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf, int ld_sf,
                              const int32_t* expert_ends, int E, int A, int cap, const uint8_t* w,
                              const uint32_t* w_sf, int w_format, int N, int K, uint16_t* out,

@@ -160,7 +160,8 @@ MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t
 
 static int check_gemm(const moe::GemmArgs& g) {
   if (!g.a || !g.a_sf || !g.expert_ends || !g.w || !g.w_sf || !g.out) return MOE_ERR_INVALID_ARG;
-  if (g.E < 1 || g.N < 256 || g.N % 256 != 0 || g.K < 128 || g.K % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (g.E < 1 || g.E > 4096 || g.N < 256 || g.N % 256 != 0 || g.K < 128 || g.K % 128 != 0)
+    return MOE_ERR_INVALID_ARG;
   if (g.cap < 0 || g.cap % 128 != 0 || g.ld_sf < g.cap || g.ld_sf % 4 != 0) return MOE_ERR_INVALID_ARG;
   if (g.w_format != MOE_GEMM_W_E2M1 && g.w_format != MOE_GEMM_W_E4M3) return MOE_ERR_INVALID_ARG;
   if (!al(g.a, 16) || !al(g.w, 32) || !al(g.out, 16) || !al(g.a_sf, 16) || !al(g.w_sf, 16))

@@ -45,7 +45,10 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+#ifndef MOE_GEMM_STAGES
+#define MOE_GEMM_STAGES 4
+#endif
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = MOE_GEMM_STAGES;
 constexpr int kThreads = 256;
 constexpr uint32_t A_BYTES = BM * BK;
 constexpr uint32_t B_BYTES = BN * BK;
@@ -60,7 +63,9 @@ constexpr uint32_t OFF_BAR = OFF_SFA_IN + STAGES * SFA_BYTES;
 constexpr uint32_t NUM_BARS = 3 * STAGES + 3;
 constexpr uint32_t OFF_TMEM_PTR = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_PTR + 4;
-constexpr uint32_t SMEM_USED = OFF_ABORT + 4;
+constexpr uint32_t OFF_ENDS = OFF_ABORT + 12;                   // expert_ends copy, 16-byte aligned
+constexpr int kMaxExperts = 4096;
+constexpr uint32_t SMEM_USED = OFF_ENDS + kMaxExperts * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = 256;             // stage s: SFA cols 256+16s, SFB cols 264+16s
@@ -191,12 +196,13 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Expert of the live 128-row tile starting at m0: the smallest e with
-// align_up(end[e], 128) > m0 (start[e] <= m0 < end[e] follows).
-__device__ __forceinline__ int expert_of_tile(const int32_t* __restrict__ ends, int E, int m0) {
+// align_up(end[e], 128) > m0 (start[e] <= m0 < end[e] follows). `ends` is
+// the shared-memory copy of the endpoint tensor.
+__device__ __forceinline__ int expert_of_tile(const int32_t* ends, int E, int m0) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if ((int)align_up64(__ldg(ends + mid), BM) > m0) hi = mid; else lo = mid + 1;
+    if ((int)align_up64(ends[mid], BM) > m0) hi = mid; else lo = mid + 1;
   }
   return lo;
 }
@@ -220,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   const uint32_t tmem_empty_bar = bar0 + 8u * (3 * STAGES + 1);
   const uint32_t done_bar = bar0 + 8u * (3 * STAGES + 2);
 
+  int32_t* ends_s = reinterpret_cast<int32_t*>(smem + OFF_ENDS);
+  for (int i = threadIdx.x; i < E; i += blockDim.x) ends_s[i] = __ldg(ends + i);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 2);   // producer's expect_tx arrive + scale transposer's arrive
@@ -246,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
 
   const int KC = K / BK;
   const int n_tiles = N / BN;
-  int rows_aligned = (int)align_up64(__ldg(ends + E - 1), BM);
+  int rows_aligned = (int)align_up64(ends_s[E - 1], BM);
   if (rows_aligned > cap || rows_aligned < 0) {
     if (threadIdx.x == 0) raise_error(err, MOE_DEVERR_ENDPOINTS);
     rows_aligned = 0;
@@ -265,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
-        const int e = expert_of_tile(ends, E, m0);
+        const int e = expert_of_tile(ends_s, E, m0);
         for (int kc = 0; kc < KC; ++kc) {
           if (!(ok = wait_phase(empty_bar(s), ph ^ 1u, abort_flag, err))) break;
           mbar_arrive_expect_tx(sfa_bar(s), SFA_BYTES);
@@ -357,19 +365,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     uint32_t acc_ph = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
-      const int e = expert_of_tile(ends, E, m0);
-      const int row_end = __ldg(ends + e);
+      const int e = expert_of_tile(ends_s, E, m0);
+      const int row_end = ends_s[e];
       if (!wait_phase(tmem_full_bar, acc_ph, abort_flag, err)) break;
       tc_fence_after();
       uint32_t packed[BN / 2];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + 32u * c, r);
+      for (int c = 0; c < BN / 32; c += 2) {
+        uint32_t r0[32], r1[32];
+        tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + 32u * c, r0);
+        tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + 32u * (c + 1), r1);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          packed[16 * c + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        for (int i = 0; i < 16; ++i) {
+          packed[16 * c + i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+          packed[16 * (c + 1) + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+        }
       }
       tc_fence_before();
       __syncwarp();
