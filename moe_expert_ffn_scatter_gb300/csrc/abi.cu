@@ -5,7 +5,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 
-#include "../../include/moe_gb300.h"
+#include "moe_gb300.h"
 #include "kernels.h"
 
 struct moe_ctx {

@@ -25,22 +25,22 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j0 = 0; j0 < k; j0 += 4) {
-      int dst[4];
-      float wt[4];
-      uint4 v[4];
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      int dst[8];
+      float wt[8];
+      uint4 v[8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 8; ++q) {
         const int j = j0 + q;
         dst[q] = (j < k) ? s2d[(size_t)t * k + j] : -1;
         wt[q] = (j < k) ? topk_w[(size_t)t * k + j] : 0.0f;
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < 8; ++q)
         v[q] = (dst[q] >= 0) ? __ldg(reinterpret_cast<const uint4*>(down + (size_t)dst[q] * H) + c)
                              : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 8; ++q) {
         if (dst[q] < 0) continue;
         const uint32_t* pv = &v[q].x;
 #pragma unroll

@@ -15,7 +15,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/moe_gb300.h"
+#include "moe_gb300.h"
 
 namespace moe {
 
@@ -37,8 +37,12 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
   u += 0x7FFFu + ((u >> 16) & 1u);
   return u >> 16;
 }
+// Two fp32 -> packed bf16x2 (lo in bits 0-15), hardware round-to-nearest-even
+// (one cvt.rn.bf16x2.f32); equal to f32_to_bf16_bits on every non-NaN input.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return f32_to_bf16_bits(lo) | (f32_to_bf16_bits(hi) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // ------------------------------------------------------------------- e4m3

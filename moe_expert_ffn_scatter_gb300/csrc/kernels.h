@@ -5,7 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/moe_gb300.h"
+#include "moe_gb300.h"
 
 namespace moe {
 
