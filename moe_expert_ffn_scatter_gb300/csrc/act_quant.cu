@@ -52,14 +52,23 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
     const bool active = col < I;
     float h[16];
     float amax = 0.0f;
+    uint4 g0 = make_uint4(0, 0, 0, 0), g1 = g0, u0 = g0, u1 = g0;
     if (active) {
       const uint16_t* g = gateup + (size_t)row * 2 * I + col;
-      const uint4 g0 = __ldg(reinterpret_cast<const uint4*>(g));
-      const uint4 g1 = __ldg(reinterpret_cast<const uint4*>(g + 8));
-      const uint4 u0 = __ldg(reinterpret_cast<const uint4*>(g + I));
-      const uint4 u1 = __ldg(reinterpret_cast<const uint4*>(g + I + 8));
-      const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-      const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      g0 = __ldg(reinterpret_cast<const uint4*>(g));
+      g1 = __ldg(reinterpret_cast<const uint4*>(g + 8));
+      u0 = __ldg(reinterpret_cast<const uint4*>(g + I));
+      u1 = __ldg(reinterpret_cast<const uint4*>(g + I + 8));
+    }
+    const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    // Gate magnitudes stay below 87 in practice: then the whole warp takes
+    // the in-range exp (bitwise the same results, fewer instructions).
+    float gmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) gmax = fmaxf(gmax, fmaxf(fabsf(bf16_lo(gw[i])), fabsf(bf16_hi(gw[i]))));
+    const bool fast = __all_sync(kFull, gmax <= 87.0f);  // NaN gates fail the test
+    if (active) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float ga = bf16_lo(gw[i]), gb = bf16_hi(gw[i]);
@@ -70,7 +79,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
           ua = fminf(fmaxf(ua, -limit), limit);
           ub = fminf(fmaxf(ub, -limit), limit);
         }
-        const float2 hh = mul2(spec_silu2(make_float2(ga, gb)), make_float2(ua, ub));
+        const float2 hh = mul2(spec_silu2(make_float2(ga, gb), fast), make_float2(ua, ub));
         h[2 * i] = hh.x;
         h[2 * i + 1] = hh.y;
         amax = fmaxf(amax, fmaxf(fabsf(hh.x), fabsf(hh.y)));
