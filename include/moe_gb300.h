@@ -161,6 +161,32 @@ typedef struct moe_route_args {
 MOE_API size_t moe_route_scatter_workspace_size(int T, int E, int k);
 MOE_API int moe_route_scatter(moe_ctx* ctx, const moe_route_args* args, moe_stream_t stream);
 
+/* -------------------------------------------- route + scatter, no allocation
+ * The pages have no counterpart of this entry point.
+ *
+ * For callers that cannot allocate device memory: code that runs inside a
+ * host framework which plans and owns every device buffer and hands the
+ * library only the tensors of the operation, or code on a latency-critical
+ * path where an allocation (which may synchronise the device) is not allowed.
+ * They cannot provide the scratch workspace moe_route_scatter needs.
+ *
+ * Same operation, arguments, results and errors as moe_route_scatter, except
+ * that args->workspace and args->workspace_bytes are ignored: the scratch (the
+ * per-chunk expert histograms, ceil(T/64) * E int32) lives in a 1 MiB device
+ * array inside the library. Every GPU that loads the library holds that array
+ * until the process exits. Limit: ceil(T/64) * E * 4 <= 1 MiB (T <= 4096 with
+ * any E <= 4096; T = 65536 with E <= 256); larger sizes return
+ * MOE_ERR_UNSUPPORTED. Allocates nothing.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it: make that first call before any stream
+ * capture. All calls share the one array: calls that may overlap on the GPU
+ * (on different streams, or from different threads, without ordering between
+ * them) race and give wrong results; order them. Nothing in the array needs
+ * clearing between calls: each call writes every histogram entry before
+ * reading it. */
+MOE_API int moe_route_scatter_noalloc(moe_ctx* ctx, const moe_route_args* args, moe_stream_t stream);
+
 /* ------------------------------------------------------- weight prepare
  * Load-time (not on the hot path) re-layout of MXFP4 weights for the grouped
  * GEMM ([DG] §2.1.2 path A: weight scales are transformed once at load into

@@ -80,6 +80,7 @@ _SIGS = {
     "moe_expert_ends_from_counts": (_I, [_P, _P, _I, _I, _P, _P]),
     "moe_route_scatter_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "moe_route_scatter": (_I, [_P, ctypes.POINTER(moe_route_args), _P]),
+    "moe_route_scatter_noalloc": (_I, [_P, ctypes.POINTER(moe_route_args), _P]),
     "moe_prepare_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_gemm": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P]),
     "moe_act_quant": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.POINTER(moe_act_params), _P]),
@@ -178,6 +179,16 @@ def moe_route_scatter(ctx, *, routing_mode, x, topk_ids, expert_ends, src2dst, a
                        ptr(a_fp8), ptr(a_sf), ptr(expert_ends), ptr(src2dst), ptr(workspace),
                        workspace.numel() * workspace.element_size(), T, E, k, H, A, cap)
     _check("moe_route_scatter", load().moe_route_scatter(ctx.handle, ctypes.byref(a), cur_stream(stream)))
+
+
+def moe_route_scatter_noalloc(ctx, *, routing_mode, x, topk_ids, expert_ends, src2dst, a_fp8, a_sf,
+                              T, E, k, H, A, cap, logits=None, corr_bias=None, topk_w=None, stream=None):
+    """moe_route_scatter without a caller workspace: the library's built-in
+    scratch array is used (for callers that cannot allocate device memory)."""
+    a = moe_route_args(routing_mode, ptr(logits), ptr(corr_bias), ptr(topk_ids), ptr(topk_w), ptr(x),
+                       ptr(a_fp8), ptr(a_sf), ptr(expert_ends), ptr(src2dst), None, 0, T, E, k, H, A, cap)
+    _check("moe_route_scatter_noalloc",
+           load().moe_route_scatter_noalloc(ctx.handle, ctypes.byref(a), cur_stream(stream)))
 
 
 def moe_prepare_weights(ctx, w_in, sf_in, E, N, K, w_format, w_out, sf_out, stream=None):

@@ -146,6 +146,37 @@ MOE_API int moe_route_scatter(moe_ctx* ctx, const moe_route_args* a, moe_stream_
   return cuda_status(moe::launch_route_scatter(*a, ctx->num_sms, ctx->d_err, S(stream)));
 }
 
+// Argument checks of moe_route_scatter_noalloc: those of moe_route_scatter
+// minus the workspace, plus the size limit of the built-in scratch array.
+static int check_route_noalloc(const moe_route_args* a) {
+  if (a->T < 0 || a->E < 1 || a->E > 4096 || a->k < 1 || a->k > 32 || a->k > a->E || a->H < 128 ||
+      a->H % 128 != 0 || a->A < 1 || a->cap < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (a->routing_mode != MOE_ROUTE_SOFTMAX_TOPK && a->routing_mode != MOE_ROUTE_SIGMOID_BIAS_TOPK &&
+      a->routing_mode != MOE_ROUTE_PRECOMPUTED)
+    return MOE_ERR_INVALID_ARG;
+  if (a->routing_mode != MOE_ROUTE_PRECOMPUTED && (a->E > 1024 || !a->logits || !a->topk_w))
+    return MOE_ERR_INVALID_ARG;
+  if (a->routing_mode == MOE_ROUTE_SIGMOID_BIAS_TOPK && !a->corr_bias) return MOE_ERR_INVALID_ARG;
+  if (!a->topk_ids || !a->expert_ends) return MOE_ERR_INVALID_ARG;
+  if (a->T > 0 && (!a->x || !a->a_fp8 || !a->a_sf || !a->src2dst)) return MOE_ERR_INVALID_ARG;
+  if (a->T > 0 && (!al(a->x, 16) || !al(a->a_fp8, 8) || !al(a->a_sf, 4))) return MOE_ERR_INVALID_ARG;
+  if ((long)a->cap < (long)a->T * a->k + (long)a->E * (a->A - 1)) return MOE_ERR_CAPACITY;
+  if ((long)a->cap * a->H > 0x7FFFFFFFFFFFL) return MOE_ERR_INVALID_ARG;
+  if (moe::route_scatter_ws_bytes(a->T, a->E, a->k) > moe::route_scatter_noalloc_max_bytes())
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+MOE_API int moe_route_scatter_noalloc(moe_ctx* ctx, const moe_route_args* a, moe_stream_t stream) {
+  if (!ctx || !a) return MOE_ERR_INVALID_ARG;
+  const int rc = check_route_noalloc(a);
+  if (rc != MOE_OK) return rc;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return MOE_ERR_CUDA;
+  return cuda_status(moe::launch_route_scatter_noalloc(*a, ctx->device, ctx->num_sms, ctx->d_err, S(stream)));
+}
+
 MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t* sf_in, int E, int N,
                                 int K, int w_format, uint8_t* w_out, uint32_t* sf_out, moe_stream_t stream) {
   if (!ctx || !w_in || !sf_in || !w_out || !sf_out || E < 1 || N < 128 || N % 128 != 0 || K < 128 ||

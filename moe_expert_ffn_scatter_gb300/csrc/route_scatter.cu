@@ -21,6 +21,7 @@
 //      row is quantised once (16 lanes per 128-column group, uint4 loads) and
 //      its codes and packed scale words are stored to each destination row.
 #include <climits>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -349,6 +350,44 @@ cudaError_t launch_route_scatter(const moe_route_args& a, int num_sms, uint32_t*
     ce = cudaGetLastError();
   }
   return ce;
+}
+
+// ---------------------------------------------------- no-allocation variant
+// Scratch of moe_route_scatter_noalloc: the per-chunk expert histograms live
+// in this file-scope device array instead of a caller-provided workspace.
+// Every GPU that loads the library holds these 1 MiB until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
+static __device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+size_t route_scatter_noalloc_max_bytes() { return kNoAllocScratchBytes; }
+
+// `device` must be the current device. Its first call on a device looks the
+// array's device address up once (the host-side symbol is only a stand-in,
+// never a device address) and caches it.
+cudaError_t launch_route_scatter_noalloc(const moe_route_args& a, int device, int num_sms, uint32_t* err,
+                                         cudaStream_t st) {
+  if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[device]) {
+      void* p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+      if (e != cudaSuccess) return e;
+      g_scratch_addr[device] = p;
+    }
+    scratch = g_scratch_addr[device];
+  }
+  moe_route_args b = a;
+  b.workspace = scratch;
+  b.workspace_bytes = kNoAllocScratchBytes;
+  return launch_route_scatter(b, num_sms, err, st);
 }
 
 }  // namespace moe
