@@ -59,6 +59,28 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("grouped_gemm.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "moe_expert_ffn_scatter_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(name):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, or
+    None when the kernel source changed since those counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f).get(name)
+    if not d or d.get("source_sha256_16") != kernel_source_hash():
+        return None
+    return d["dram_bytes_per_launch"]
+
+
 def workload_config(cfg):
     return {"workload": cfg.name, "T": cfg.T, "E": cfg.E, "k": cfg.k, "H": cfg.H, "I": cfg.I, "A": cfg.A,
             "cap": cfg.cap, "routing": "softmax top-k, renormalised", "weights": "MXFP4 e2m1 + UE8M0 group 32",
@@ -286,7 +308,7 @@ def run_ours(args):
     }
     roofline = {"bound": "tensor", "kernel": "gemm1 (grouped_gemm_kernel, tcgen05 mxf8f6f4 block-scaled)",
                 "achieved": g1_tf, "peak": fp8_peak, "unit": "TFLOP/s", "frac": g1_tf / fp8_peak,
-                "traffic": None,
+                "traffic": recorded_traffic("gemm1"),
                 "peak_note": "%s sustained bf16 x 2 (dense FP8/FP6/FP4-in-mxf8f6f4 rate is twice bf16)" % pk_kind,
                 "algorithmic": "2*R*2I*H = %.1f GFLOP per launch over live rows only" % (g1_flop / 1e9)}
 
@@ -330,6 +352,7 @@ def run_ours(args):
     extras = {}
     if not args.no_extras:
         extras["act_quant_microbench"] = actq_microbench(ctx, B, synth, torch, np, hbm)
+        extras["decode_microbench"] = decode_microbench(ctx, B, synth, torch, np, hbm)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "us_per_layer": 1e3 * ms_step, "higher_is_better": True,
@@ -378,6 +401,61 @@ def actq_microbench(ctx, B, synth, torch, np, hbm, reps=50):
                           "live_rows": live_rows}
     if "full" in res and "dense" in res:
         res["full_over_dense"] = res["full"]["us"] / res["dense"]["us"]
+    return res
+
+
+def decode_microbench(ctx, B, synth, torch, np, hbm, n_layers=24, reps=5):
+    """gpt-oss-shaped sparse decode (E=32, top-4, H=I=2,880), FP8-per-expert and
+    MXFP4 weights, T in {1, 8}: 24 layers with their own weight copies run in
+    sequence, so L2 (126 MB) cannot serve the 0.4-0.8 GB of weights per layer.
+    Bytes counted: weights (+ scales, bias) of the distinct experts selected."""
+    d = synth.decode_inputs(8)
+    E, k, H, I = synth.DECODE_E, synth.DECODE_K, synth.DECODE_H, synth.DECODE_I
+    res = {}
+    for fmt_name, wfmt, W in (("fp8", B.MOE_WFMT_FP8_PER_EXPERT, d.fp8), ("mxfp4", B.MOE_WFMT_MXFP4_G32, d.mxfp4)):
+        layers = []
+        base = {kk: torch.from_numpy(np.ascontiguousarray(v)).cuda() for kk, v in W.items()}
+        for _ in range(n_layers):
+            layers.append({kk: v.clone() for kk, v in base.items()})
+        del base
+        per_expert = sum(v[0].numel() * v.element_size() for kk, v in layers[0].items() if kk not in ("gu_scale", "d_scale"))
+        for T in (1, 8):
+            x = torch.from_numpy(d.x[:T].view(np.int16)).view(torch.bfloat16).cuda()
+            # routing is an input of this call: the 4 largest generator logits per token,
+            # slot weights 1/4 each (the decode GEMVs' cost does not depend on them)
+            ids_np = np.argsort(-d.logits[:T], axis=1, kind="stable")[:, :k].astype(np.int32)
+            ids = torch.from_numpy(ids_np).cuda()
+            w = torch.full((T, k), 0.25, dtype=torch.float32, device="cuda")
+            uniq = len(set(ids_np.ravel().tolist()))
+            bf = lambda *shape: torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+            y1, act, y2, out = bf(T, k, 2 * I), bf(T * k, I), bf(T, k, H), bf(T, H)
+
+            def run_layers():
+                for L in layers:
+                    kw = (dict(w_gu_scale=L["gu_scale"], w_d_scale=L["d_scale"]) if wfmt == 0 else
+                          dict(w_gu_sf=L["gu_sf"], w_d_sf=L["d_sf"]))
+                    B.moe_sparse_gemv_decode(ctx, x=x, topk_ids=ids, topk_w=w, expert_start=0, num_local_experts=E,
+                                             wfmt=wfmt, w_gu=L["w_gu"], b_gu=L["b_gu"], w_d=L["w_d"], b_d=L["b_d"],
+                                             y1=y1, act=act, y2=y2, out=out, T=T, H=H, I=I, k=k, **kw)
+            run_layers()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                run_layers()
+            e1.record()
+            torch.cuda.synchronize()
+            us_layer = 1e3 * e0.elapsed_time(e1) / (reps * n_layers)
+            nbytes = uniq * per_expert
+            res["%s_T%d" % (fmt_name, T)] = {"us_per_layer": us_layer, "us_per_24_layers": us_layer * n_layers,
+                                             "unique_experts": uniq, "bytes_per_layer": nbytes,
+                                             "gbs": nbytes / (us_layer * 1e-6) / 1e9,
+                                             "frac_of_hbm": nbytes / (us_layer * 1e-6) / 1e9 / hbm}
+        del layers
+        torch.cuda.empty_cache()
+    if B.moe_get_device_error(ctx) != 0:
+        raise RuntimeError("device error in the decode microbench")
     return res
 
 
