@@ -19,7 +19,8 @@
  *  - Ownership: the caller allocates and owns every buffer, including the
  *    capacity workspaces; the library never allocates on the hot path, keeps
  *    no pointer after a call returns and never returns aliases. (Only
- *    moe_ctx_create allocates: the context and its 4-byte device error word.)
+ *    moe_ctx_create allocates: the context, its 4-byte device error word and
+ *    a 256 KB table of SiLU over all bf16 values, filled once on the device.)
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream) and enqueue a fixed launch structure that depends on the
  *    sizes only, never on routing counts: every call may be captured into a
@@ -93,7 +94,10 @@ typedef void* moe_stream_t; /* cudaStream_t */
 
 /* ------------------------------------------------------------- context
  * moe_ctx_create: binds `device`, reads its SM count, allocates the 4-byte
- *   device error word. Returns MOE_ERR_CUDA if the device is unusable.
+ *   device error word and the SiLU table (entry i = silu of the bf16 value
+ *   with bits i under the library's exp specification; the activation step
+ *   looks SiLU up there, its input being a bf16 gate value). Returns
+ *   MOE_ERR_CUDA if the device is unusable.
  * moe_ctx_destroy: frees the context (NULL is ignored).
  * moe_get_device_error: synchronises `stream`, reads the error word into
  *   *bits (host) and clears it. */
@@ -109,6 +113,13 @@ MOE_API int moe_version(void);
  * ([LR] §2, "概念伪代码"). One block; 1 <= E <= 8192. */
 MOE_API int moe_expert_ends_from_counts(moe_ctx* ctx, const int32_t* counts, int E, int A,
                                         int32_t* expert_ends, moe_stream_t stream);
+
+/* The activation between the GEMMs (moe_act_quant, moe_grouped_gemm_act_quant,
+ * moe_ffn_forward). */
+typedef struct moe_act_params {
+    int32_t kind;  /* MOE_ACT_* */
+    float limit;   /* L for SILU_CLAMP */
+} moe_act_params;
 
 /* ------------------------------------------------------ route + scatter
  * [LR] §2 ("scatter 在现有步骤内写出 int32 endpoint"), [DG] §2.2.4 (compact
@@ -200,9 +211,16 @@ MOE_API int moe_route_scatter_noalloc(moe_ctx* ctx, const moe_route_args* args, 
  *   MOE_GEMM_W_E4M3: the same values re-encoded exactly as e4m3 [E][N][K]
  *                    (twice the bytes; [DG] §2.1.2 path B does the same
  *                    lossless widening of e2m1 to e4m3)
- * Requires K % 128 == 0, N % 128 == 0; w_out must not overlap sf_out. */
+ * The flag MOE_GEMM_W_GATEUP_BLOCK128 (for w13 = [gate; up] halves, N = 2I)
+ * also reorders the rows (and their scales) so that output rows 256b..256b+127
+ * are gate rows 128b..128b+127 and rows 256b+128..256b+255 are up rows
+ * I+128b..: every 256-column GEMM tile then holds one matching gate/up group,
+ * which lets moe_ffn_forward run SiLU*mul and the quantisation inside GEMM1.
+ * Requires K % 128 == 0, N % 128 == 0 (N % 256 with the flag); w_out must not
+ * overlap sf_out, and must differ from w_in when widening or reordering. */
 #define MOE_GEMM_W_E2M1 0
 #define MOE_GEMM_W_E4M3 1
+#define MOE_GEMM_W_GATEUP_BLOCK128 2 /* flag, or-ed with the format: w13 only */
 MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t* sf_in, int E, int N,
                                 int K, int w_format, uint8_t* w_out, uint32_t* sf_out,
                                 moe_stream_t stream);
@@ -225,6 +243,22 @@ MOE_API int moe_grouped_gemm(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf
                              const uint32_t* w_sf, int w_format, int N, int K, uint16_t* out,
                              moe_stream_t stream);
 
+/* ------------------------------------- GEMM1 fused with SiLU*mul + quant
+ * GEMM1 of the live rows with the activation step in its epilogue: the
+ * operation of moe_grouped_gemm with w13 (N = 2I) prepared with
+ * MOE_GEMM_W_GATEUP_BLOCK128, followed by that of moe_act_quant on the
+ * bf16 gate/up values, without storing them ([DG] §2.4.1 fuses activation
+ * and quantisation to avoid a round trip of the intermediate; here the round
+ * trip of the GEMM1 output disappears too). Output: out_fp8 [cap, I] e4m3 and
+ * out_sf ASF [ceil(I/512)][align4(cap)], live rows only, bitwise equal to
+ * moe_grouped_gemm + moe_act_quant on the same inputs. Requires I % 128 == 0
+ * and the constraints of moe_grouped_gemm (K = H). */
+MOE_API int moe_grouped_gemm_act_quant(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf, int ld_sf,
+                                       const int32_t* expert_ends, int E, int A, int cap, const uint8_t* w13,
+                                       const uint32_t* w13_sf, int w_format, int I, int K,
+                                       const moe_act_params* act, uint8_t* out_fp8, int32_t* out_sf,
+                                       moe_stream_t stream);
+
 /* ---------------------------------------------------- activation quant
  * [LR] §2-3 (live-row activation kernel: 3-D grid with the expert on axis z,
  * grid-stride loop over [start[e], end[e]), padding left unwritten; a dense
@@ -239,10 +273,7 @@ MOE_API int moe_grouped_gemm(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf
  * gateup [M_alloc, 2I] bf16; out [M_alloc, I] e4m3; out_sf ASF
  * [ceil(I/512)][align4(M_alloc)]; expert_ends [E] or NULL (dense fallback:
  * every row of [0, M_alloc)). Requires I % 128 == 0, A >= 1. */
-typedef struct moe_act_params {
-    int32_t kind;  /* MOE_ACT_* */
-    float limit;   /* L for SILU_CLAMP */
-} moe_act_params;
+
 
 MOE_API int moe_act_quant(moe_ctx* ctx, const uint16_t* gateup, uint8_t* out, int32_t* out_sf,
                           const int32_t* expert_ends, int E, int A, int M_alloc, int I,
@@ -261,7 +292,10 @@ MOE_API int moe_combine(moe_ctx* ctx, const uint16_t* down, int H, const float* 
 /* ----------------------------------------------------------- FFN forward
  * GEMM1 -> act-quant -> GEMM2 -> combine on one stream, all driven by the
  * device-side expert_ends ([LR] §2 "FC1(endpoint) → SiLU+mul+quant(endpoint)
- * → FC2(endpoint)"). Inputs: a_fp8/a_sf/expert_ends/src2dst as written by
+ * → FC2(endpoint)"). When w13 was prepared with MOE_GEMM_W_GATEUP_BLOCK128
+ * (w_format carries the flag), SiLU*mul and the quantisation run in GEMM1's
+ * epilogue on its bf16-rounded accumulators, bitwise equal to the separate
+ * act-quant step, and `gateup` is not used (may be NULL). Inputs: a_fp8/a_sf/expert_ends/src2dst as written by
  * moe_route_scatter; topk_w [T,k]; w13 [E][2I][H/2] and w2 [E][H][I/2]
  * prepared with their scales by moe_prepare_weights. Workspaces (caller
  * owned, fixed capacity, contents need not be initialised): gateup

@@ -25,6 +25,7 @@ MOE_GLU_HALVES = 0
 MOE_GLU_INTERLEAVED = 1
 MOE_GEMM_W_E2M1 = 0
 MOE_GEMM_W_E4M3 = 1
+MOE_GEMM_W_GATEUP_BLOCK128 = 2
 MOE_DEVERR_EXPERT_ID = 0x1
 MOE_DEVERR_CAPACITY = 0x2
 MOE_DEVERR_WAIT_TIMEOUT = 0x4
@@ -83,6 +84,8 @@ _SIGS = {
     "moe_route_scatter_noalloc": (_I, [_P, ctypes.POINTER(moe_route_args), _P]),
     "moe_prepare_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_gemm": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_grouped_gemm_act_quant": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _I, _I, _I,
+                                        ctypes.POINTER(moe_act_params), _P, _P, _P]),
     "moe_act_quant": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.POINTER(moe_act_params), _P]),
     "moe_combine": (_I, [_P, _P, _I, _P, _P, _I, _I, _F, _P, _P]),
     "moe_ffn_forward": (_I, [_P, ctypes.POINTER(moe_ffn_args), _P]),
@@ -201,6 +204,15 @@ def moe_grouped_gemm(ctx, a, a_sf, ld_sf, expert_ends, E, A, cap, w, w_sf, w_for
     _check("moe_grouped_gemm",
            load().moe_grouped_gemm(ctx.handle, ptr(a), ptr(a_sf), ld_sf, ptr(expert_ends), E, A, cap, ptr(w),
                                    ptr(w_sf), w_format, N, K, ptr(out), cur_stream(stream)))
+
+
+def moe_grouped_gemm_act_quant(ctx, a, a_sf, ld_sf, expert_ends, E, A, cap, w13, w13_sf, w_format, I, K,
+                               out_fp8, out_sf, kind=MOE_ACT_SILU, limit=0.0, stream=None):
+    p = moe_act_params(kind, limit)
+    _check("moe_grouped_gemm_act_quant",
+           load().moe_grouped_gemm_act_quant(ctx.handle, ptr(a), ptr(a_sf), ld_sf, ptr(expert_ends), E, A, cap,
+                                             ptr(w13), ptr(w13_sf), w_format, I, K, ctypes.byref(p), ptr(out_fp8),
+                                             ptr(out_sf), cur_stream(stream)))
 
 
 def moe_act_quant(ctx, gateup, out, out_sf, expert_ends, E, A, M_alloc, I, kind=MOE_ACT_SILU, limit=0.0,

@@ -12,6 +12,7 @@ struct moe_ctx {
   int device;
   int num_sms;
   uint32_t* d_err;
+  float* d_silu;  // 65,536-entry SiLU table of the exp/SiLU specification
   moe::EncodeTiledFn encode;
 };
 
@@ -81,8 +82,14 @@ MOE_API int moe_ctx_create(moe_ctx** out, int device) {
     free(c);
     return MOE_ERR_CUDA;
   }
+  if (cudaMalloc(&c->d_silu, 65536 * sizeof(float)) != cudaSuccess) {
+    cudaFree(c->d_err);
+    free(c);
+    return MOE_ERR_CUDA;
+  }
   if (moe::init_grouped_gemm() != cudaSuccess || cudaMemset(c->d_err, 0, sizeof(uint32_t)) != cudaSuccess ||
-      cudaDeviceSynchronize() != cudaSuccess) {
+      moe::launch_silu_table(c->d_silu, 0) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(c->d_silu);
     cudaFree(c->d_err);
     free(c);
     return MOE_ERR_CUDA;
@@ -94,6 +101,7 @@ MOE_API int moe_ctx_create(moe_ctx** out, int device) {
 MOE_API int moe_ctx_destroy(moe_ctx* ctx) {
   if (!ctx) return MOE_OK;
   DeviceGuard g(ctx->device);
+  cudaFree(ctx->d_silu);
   cudaFree(ctx->d_err);
   free(ctx);
   return MOE_OK;
@@ -182,20 +190,22 @@ MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t
   if (!ctx || !w_in || !sf_in || !w_out || !sf_out || E < 1 || N < 128 || N % 128 != 0 || K < 128 ||
       K % 128 != 0)
     return MOE_ERR_INVALID_ARG;
-  if (w_format != MOE_GEMM_W_E2M1 && w_format != MOE_GEMM_W_E4M3) return MOE_ERR_INVALID_ARG;
-  if (w_format == MOE_GEMM_W_E4M3 && w_out == w_in) return MOE_ERR_INVALID_ARG;
-  if (!al(sf_out, 4) || (w_format == MOE_GEMM_W_E4M3 && !al(w_out, 2))) return MOE_ERR_INVALID_ARG;
+  if ((w_format & ~(MOE_GEMM_W_E4M3 | MOE_GEMM_W_GATEUP_BLOCK128)) != 0) return MOE_ERR_INVALID_ARG;
+  if ((w_format & MOE_GEMM_W_GATEUP_BLOCK128) && N % 256 != 0) return MOE_ERR_INVALID_ARG;
+  if ((w_format & (MOE_GEMM_W_E4M3 | MOE_GEMM_W_GATEUP_BLOCK128)) && w_out == w_in) return MOE_ERR_INVALID_ARG;
+  if (!al(sf_out, 4) || ((w_format & MOE_GEMM_W_E4M3) && !al(w_out, 2))) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
   return cuda_status(moe::launch_prepare_weights(w_in, sf_in, E, N, K, w_format, w_out, sf_out, S(stream)));
 }
 
 static int check_gemm(const moe::GemmArgs& g) {
-  if (!g.a || !g.a_sf || !g.expert_ends || !g.w || !g.w_sf || !g.out) return MOE_ERR_INVALID_ARG;
+  if (!g.a || !g.a_sf || !g.expert_ends || !g.w || !g.w_sf || (g.epi == 0 && !g.out)) return MOE_ERR_INVALID_ARG;
   if (g.E < 1 || g.E > 4096 || g.N < 256 || g.N % 256 != 0 || g.K < 128 || g.K % 128 != 0)
     return MOE_ERR_INVALID_ARG;
   if (g.cap < 0 || g.cap % 128 != 0 || g.ld_sf < g.cap || g.ld_sf % 4 != 0) return MOE_ERR_INVALID_ARG;
-  if (g.w_format != MOE_GEMM_W_E2M1 && g.w_format != MOE_GEMM_W_E4M3) return MOE_ERR_INVALID_ARG;
-  if (!al(g.a, 16) || !al(g.w, 32) || !al(g.out, 16) || !al(g.a_sf, 16) || !al(g.w_sf, 16))
+  if ((g.w_format & ~(MOE_GEMM_W_E4M3 | MOE_GEMM_W_GATEUP_BLOCK128)) != 0) return MOE_ERR_INVALID_ARG;
+  if (!al(g.a, 16) || !al(g.w, 32) || !al(g.a_sf, 16) || !al(g.w_sf, 16)) return MOE_ERR_INVALID_ARG;
+  if (g.epi == 0 ? (!al(g.out, 16)) : (!g.out_q || !g.out_sf || !al(g.out_q, 16) || g.N % 256 != 0))
     return MOE_ERR_INVALID_ARG;
   if ((long)g.E * g.N >= (1L << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -214,6 +224,29 @@ MOE_API int moe_grouped_gemm(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf
   return moe::launch_grouped_gemm(g, ctx->encode, ctx->num_sms, ctx->d_err, S(stream));
 }
 
+MOE_API int moe_grouped_gemm_act_quant(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf, int ld_sf,
+                                       const int32_t* expert_ends, int E, int A, int cap, const uint8_t* w13,
+                                       const uint32_t* w13_sf, int w_format, int I, int K,
+                                       const moe_act_params* act, uint8_t* out_fp8, int32_t* out_sf,
+                                       moe_stream_t stream) {
+  if (!ctx || !act || A != 128 || !(w_format & MOE_GEMM_W_GATEUP_BLOCK128)) return MOE_ERR_INVALID_ARG;
+  if (act->kind != MOE_ACT_SILU && act->kind != MOE_ACT_SILU_CLAMP) return MOE_ERR_INVALID_ARG;
+  if (I < 128 || I % 128 != 0) return MOE_ERR_INVALID_ARG;
+  moe::GemmArgs g{a, a_sf, ld_sf, expert_ends, E, cap, w13, w13_sf, w_format & MOE_GEMM_W_E4M3, 2 * I, K, nullptr};
+  g.epi = (act->kind == MOE_ACT_SILU_CLAMP) ? 2 : 1;
+  g.silu_tbl = ctx->d_silu;
+  g.out_q = out_fp8;
+  g.out_sf = out_sf;
+  g.ld_out_sf = (int)align4l(cap);
+  g.limit = act->limit;
+  int rc = check_gemm(g);
+  if (rc != MOE_OK) return rc;
+  if (!al(out_sf, 4)) return MOE_ERR_INVALID_ARG;
+  if (cap == 0) return MOE_OK;
+  DeviceGuard dg(ctx->device);
+  return moe::launch_grouped_gemm(g, ctx->encode, ctx->num_sms, ctx->d_err, S(stream));
+}
+
 MOE_API int moe_act_quant(moe_ctx* ctx, const uint16_t* gateup, uint8_t* out, int32_t* out_sf,
                           const int32_t* expert_ends, int E, int A, int M_alloc, int I,
                           const moe_act_params* act, moe_stream_t stream) {
@@ -224,7 +257,7 @@ MOE_API int moe_act_quant(moe_ctx* ctx, const uint16_t* gateup, uint8_t* out, in
   if (!al(gateup, 16) || !al(out, 16) || !al(out_sf, 4)) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
   return cuda_status(moe::launch_act_quant(gateup, out, out_sf, expert_ends, E, A, M_alloc, I, act->kind,
-                                           act->limit, ctx->num_sms, ctx->d_err, S(stream)));
+                                           act->limit, ctx->d_silu, ctx->num_sms, ctx->d_err, S(stream)));
 }
 
 MOE_API int moe_combine(moe_ctx* ctx, const uint16_t* down, int H, const float* topk_w,
@@ -241,24 +274,36 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* a, moe_stream_t st
   if (a->T < 0 || a->k < 1 || a->A != 128 || a->H % 256 != 0 || a->I % 128 != 0 || (2 * a->I) % 256 != 0 ||
       a->cap % 128 != 0)
     return MOE_ERR_INVALID_ARG;
-  if (!a->gateup || !a->act_fp8 || !a->act_sf || !a->down || !a->topk_w || !a->src2dst || !a->out)
+  const bool fused = (a->w_format & MOE_GEMM_W_GATEUP_BLOCK128) != 0;
+  if ((!fused && !a->gateup) || !a->act_fp8 || !a->act_sf || !a->down || !a->topk_w || !a->src2dst || !a->out)
     return MOE_ERR_INVALID_ARG;
   if (a->act.kind != MOE_ACT_SILU && a->act.kind != MOE_ACT_SILU_CLAMP) return MOE_ERR_INVALID_ARG;
   const int ld = (int)align4l(a->cap);
-  moe::GemmArgs g1{a->a_fp8, a->a_sf, ld, a->expert_ends, a->E, a->cap, a->w13, a->w13_sf, a->w_format,
+  const int fmt = a->w_format & MOE_GEMM_W_E4M3;
+  moe::GemmArgs g1{a->a_fp8, a->a_sf, ld, a->expert_ends, a->E, a->cap, a->w13, a->w13_sf, fmt,
                    2 * a->I, a->H, a->gateup};
-  moe::GemmArgs g2{a->act_fp8, a->act_sf, ld, a->expert_ends, a->E, a->cap, a->w2, a->w2_sf, a->w_format,
+  if (fused) {
+    g1.silu_tbl = ctx->d_silu;
+    g1.epi = (a->act.kind == MOE_ACT_SILU_CLAMP) ? 2 : 1;
+    g1.out_q = a->act_fp8;
+    g1.out_sf = a->act_sf;
+    g1.ld_out_sf = ld;
+    g1.limit = a->act.limit;
+  }
+  moe::GemmArgs g2{a->act_fp8, a->act_sf, ld, a->expert_ends, a->E, a->cap, a->w2, a->w2_sf, fmt,
                    a->H, a->I, a->down};
   int rc;
   if ((rc = check_gemm(g1)) != MOE_OK || (rc = check_gemm(g2)) != MOE_OK) return rc;
-  if (!al(a->gateup, 16) || !al(a->act_fp8, 16) || !al(a->down, 16) || !al(a->out, 16))
+  if ((!fused && !al(a->gateup, 16)) || !al(a->act_fp8, 16) || !al(a->act_sf, 4) || !al(a->down, 16) ||
+      !al(a->out, 16))
     return MOE_ERR_INVALID_ARG;
   DeviceGuard dg(ctx->device);
   if (a->cap > 0) {
     if ((rc = moe::launch_grouped_gemm(g1, ctx->encode, ctx->num_sms, ctx->d_err, S(stream))) != MOE_OK) return rc;
-    if ((rc = cuda_status(moe::launch_act_quant(a->gateup, a->act_fp8, a->act_sf, a->expert_ends, a->E, a->A,
-                                                a->cap, a->I, a->act.kind, a->act.limit, ctx->num_sms,
-                                                ctx->d_err, S(stream)))) != MOE_OK)
+    if (!fused &&
+        (rc = cuda_status(moe::launch_act_quant(a->gateup, a->act_fp8, a->act_sf, a->expert_ends, a->E, a->A,
+                                                a->cap, a->I, a->act.kind, a->act.limit, ctx->d_silu,
+                                                ctx->num_sms, ctx->d_err, S(stream)))) != MOE_OK)
       return rc;
     if ((rc = moe::launch_grouped_gemm(g2, ctx->encode, ctx->num_sms, ctx->d_err, S(stream))) != MOE_OK) return rc;
   }

@@ -28,7 +28,9 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
                                                              int32_t* __restrict__ out_sf,
                                                              const int32_t* __restrict__ ends, int E,
                                                              int A, int M_alloc, int I, int ld_sf,
-                                                             float limit, uint32_t* err) {
+                                                             float limit, const float* __restrict__ silu_tbl,
+                                                             uint32_t* err) {
+  const float silu_limit = kClamp ? spec_silu(limit) : 0.0f;
   int r0 = 0, r1 = M_alloc;
   if (kLive) {
     const int e = blockIdx.z;
@@ -62,24 +64,18 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
     }
     const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
     const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-    // Gate magnitudes stay below 87 in practice: then the whole warp takes
-    // the in-range exp (bitwise the same results, fewer instructions).
-    float gmax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) gmax = fmaxf(gmax, fmaxf(fabsf(bf16_lo(gw[i])), fabsf(bf16_hi(gw[i]))));
-    const bool fast = __all_sync(kFull, gmax <= 87.0f);  // NaN gates fail the test
     if (active) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        float ga = bf16_lo(gw[i]), gb = bf16_hi(gw[i]);
+        const float ga = bf16_lo(gw[i]), gb = bf16_hi(gw[i]);
         float ua = bf16_lo(uw[i]), ub = bf16_hi(uw[i]);
         if (kClamp) {
-          ga = fminf(ga, limit);
-          gb = fminf(gb, limit);
           ua = fminf(fmaxf(ua, -limit), limit);
           ub = fminf(fmaxf(ub, -limit), limit);
         }
-        const float2 hh = mul2(spec_silu2(make_float2(ga, gb), fast), make_float2(ua, ub));
+        const float sa = silu_of_bf16<kClamp>(silu_tbl, gw[i], ga, limit, silu_limit);
+        const float sb = silu_of_bf16<kClamp>(silu_tbl, gw[i] >> 16, gb, limit, silu_limit);
+        const float2 hh = mul2(make_float2(sa, sb), make_float2(ua, ub));
         h[2 * i] = hh.x;
         h[2 * i + 1] = hh.y;
         amax = fmaxf(amax, fmaxf(fabsf(hh.x), fabsf(hh.y)));
@@ -106,16 +102,22 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
 
 template <bool kLive>
 cudaError_t launch_kind(const uint16_t* gateup, uint8_t* out, int32_t* out_sf, const int32_t* ends,
-                        int E, int A, int M_alloc, int I, int kind, float limit, dim3 grid,
-                        uint32_t* err, cudaStream_t st) {
+                        int E, int A, int M_alloc, int I, int kind, float limit, const float* silu_tbl,
+                        dim3 grid, uint32_t* err, cudaStream_t st) {
   const int ld = (int)align_up64(M_alloc, 4);
   if (kind == MOE_ACT_SILU_CLAMP)
     act_quant_kernel<kLive, true><<<grid, kThreads, 0, st>>>(gateup, out, out_sf, ends, E, A, M_alloc, I,
-                                                           ld, limit, err);
+                                                           ld, limit, silu_tbl, err);
   else
     act_quant_kernel<kLive, false><<<grid, kThreads, 0, st>>>(gateup, out, out_sf, ends, E, A, M_alloc,
-                                                            I, ld, limit, err);
+                                                            I, ld, limit, silu_tbl, err);
   return cudaGetLastError();
+}
+
+// Entry i = spec_silu of the bf16 value with bits i.
+__global__ void silu_table_kernel(float* __restrict__ tbl) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < 65536) tbl[i] = spec_silu(bf16_to_f32((uint16_t)i));
 }
 
 }  // namespace
@@ -124,19 +126,24 @@ cudaError_t launch_kind(const uint16_t* gateup, uint8_t* out, int32_t* out_sf, c
 // chosen from the sizes only (never from the counts), so the launch can be
 // captured once and replayed: about 4 blocks per SM in total when the rows
 // are spread over the experts, at least 2 per expert.
+cudaError_t launch_silu_table(float* tbl, cudaStream_t st) {
+  silu_table_kernel<<<256, 256, 0, st>>>(tbl);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_act_quant(const uint16_t* gateup, uint8_t* out, int32_t* out_sf,
                              const int32_t* expert_ends, int E, int A, int M_alloc, int I, int kind,
-                             float limit, int num_sms, uint32_t* err, cudaStream_t st) {
+                             float limit, const float* silu_tbl, int num_sms, uint32_t* err, cudaStream_t st) {
   if (M_alloc == 0) return cudaSuccess;
   if (expert_ends) {
     if (E == 0) return cudaSuccess;
     const int gy = (int)lmin(lmax(2, (4L * num_sms + E - 1) / E), 65535);
-    return launch_kind<true>(gateup, out, out_sf, expert_ends, E, A, M_alloc, I, kind, limit,
+    return launch_kind<true>(gateup, out, out_sf, expert_ends, E, A, M_alloc, I, kind, limit, silu_tbl,
                              dim3(1, gy, E), err, st);
   }
   const long items = (long)M_alloc * (((I / 128) + 3) / 4);
   const int gy = (int)lmin((items + 7) / 8, 8L * num_sms);
-  return launch_kind<false>(gateup, out, out_sf, nullptr, 0, A, M_alloc, I, kind, limit,
+  return launch_kind<false>(gateup, out, out_sf, nullptr, 0, A, M_alloc, I, kind, limit, silu_tbl,
                             dim3(1, gy, 1), err, st);
 }
 

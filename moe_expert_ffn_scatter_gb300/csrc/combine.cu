@@ -63,7 +63,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 // holds the four bytes sf[e][n][4c .. 4c+3], byte 4c lowest; inside every
 // block of 128 rows, position 4 i + j holds row 32 j + i (the source layout of
 // tcgen05.cp 32x128b.warpx4, so the GEMM copies it without rearranging).
-__global__ void prepare_scales_kernel(const uint8_t* __restrict__ sf_in, int E, int N, int K,
+// Source row of output row n: identity, or (gate/up interleave in blocks of
+// 128) output rows 256b .. 256b+127 take gate rows 128b .., rows 256b+128 ..
+// take up rows N/2 + 128b ...
+__device__ __forceinline__ int src_row(int n, int N, bool blocked) {
+  if (!blocked) return n;
+  const int b = n >> 8, w = n & 255;
+  return (w < 128) ? (b << 7) + w : (N >> 1) + (b << 7) + (w - 128);
+}
+
+__global__ void prepare_scales_kernel(const uint8_t* __restrict__ sf_in, int E, int N, int K, bool blocked,
                                       uint32_t* __restrict__ sf_out) {
   const int KC = K / 128;
   const long total = (long)E * KC * N;
@@ -74,18 +83,28 @@ __global__ void prepare_scales_kernel(const uint8_t* __restrict__ sf_in, int E, 
     const long ec = i / N;
     const int c = (int)(ec % KC);
     const int e = (int)(ec / KC);
-    const uint8_t* p = sf_in + ((size_t)e * N + n) * (K / 32) + 4 * c;
+    const uint8_t* p = sf_in + ((size_t)e * N + src_row(n, N, blocked)) * (K / 32) + 4 * c;
     sf_out[i] = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
   }
 }
 
 // Packed e2m1 byte pairs -> e4m3 codes (exact: every e2m1 value is an e4m3
-// value). One thread per input byte, two output bytes.
-__global__ void widen_e2m1_kernel(const uint8_t* __restrict__ w_in, long nbytes, uint16_t* __restrict__ w_out) {
+// value), or a copy; rows remapped by src_row. One thread per output byte
+// pair (e4m3) or byte (e2m1).
+__global__ void weights_kernel(const uint8_t* __restrict__ w_in, int E, int N, int K, bool blocked, bool widen,
+                               uint8_t* __restrict__ w_out) {
+  const long rowb = K / 2;
+  const long nbytes = (long)E * N * rowb;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nbytes; i += (long)gridDim.x * blockDim.x) {
-    const uint32_t b = w_in[i];
-    const float lo = e2m1_to_f32(b & 0xFu), hi = e2m1_to_f32(b >> 4);
-    w_out[i] = (uint16_t)e4m3x2_satfinite(lo, hi);
+    const long rowi = i / rowb, col = i % rowb;
+    const int e = (int)(rowi / N), n = (int)(rowi % N);
+    const uint32_t b = w_in[((long)e * N + src_row(n, N, blocked)) * rowb + col];
+    if (widen) {
+      const float lo = e2m1_to_f32(b & 0xFu), hi = e2m1_to_f32(b >> 4);
+      reinterpret_cast<uint16_t*>(w_out)[i] = (uint16_t)e4m3x2_satfinite(lo, hi);
+    } else {
+      w_out[i] = (uint8_t)b;
+    }
   }
 }
 
@@ -102,21 +121,22 @@ cudaError_t launch_combine(const uint16_t* down, int H, const float* topk_w, con
 
 cudaError_t launch_prepare_weights(const uint8_t* w_in, const uint8_t* sf_in, int E, int N, int K,
                                    int w_format, uint8_t* w_out, uint32_t* sf_out, cudaStream_t st) {
+  const bool blocked = (w_format & MOE_GEMM_W_GATEUP_BLOCK128) != 0;
+  const bool widen = (w_format & MOE_GEMM_W_E4M3) != 0;
   const long words = (long)E * (K / 128) * N;
   if (words > 0) {
-    prepare_scales_kernel<<<(int)lmin((words + 255) / 256, 65535), 256, 0, st>>>(sf_in, E, N, K, sf_out);
+    prepare_scales_kernel<<<(int)lmin((words + 255) / 256, 65535), 256, 0, st>>>(sf_in, E, N, K, blocked, sf_out);
     cudaError_t ce = cudaGetLastError();
     if (ce != cudaSuccess) return ce;
   }
   const long nbytes = (long)E * N * (K / 2);
   if (nbytes == 0) return cudaSuccess;
-  if (w_format == MOE_GEMM_W_E4M3) {
-    widen_e2m1_kernel<<<(int)lmin((nbytes + 255) / 256, 65535), 256, 0, st>>>(
-        w_in, nbytes, reinterpret_cast<uint16_t*>(w_out));
-    return cudaGetLastError();
+  if (!blocked && !widen) {
+    if (w_out != w_in) return cudaMemcpyAsync(w_out, w_in, (size_t)nbytes, cudaMemcpyDeviceToDevice, st);
+    return cudaSuccess;
   }
-  if (w_out != w_in) return cudaMemcpyAsync(w_out, w_in, (size_t)nbytes, cudaMemcpyDeviceToDevice, st);
-  return cudaSuccess;
+  weights_kernel<<<(int)lmin((nbytes + 255) / 256, 65535), 256, 0, st>>>(w_in, E, N, K, blocked, widen, w_out);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -161,75 +161,14 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
 }
 __device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
 
-// The exp specification on a pair, bitwise equal to spec_exp on each half.
-// rint(t) is taken as (t + 1.5*2^23) - 1.5*2^23, exact round-to-nearest-even
-// for |t| < 2^22; 2^n is applied as 2^(n>>1) * 2^(n - (n>>1)): the first
-// product is exact (normal range) for every n this range produces, so the
-// result equals the n/2 split of the definition.
-__device__ __forceinline__ float2 spec_exp2(float2 x) {
-  const float kMagic = 12582912.0f;  // 1.5 * 2^23
-  const float2 t = mul2(x, splat2(__uint_as_float(0x3fb8aa3bu)));
-  const float2 y = add2(t, splat2(kMagic));
-  const float2 fn = add2(y, splat2(-kMagic));
-  const int n0 = __float_as_int(y.x) - 0x4B400000, n1 = __float_as_int(y.y) - 0x4B400000;
-  float2 r = fma2(make_float2(-fn.x, -fn.y), splat2(__uint_as_float(0x3f317000u)), x);
-  r = fma2(make_float2(-fn.x, -fn.y), splat2(__uint_as_float(0x3805fdf4u)), r);
-  float2 p = splat2(__uint_as_float(0x39500d01u));
-  p = fma2(p, r, splat2(__uint_as_float(0x3ab60b61u)));
-  p = fma2(p, r, splat2(__uint_as_float(0x3c088889u)));
-  p = fma2(p, r, splat2(__uint_as_float(0x3d2aaaabu)));
-  p = fma2(p, r, splat2(__uint_as_float(0x3e2aaaabu)));
-  p = fma2(p, r, splat2(0.5f));
-  p = fma2(p, r, splat2(1.0f));
-  p = fma2(p, r, splat2(1.0f));
-  const int h0 = n0 >> 1, h1 = n1 >> 1;
-  const float2 s1 = make_float2(__uint_as_float((uint32_t)(h0 + 127) << 23), __uint_as_float((uint32_t)(h1 + 127) << 23));
-  const float2 s2 = make_float2(__uint_as_float((uint32_t)(n0 - h0 + 127) << 23),
-                                __uint_as_float((uint32_t)(n1 - h1 + 127) << 23));
-  float2 res = mul2(mul2(p, s1), s2);
-  // out-of-range and NaN inputs, as in the scalar definition
-  if (!(x.x > -150.0f && x.x < 128.0f)) res.x = isnan(x.x) ? x.x : (x.x >= 128.0f ? __uint_as_float(0x7F800000u) : 0.0f);
-  if (!(x.y > -150.0f && x.y < 128.0f)) res.y = isnan(x.y) ? x.y : (x.y >= 128.0f ? __uint_as_float(0x7F800000u) : 0.0f);
-  return res;
-}
-
-// exp on a pair when both inputs lie in [-87, 87]: then n lies in
-// [-126, 126] and 2^n is a normal number, so p * 2^n is one correctly
-// rounded product, equal to the two-step scaling of the definition (whose
-// first step is exact). Callers take this path only when every lane of the
-// warp qualifies.
-__device__ __forceinline__ float2 spec_exp2_inrange(float2 x) {
-  const float kMagic = 12582912.0f;  // 1.5 * 2^23
-  const float2 t = mul2(x, splat2(__uint_as_float(0x3fb8aa3bu)));
-  const float2 y = add2(t, splat2(kMagic));
-  const float2 nfn = add2(splat2(kMagic), make_float2(-y.x, -y.y));  // -rint(t)
-  float2 r = fma2(nfn, splat2(__uint_as_float(0x3f317000u)), x);
-  r = fma2(nfn, splat2(__uint_as_float(0x3805fdf4u)), r);
-  float2 p = splat2(__uint_as_float(0x39500d01u));
-  p = fma2(p, r, splat2(__uint_as_float(0x3ab60b61u)));
-  p = fma2(p, r, splat2(__uint_as_float(0x3c088889u)));
-  p = fma2(p, r, splat2(__uint_as_float(0x3d2aaaabu)));
-  p = fma2(p, r, splat2(__uint_as_float(0x3e2aaaabu)));
-  p = fma2(p, r, splat2(0.5f));
-  p = fma2(p, r, splat2(1.0f));
-  p = fma2(p, r, splat2(1.0f));
-  // y's low mantissa bits hold n + 2^22 + 2^23 ... shifted: (bits(y) - bits(1.5*2^23) + 127) << 23
-  const float2 s2n = make_float2(__uint_as_float((uint32_t)(__float_as_int(y.x) - 0x4B400000 + 127) << 23),
-                                 __uint_as_float((uint32_t)(__float_as_int(y.y) - 0x4B400000 + 127) << 23));
-  return mul2(p, s2n);
-}
-
-// silu on a pair, bitwise equal to spec_silu on each half. `all_in_range`
-// must be warp-uniform and true only if every gate value the warp evaluates
-// lies in [-87, 87] (callers decide it with a vote before any divergence).
-__device__ __forceinline__ float2 spec_silu2(float2 g, bool all_in_range) {
-  float2 e;
-  if (all_in_range)
-    e = spec_exp2_inrange(make_float2(-g.x, -g.y));
-  else
-    e = spec_exp2(make_float2(-g.x, -g.y));
-  const float2 d = add2(splat2(1.0f), e);
-  return make_float2(__fdiv_rn(g.x, d.x), __fdiv_rn(g.y, d.y));
+// SiLU of a bf16 gate value through the per-context table (65,536 entries,
+// entry i = spec_silu(bf16 with bits i)); with the clamp, gate values above
+// the limit (or NaN) take spec_silu(limit) instead, as min(g, L) does.
+template <bool kClamp>
+__device__ __forceinline__ float silu_of_bf16(const float* __restrict__ tbl, uint32_t gbits, float g, float limit,
+                                              float silu_limit) {
+  if (kClamp && !(g <= limit) && !isnan(limit)) return silu_limit;
+  return __ldg(tbl + (gbits & 0xFFFFu));
 }
 
 // ------------------------------------------------------------------- e2m1

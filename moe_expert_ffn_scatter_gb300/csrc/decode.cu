@@ -48,51 +48,57 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(
   float acc[kColsPerWarp];
 #pragma unroll
   for (int q = 0; q < kColsPerWarp; ++q) acc[q] = 0.0f;
-  for (int c = lane; c < nchunk; c += 32) {
-    uint4 wv[kColsPerWarp];
+  // Two 16-byte chunks per row and lane in flight: 8 loads per lane per step.
+  for (int c0 = lane; c0 < nchunk; c0 += 64) {
+    uint4 wv[2][kColsPerWarp];
+    float sc[2][kColsPerWarp];
 #pragma unroll
-    for (int q = 0; q < kColsPerWarp; ++q) {
-      const int n = min(n0 + q, N - 1);
-      wv[q] = __ldg(reinterpret_cast<const uint4*>(W + ((size_t)lid * N + n) * row_bytes) + c);
-    }
-    float sc[kColsPerWarp];
-    if (WFMT == MOE_WFMT_MXFP4_G32) {
+    for (int u = 0; u < 2; ++u) {
+      const int c = c0 + 32 * u;
 #pragma unroll
       for (int q = 0; q < kColsPerWarp; ++q) {
         const int n = min(n0 + q, N - 1);
-        sc[q] = pow2_f32((int)wsf[((size_t)lid * N + n) * (K / 32) + c] - 127);
+        wv[u][q] = (c < nchunk) ? __ldg(reinterpret_cast<const uint4*>(W + ((size_t)lid * N + n) * row_bytes) + c)
+                                : make_uint4(0, 0, 0, 0);
+        if (WFMT == MOE_WFMT_MXFP4_G32)
+          sc[u][q] = (c < nchunk) ? pow2_f32((int)wsf[((size_t)lid * N + n) * (K / 32) + c] - 127) : 0.0f;
       }
     }
-    float part[kColsPerWarp];
 #pragma unroll
-    for (int q = 0; q < kColsPerWarp; ++q) part[q] = 0.0f;
+    for (int u = 0; u < 2; ++u) {
+      const int c = c0 + 32 * u;
+      if (c >= nchunk) break;
+      float part[kColsPerWarp];
 #pragma unroll
-    for (int i = 0; i < EPC / 4; ++i) {
-      const float4 xv = xs4[swz(c * (EPC / 4) + i)];
+      for (int q = 0; q < kColsPerWarp; ++q) part[q] = 0.0f;
 #pragma unroll
-      for (int q = 0; q < kColsPerWarp; ++q) {
-        const uint32_t* pw = &wv[q].x;
-        float w0, w1, w2, w3;
-        if (WFMT == MOE_WFMT_FP8_PER_EXPERT) {
-          const uint32_t word = pw[i];
-          const float2 a = e4m3x2_to_f32x2(word & 0xFFFFu);
-          const float2 b = e4m3x2_to_f32x2(word >> 16);
-          w0 = a.x; w1 = a.y; w2 = b.x; w3 = b.y;
-        } else {
-          const uint32_t word = pw[i >> 1] >> ((i & 1) * 16);
-          const float2 a = e2m1x2_to_f32x2(word & 0xFFu);
-          const float2 b = e2m1x2_to_f32x2((word >> 8) & 0xFFu);
-          w0 = a.x; w1 = a.y; w2 = b.x; w3 = b.y;
+      for (int i = 0; i < EPC / 4; ++i) {
+        const float4 xv = xs4[swz(c * (EPC / 4) + i)];
+#pragma unroll
+        for (int q = 0; q < kColsPerWarp; ++q) {
+          const uint32_t* pw = &wv[u][q].x;
+          float w0, w1, w2, w3;
+          if (WFMT == MOE_WFMT_FP8_PER_EXPERT) {
+            const uint32_t word = pw[i];
+            const float2 a = e4m3x2_to_f32x2(word & 0xFFFFu);
+            const float2 b = e4m3x2_to_f32x2(word >> 16);
+            w0 = a.x; w1 = a.y; w2 = b.x; w3 = b.y;
+          } else {
+            const uint32_t word = pw[i >> 1] >> ((i & 1) * 16);
+            const float2 a = e2m1x2_to_f32x2(word & 0xFFu);
+            const float2 b = e2m1x2_to_f32x2((word >> 8) & 0xFFu);
+            w0 = a.x; w1 = a.y; w2 = b.x; w3 = b.y;
+          }
+          part[q] = fmaf(w0, xv.x, part[q]);
+          part[q] = fmaf(w1, xv.y, part[q]);
+          part[q] = fmaf(w2, xv.z, part[q]);
+          part[q] = fmaf(w3, xv.w, part[q]);
         }
-        part[q] = fmaf(w0, xv.x, part[q]);
-        part[q] = fmaf(w1, xv.y, part[q]);
-        part[q] = fmaf(w2, xv.z, part[q]);
-        part[q] = fmaf(w3, xv.w, part[q]);
       }
-    }
 #pragma unroll
-    for (int q = 0; q < kColsPerWarp; ++q)
-      acc[q] = (WFMT == MOE_WFMT_MXFP4_G32) ? fmaf(part[q], sc[q], acc[q]) : acc[q] + part[q];
+      for (int q = 0; q < kColsPerWarp; ++q)
+        acc[q] = (WFMT == MOE_WFMT_MXFP4_G32) ? fmaf(part[q], sc[u][q], acc[q]) : acc[q] + part[q];
+    }
   }
 #pragma unroll
   for (int q = 0; q < kColsPerWarp; ++q)

@@ -207,11 +207,17 @@ __device__ __forceinline__ int expert_of_tile(const int32_t* ends, int E, int m0
   return lo;
 }
 
-template <bool kBfp4>
+// Epilogue kinds: bf16 output, or (GEMM1 with gate/up rows interleaved in
+// blocks of 128) SiLU*mul + e4m3/UE8M0 quantisation of the bf16-rounded
+// accumulators, optionally with the gate/up clamp.
+constexpr int kEpiBf16 = 0, kEpiSilu = 1, kEpiSiluClamp = 2;
+
+template <bool kBfp4, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
     const int32_t* __restrict__ a_sf, int ld_sf, const int32_t* __restrict__ ends, int E, int cap,
-    const uint32_t* __restrict__ w_sf, int N, int K, uint16_t* __restrict__ out, uint32_t* err) {
+    const uint32_t* __restrict__ w_sf, int N, int K, uint16_t* __restrict__ out, uint8_t* __restrict__ out_q,
+    int32_t* __restrict__ out_sf, int ld_out_sf, float limit, const float* __restrict__ silu_tbl, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -362,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   } else if (warp >= 4) {
     // ------------------------------------------------------ epilogue
     const int q = warp & 3;
+    const float silu_limit = (kEpi == kEpiSiluClamp) ? spec_silu(limit) : 0.0f;
     uint32_t acc_ph = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
@@ -386,11 +393,59 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty_bar);
       const int row = m0 + 32 * q + lane;
-      if (row < row_end) {
-        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * N + n0);
+      if (kEpi == kEpiBf16) {
+        if (row < row_end) {
+          uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * N + n0);
 #pragma unroll
-        for (int i = 0; i < BN / 8; ++i)
-          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          for (int i = 0; i < BN / 8; ++i)
+            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        }
+      } else {
+        // This thread holds its row's gate (columns 0-127) and up (128-255)
+        // of one 128-column group, already rounded to bf16 like the stored
+        // gate/up buffer of the unfused path; with the same SiLU table the
+        // result is bitwise that of the act-quant kernel on that buffer.
+        const int grp = n0 / BN;
+        const int I = N / 2;
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float ga = bf16_lo(packed[i]), gb = bf16_hi(packed[i]);
+          float ua = bf16_lo(packed[64 + i]), ub = bf16_hi(packed[64 + i]);
+          if (kEpi == kEpiSiluClamp) {
+            ua = fminf(fmaxf(ua, -limit), limit);
+            ub = fminf(fmaxf(ub, -limit), limit);
+          }
+          const float sa = silu_of_bf16<kEpi == kEpiSiluClamp>(silu_tbl, packed[i], ga, limit, silu_limit);
+          const float sb = silu_of_bf16<kEpi == kEpiSiluClamp>(silu_tbl, packed[i] >> 16, gb, limit, silu_limit);
+          const float2 hh = mul2(make_float2(sa, sb), make_float2(ua, ub));
+          packed[i] = __float_as_uint(hh.x);       // h[2i]
+          packed[64 + i] = __float_as_uint(hh.y);  // h[2i + 1]
+          amax = fmaxf(amax, fmaxf(fabsf(hh.x), fabsf(hh.y)));
+        }
+        const uint32_t b = group_scale_byte(amax);
+        if (row < row_end) {
+          const float sc = pow2_f32(127 - (int)b);
+          uint4* dst = reinterpret_cast<uint4*>(out_q + (size_t)row * I + (size_t)grp * 128);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            uint32_t wq[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const int j = 16 * v + 4 * w;  // h[j] = packed[j/2] (j even), packed[64 + j/2] (j odd)
+              const float h0 = __uint_as_float(packed[j / 2]), h1 = __uint_as_float(packed[64 + j / 2]);
+              const float h2 = __uint_as_float(packed[j / 2 + 1]), h3 = __uint_as_float(packed[64 + j / 2 + 1]);
+              wq[w] = e4m3x2_satfinite(__fmul_rn(h0, sc), __fmul_rn(h1, sc)) |
+                      (e4m3x2_satfinite(__fmul_rn(h2, sc), __fmul_rn(h3, sc)) << 16);
+            }
+            dst[v] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+          }
+          uint8_t* sfb = reinterpret_cast<uint8_t*>(out_sf) + ((size_t)(grp >> 2) * ld_out_sf + row) * 4;
+          sfb[grp & 3] = (uint8_t)b;
+          const int G = I / 128;
+          if (grp == G - 1)
+            for (int t = (grp & 3) + 1; t < 4; ++t) sfb[t] = 0;  // unused bytes of the last word
+        }
       }
       acc_ph ^= 1u;
     }
@@ -417,7 +472,7 @@ bool encode_2d(EncodeTiledFn encode, CUtensorMap* map, CUtensorMapDataType dt, c
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kBfp4>
+template <bool kBfp4, int kEpi>
 int launch_impl(const GemmArgs& g, EncodeTiledFn encode, int num_sms, uint32_t* err, cudaStream_t st) {
   CUtensorMap tmA, tmB;
   if (!encode_2d(encode, &tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a, (uint64_t)g.K, (uint64_t)g.cap,
@@ -432,24 +487,36 @@ int launch_impl(const GemmArgs& g, EncodeTiledFn encode, int num_sms, uint32_t* 
   const long max_tiles = (long)(g.cap / BM) * (g.N / BN);
   const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
   if (grid <= 0) return MOE_OK;
-  grouped_gemm_kernel<kBfp4><<<grid, kThreads, SMEM_BYTES, st>>>(tmA, tmB, g.a_sf, g.ld_sf, g.expert_ends, g.E,
-                                                                  g.cap, g.w_sf, g.N, g.K, g.out, err);
+  grouped_gemm_kernel<kBfp4, kEpi><<<grid, kThreads, SMEM_BYTES, st>>>(
+      tmA, tmB, g.a_sf, g.ld_sf, g.expert_ends, g.E, g.cap, g.w_sf, g.N, g.K, g.out, g.out_q, g.out_sf,
+      g.ld_out_sf, g.limit, g.silu_tbl, err);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+template <int kEpi>
+int launch_fmt(const GemmArgs& g, EncodeTiledFn encode, int num_sms, uint32_t* err, cudaStream_t st) {
+  if (g.w_format & MOE_GEMM_W_E4M3) return launch_impl<false, kEpi>(g, encode, num_sms, err, st);
+  return launch_impl<true, kEpi>(g, encode, num_sms, err, st);
 }
 
 }  // namespace
 
 cudaError_t init_grouped_gemm() {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(grouped_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)SMEM_BYTES);
+  const void* fns[] = {
+      (const void*)grouped_gemm_kernel<true, kEpiBf16>,  (const void*)grouped_gemm_kernel<false, kEpiBf16>,
+      (const void*)grouped_gemm_kernel<true, kEpiSilu>,  (const void*)grouped_gemm_kernel<false, kEpiSilu>,
+      (const void*)grouped_gemm_kernel<true, kEpiSiluClamp>, (const void*)grouped_gemm_kernel<false, kEpiSiluClamp>};
+  for (const void* f : fns) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, uint32_t* err, cudaStream_t st) {
-  if (g.w_format == MOE_GEMM_W_E4M3) return launch_impl<false>(g, encode, num_sms, err, st);
-  return launch_impl<true>(g, encode, num_sms, err, st);
+  if (g.epi == 1) return launch_fmt<kEpiSilu>(g, encode, num_sms, err, st);
+  if (g.epi == 2) return launch_fmt<kEpiSiluClamp>(g, encode, num_sms, err, st);
+  return launch_fmt<kEpiBf16>(g, encode, num_sms, err, st);
 }
 
 }  // namespace moe

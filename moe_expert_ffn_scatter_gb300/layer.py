@@ -18,7 +18,11 @@ def ceil_div(a, b):
 
 class MoEFFNLayer:
     def __init__(self, ctx, *, T, E, k, H, I, A=128, cap=None, routing=B.MOE_ROUTE_SOFTMAX_TOPK,
-                 act_kind=B.MOE_ACT_SILU, limit=0.0, rsf=1.0, w_format=B.MOE_GEMM_W_E2M1, device="cuda"):
+                 act_kind=B.MOE_ACT_SILU, limit=0.0, rsf=1.0, w_format=B.MOE_GEMM_W_E2M1, fused=True,
+                 device="cuda"):
+        """fused: run SiLU*mul and the quantisation in GEMM1's epilogue (w13 is
+        prepared with gate/up rows interleaved in blocks of 128); otherwise
+        GEMM1 writes the bf16 gate/up buffer and the act-quant kernel follows."""
         self.ctx = ctx
         self.T, self.E, self.k, self.H, self.I, self.A = T, E, k, H, I, A
         if cap is None:
@@ -27,6 +31,8 @@ class MoEFFNLayer:
         self.routing = routing
         self.act_kind, self.limit, self.rsf = act_kind, limit, rsf
         self.w_format = w_format
+        self.fused = fused
+        self.w13_format = w_format | (B.MOE_GEMM_W_GATEUP_BLOCK128 if fused else 0)
         dev = torch.device(device)
         u8, i32, f32, bf16 = torch.uint8, torch.int32, torch.float32, torch.bfloat16
         self.topk_ids = torch.empty((T, k), dtype=i32, device=dev)
@@ -36,7 +42,7 @@ class MoEFFNLayer:
         self.a_fp8 = torch.empty((cap, H), dtype=u8, device=dev)
         self.a_sf = torch.empty((ceil_div(H, 512), align4(cap)), dtype=i32, device=dev)
         self.ws = torch.empty((max(16, B.moe_route_scatter_workspace_size(T, E, k)),), dtype=u8, device=dev)
-        self.gateup = torch.empty((cap, 2 * I), dtype=bf16, device=dev)
+        self.gateup = None if fused else torch.empty((cap, 2 * I), dtype=bf16, device=dev)
         self.act_fp8 = torch.empty((cap, I), dtype=u8, device=dev)
         self.act_sf = torch.empty((ceil_div(I, 512), align4(cap)), dtype=i32, device=dev)
         self.down = torch.empty((cap, H), dtype=bf16, device=dev)
@@ -50,19 +56,21 @@ class MoEFFNLayer:
         dev = self.out.device
         E, H, I = self.E, self.H, self.I
 
-        def prep(w, sf, N, K):
+        def prep(w, sf, N, K, fmt):
             w_in = torch.as_tensor(w).to(dev).contiguous()
             sf_in = torch.as_tensor(sf).to(dev).contiguous()
-            if self.w_format == B.MOE_GEMM_W_E4M3:
+            if fmt & B.MOE_GEMM_W_E4M3:
                 w_out = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
+            elif fmt & B.MOE_GEMM_W_GATEUP_BLOCK128:
+                w_out = torch.empty((E, N, K // 2), dtype=torch.uint8, device=dev)
             else:
                 w_out = w_in
             sf_out = torch.empty((E, K // 128, N), dtype=torch.int32, device=dev)
-            B.moe_prepare_weights(self.ctx, w_in, sf_in, E, N, K, self.w_format, w_out, sf_out, stream=stream)
+            B.moe_prepare_weights(self.ctx, w_in, sf_in, E, N, K, fmt, w_out, sf_out, stream=stream)
             return w_out, sf_out
 
-        self.w13, self.w13_sf = prep(w13, w13_sf, 2 * I, H)
-        self.w2, self.w2_sf = prep(w2, w2_sf, H, I)
+        self.w13, self.w13_sf = prep(w13, w13_sf, 2 * I, H, self.w13_format)
+        self.w2, self.w2_sf = prep(w2, w2_sf, H, I, self.w_format)
 
     # ------------------------------------------------------------------ steps
     def route_scatter(self, x, logits=None, bias=None, stream=None):
@@ -76,7 +84,7 @@ class MoEFFNLayer:
                           w13_sf=self.w13_sf, w2=self.w2, w2_sf=self.w2_sf, gateup=self.gateup,
                           act_fp8=self.act_fp8, act_sf=self.act_sf, down=self.down, topk_w=self.topk_w,
                           src2dst=self.src2dst, out=self.out, T=self.T, E=self.E, k=self.k, H=self.H, I=self.I,
-                          A=self.A, cap=self.cap, w_format=self.w_format, act_kind=self.act_kind,
+                          A=self.A, cap=self.cap, w_format=self.w13_format, act_kind=self.act_kind,
                           limit=self.limit, rsf=self.rsf, stream=stream)
 
     def forward(self, x, logits=None, bias=None, stream=None):

@@ -129,11 +129,11 @@ def test_combine_bit_exact(ctx, orc):
 
 
 # ------------------------------------------------------------ whole layer
-def make_layer(ctx, cfg, inp, fmt=B.MOE_GEMM_W_E2M1):
+def make_layer(ctx, cfg, inp, fmt=B.MOE_GEMM_W_E2M1, fused=True):
     routing = B.MOE_ROUTE_SIGMOID_BIAS_TOPK if cfg.routing == "sigmoid_bias" else B.MOE_ROUTE_SOFTMAX_TOPK
     layer = MoEFFNLayer(ctx, T=cfg.T, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I, A=cfg.A, cap=cfg.cap, routing=routing,
                         act_kind=B.MOE_ACT_SILU_CLAMP if cfg.clamp else B.MOE_ACT_SILU, limit=cfg.limit,
-                        rsf=cfg.rsf, w_format=fmt)
+                        rsf=cfg.rsf, w_format=fmt, fused=fused)
     layer.load_weights(inp.w13, inp.w13_sf, inp.w2, inp.w2_sf)
     return layer
 
@@ -146,11 +146,13 @@ def oracle_layer(orc, cfg, inp):
     return ids, w
 
 
-def test_tiny_layer_vs_oracle(ctx, orc):
+@pytest.mark.parametrize("fused", [False, True], ids=["unfused", "fused"])
+def test_tiny_layer_vs_oracle(ctx, orc, fused):
     cfg = synth.TINY
     inp = synth.ffn_inputs(cfg)
-    layer = make_layer(ctx, cfg, inp)
-    for buf in (layer.gateup, layer.act_fp8, layer.down, layer.a_fp8):
+    layer = make_layer(ctx, cfg, inp, fused=fused)
+    bufs = [b for b in (layer.gateup, layer.act_fp8, layer.down, layer.a_fp8) if b is not None]
+    for buf in bufs:
         buf.view(torch.uint8).fill_(0xAB)
     out = layer.forward(dev_bf16(inp.x), dev(inp.logits))
     torch.cuda.synchronize()
@@ -158,7 +160,7 @@ def test_tiny_layer_vs_oracle(ctx, orc):
     ids, w = oracle_layer(orc, cfg, inp)
     ends, s2d, a, a_sf = orc.scatter(ids, inp.x, cfg.E, cfg.A, cfg.cap)
     live = live_rows(ends, cfg.cap)
-    for buf in (layer.gateup, layer.act_fp8, layer.down, layer.a_fp8):
+    for buf in bufs:
         assert np.all(host(buf.view(torch.uint8))[~live] == 0xAB), "padding rows written"
     assert np.array_equal(host(layer.expert_ends), ends)
     assert np.array_equal(host(layer.src2dst), s2d)
@@ -166,8 +168,38 @@ def test_tiny_layer_vs_oracle(ctx, orc):
     act, act_sf = orc.act_quant(gu, ends, cfg.A)
     down = orc.grouped_gemm(act, act_sf, ends, cfg.A, inp.w2, inp.w2_sf)
     ref = orc.combine(down, w, s2d, rsf=cfg.rsf)
-    assert_gemm_close(host_u16(layer.gateup), gu, ends, sentinel=None)
+    if not fused:
+        assert_gemm_close(host_u16(layer.gateup), gu, ends, sentinel=None)
     check_ffn_tolerance(host_u16(out), ref)
+
+
+@pytest.mark.parametrize("clamp", [False, True], ids=["silu", "silu_clamp"])
+@pytest.mark.parametrize("fmt", [B.MOE_GEMM_W_E2M1, B.MOE_GEMM_W_E4M3], ids=["e2m1", "e4m3"])
+def test_fused_act_quant_equals_separate_kernel(ctx, clamp, fmt):
+    """GEMM1 with SiLU*mul + quant in its epilogue gives bit for bit what
+    GEMM1 -> bf16 gate/up -> act-quant gives: codes, packed scales (including
+    the zero bytes of the last word when I/128 is not a multiple of 4) and the
+    layer output. I = 384: three groups of 128."""
+    cfg = synth.FFNConfig("fused", T=700, E=6, k=3, H=512, I=384, seed=14, clamp=clamp,
+                          limit=2.5 if clamp else 0.0)
+    inp = synth.ffn_inputs(cfg)
+    res = []
+    for fused in (False, True):
+        layer = make_layer(ctx, cfg, inp, fmt=fmt, fused=fused)
+        layer.act_fp8.fill_(0xAB)
+        layer.act_sf.view(torch.uint8).fill_(0xAB)
+        layer.forward(dev_bf16(inp.x), dev(inp.logits))
+        torch.cuda.synchronize()
+        assert B.moe_get_device_error(ctx) == 0
+        res.append((host(layer.act_fp8).copy(), host(layer.act_sf).copy(), host_u16(layer.out).copy(),
+                    host(layer.expert_ends).copy()))
+    (a0, s0, o0, e0), (a1, s1, o1, e1) = res
+    assert np.array_equal(e0, e1)
+    assert np.array_equal(a0, a1)
+    assert np.array_equal(s0, s1)
+    assert np.array_equal(o0, o1)
+    live = live_rows(e0, cfg.cap)
+    assert np.all(a1[~live] == 0xAB)
 
 
 def test_deepseek_layer_sampled_tokens(ctx, orc):
