@@ -150,8 +150,12 @@ def oracle_sample(cfg, inp, n_tokens, seed=0):
 def cpu_baseline(cfg, inp, budget_s=15.0):
     import oracle as orc
 
-    t1 = oracle_sample(cfg, inp, 2, seed=1)
-    n = int(max(2, min(cfg.T, budget_s / max(t1 / 2, 1e-6))))
+    # the oracle spreads tokens over the host threads: calibrate on one round
+    # of tokens per thread, then size the sample to about budget_s seconds
+    nt = max(1, orc.num_threads())
+    t1 = oracle_sample(cfg, inp, nt, seed=1)
+    rounds = int(max(1, budget_s / max(t1, 1e-6)))
+    n = int(min(cfg.T, nt * rounds))
     t = oracle_sample(cfg, inp, n, seed=2)
     return {"value": n * cfg.k / t, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
             "sample": "%d of %d tokens (%d routed rows) of the same layer: oracle routing + per-token "
@@ -168,9 +172,9 @@ def run_reference(args):
 
     cfg = synth.DEEPSEEK
     inp = synth.ffn_inputs(cfg)
-    t1 = oracle_sample(cfg, inp, 2, seed=1)
-    per_tok = t1 / 2
-    n = int(max(1, min(64, 4.0 / max(per_tok, 1e-6))))  # about 4 s of CPU work per step
+    nt = max(1, orc.num_threads())
+    t1 = oracle_sample(cfg, inp, nt, seed=1)
+    n = int(nt * max(1, int(4.0 / max(t1, 1e-6))))  # about 4 s of CPU work per step
     for i in range(args.warmup):
         oracle_sample(cfg, inp, n, seed=100 + i)
     times = [oracle_sample(cfg, inp, n, seed=1000 + i) for i in range(args.steps)]
