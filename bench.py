@@ -40,9 +40,11 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extras", action="store_true")
-    p.add_argument("--profile-kernel", choices=["route_scatter", "gemm1_act", "gemm2", "combine"],
+    p.add_argument("--profile-kernel", choices=["route_scatter", "gemm1_act", "gemm2", "combine", "act_quant"],
                    help="set up the layer, run one full step, then launch only this step's kernel "
-                        "warmup + steps times and exit (for ncu captures); prints no JSON line")
+                        "warmup + steps times and exit (for ncu captures); prints no JSON line. "
+                        "act_quant launches the standalone live-row act-quant kernel at the "
+                        "microbench shape (3,072 live of 28,672 rows, I = 2,048)")
     return p.parse_args()
 
 
@@ -192,6 +194,30 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------- ours
+def layer_parts(B, ctx, L, cfg, stream, x, logits, bias=None):
+    """The layer's four launch groups as closures, in step order: route +
+    scatter (3 kernels), GEMM1 with the fused SiLU*mul/quant epilogue, GEMM2,
+    combine."""
+    ld = L.a_sf.shape[1]
+
+    def route_scatter():
+        L.route_scatter(x, logits, bias, stream=stream)
+
+    def gemm1_act():
+        B.moe_grouped_gemm_act_quant(ctx, L.a_fp8, L.a_sf, ld, L.expert_ends, cfg.E, cfg.A, cfg.cap, L.w13,
+                                     L.w13_sf, L.w13_format, cfg.I, cfg.H, L.act_fp8, L.act_sf,
+                                     kind=L.act_kind, limit=L.limit, stream=stream)
+
+    def gemm2():
+        B.moe_grouped_gemm(ctx, L.act_fp8, L.act_sf, ld, L.expert_ends, cfg.E, cfg.A, cfg.cap, L.w2, L.w2_sf,
+                           L.w_format, cfg.H, cfg.I, L.down, stream=stream)
+
+    def combine():
+        B.moe_combine(ctx, L.down, cfg.H, L.topk_w, L.src2dst, cfg.T, cfg.k, cfg.rsf, L.out, stream=stream)
+
+    return {"route_scatter": route_scatter, "gemm1_act": gemm1_act, "gemm2": gemm2, "combine": combine}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -202,6 +228,9 @@ def run_ours(args):
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
+    if args.profile_kernel == "act_quant":
+        profile_act_quant(args, B, synth, torch, np, local)
+        return
     pg = None
     if world > 1:
         import torch.distributed as dist
@@ -217,42 +246,21 @@ def run_ours(args):
     logits = torch.from_numpy(inp.logits).cuda()
     stream = torch.cuda.current_stream()
     L = layer
-    ld = synth.align4(cfg.cap)
-
-    def gemm1_act():
-        B.moe_grouped_gemm_act_quant(ctx, L.a_fp8, L.a_sf, ld, L.expert_ends, cfg.E, cfg.A, cfg.cap, L.w13,
-                                     L.w13_sf, L.w13_format, cfg.I, cfg.H, L.act_fp8, L.act_sf, stream=stream)
-
-    def gemm2():
-        B.moe_grouped_gemm(ctx, L.act_fp8, L.act_sf, ld, L.expert_ends, cfg.E, cfg.A, cfg.cap, L.w2, L.w2_sf,
-                           L.w_format, cfg.H, cfg.I, L.down, stream=stream)
-
-    def combine():
-        B.moe_combine(ctx, L.down, cfg.H, L.topk_w, L.src2dst, cfg.T, cfg.k, cfg.rsf, L.out, stream=stream)
+    parts = layer_parts(B, ctx, L, cfg, stream, x, logits)
 
     def step(ev=None):
         # the same launches as MoEFFNLayer.forward (route_scatter + moe_ffn_forward
         # with the fused GEMM1), made through the component entry points so that
         # each kernel is timed inside the timed region
-        if ev is not None: ev[0].record(stream)
-        L.route_scatter(x, logits, stream=stream)
-        if ev is not None: ev[1].record(stream)
-        gemm1_act()
-        if ev is not None: ev[2].record(stream)
-        gemm2()
-        if ev is not None: ev[3].record(stream)
-        combine()
+        for j, f in enumerate(parts.values()):
+            if ev is not None: ev[j].record(stream)
+            f()
         if ev is not None: ev[4].record(stream)
 
     kernels_per_step = 3 + 1 + 1 + 1
     if args.profile_kernel:
         step()
-        only = {
-            "route_scatter": lambda: L.route_scatter(x, logits, stream=stream),
-            "gemm1_act": gemm1_act,
-            "gemm2": gemm2,
-            "combine": combine,
-        }[args.profile_kernel]
+        only = parts[args.profile_kernel]
         for _ in range(args.warmup + args.steps):
             only()
         torch.cuda.synchronize()
@@ -360,6 +368,7 @@ def run_ours(args):
     if not args.no_extras:
         extras["act_quant_microbench"] = actq_microbench(ctx, B, synth, torch, np, hbm)
         extras["decode_microbench"] = decode_microbench(ctx, B, synth, torch, np, hbm)
+        extras["kimi_layer"] = kimi_layer_bench(ctx, B, synth, torch, np, hbm, fp8_peak)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "us_per_layer": 1e3 * ms_step, "higher_is_better": True,
@@ -373,6 +382,86 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def profile_act_quant(args, B, synth, torch, np, device):
+    rows, I, E = synth.ACTQ_ROWS, synth.ACTQ_I, synth.ACTQ_E
+    ctx = B.Context(device)
+    gu, counts = synth.actq_inputs(full=False)
+    g = torch.from_numpy(gu.view(np.int16)).view(torch.bfloat16).cuda()
+    out = torch.empty((rows, I), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((I // 512, rows), dtype=torch.int32, device="cuda")
+    ends = torch.empty((E,), dtype=torch.int32, device="cuda")
+    B.moe_expert_ends_from_counts(ctx, torch.from_numpy(counts).cuda(), 128, ends)
+    for _ in range(args.warmup + args.steps):
+        B.moe_act_quant(ctx, g, out, sf, ends, E, 128, rows, I)
+    torch.cuda.synchronize()
+    if B.moe_get_device_error(ctx) != 0:
+        raise RuntimeError("device error")
+
+
+def kimi_layer_bench(ctx, B, synth, torch, np, hbm, fp8_peak, steps=5, warmup=3):
+    """The Kimi-shaped layer (E = 896, top-16, T = 2,048, H = 3,584, I = 3,072,
+    sigmoid + bias routing, clamp 25) at full size, timed kernel by kernel.
+    About 37 routes per expert: each expert's weights are used by one 128-row
+    tile, so the GEMMs stream 14.8 GB of MXFP4 weights per layer and are bound
+    by HBM, not by the tensor cores; both fractions are reported."""
+    from moe_expert_ffn_scatter_gb300.layer import MoEFFNLayer
+
+    cfg = synth.KIMI
+    inp = synth.ffn_inputs(cfg)
+    L = MoEFFNLayer(ctx, T=cfg.T, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I, A=cfg.A, cap=cfg.cap,
+                    routing=B.MOE_ROUTE_SIGMOID_BIAS_TOPK, act_kind=B.MOE_ACT_SILU_CLAMP, limit=cfg.limit,
+                    rsf=cfg.rsf)
+    L.load_expert_weights(lambda e: synth.expert_weights(cfg, e))
+    x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).cuda()
+    logits = torch.from_numpy(inp.logits).cuda()
+    bias = torch.from_numpy(inp.bias).cuda()
+    stream = torch.cuda.current_stream()
+    parts = list(layer_parts(B, ctx, L, cfg, stream, x, logits, bias).items())
+    for _ in range(warmup):
+        for _, f in parts:
+            f()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(steps)]
+    for i in range(steps):
+        for j, (_, f) in enumerate(parts):
+            evs[i][j].record(stream)
+            f()
+        evs[i][-1].record(stream)
+    torch.cuda.synchronize()
+    if B.moe_get_device_error(ctx) != 0:
+        raise RuntimeError("device error in the Kimi-shaped layer")
+    per = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps for j, (n, _) in
+           enumerate(parts)}
+    ends = L.expert_ends.cpu().numpy().astype(np.int64)
+    start = np.concatenate([[0], (ends[:-1] + cfg.A - 1) // cfg.A * cfg.A])
+    counts = ends - start
+    live_e = int((counts > 0).sum())
+    tiles = int(((counts + 127) // 128).sum())
+    R, H, I = cfg.R, cfg.H, cfg.I
+    w1_bytes = live_e * (2 * I * H // 2 + 2 * I * H // 32)
+    w2_bytes = live_e * (H * I // 2 + H * I // 32)
+    g1_bytes = w1_bytes + R * (H + H // 128) + R * (I + I // 128)
+    g2_bytes = w2_bytes + R * (I + I // 128) + R * H * 2
+
+    def gemm(name, flop, tile_flop, nbytes):
+        us = 1e3 * per[name]
+        return {"us": us, "tflops_live": flop / (us * 1e-6) / 1e12,
+                "frac_of_fp8_peak_live": flop / (us * 1e-6) / 1e12 / fp8_peak,
+                "frac_of_fp8_peak_issued": tile_flop / (us * 1e-6) / 1e12 / fp8_peak,
+                "gbs": nbytes / (us * 1e-6) / 1e9, "frac_of_hbm": nbytes / (us * 1e-6) / 1e9 / hbm,
+                "bytes": nbytes}
+
+    us_layer = 1e3 * sum(per.values())
+    res = {"workload": cfg.name, "us_per_layer": us_layer, "routed_rows_per_s": R / (us_layer * 1e-6),
+           "live_experts": live_e, "live_tiles": tiles,
+           "route_scatter_us": 1e3 * per["route_scatter"], "combine_us": 1e3 * per["combine"],
+           "gemm1_act": gemm("gemm1_act", 2.0 * R * 2 * I * H, 2.0 * tiles * 128 * 2 * I * H, g1_bytes),
+           "gemm2": gemm("gemm2", 2.0 * R * H * I, 2.0 * tiles * 128 * H * I, g2_bytes)}
+    del L, parts
+    torch.cuda.empty_cache()
+    return res
 
 
 def actq_microbench(ctx, B, synth, torch, np, hbm, reps=50):

@@ -6,6 +6,9 @@ runs in the library's kernels. Every buffer is allocated once at capacity and
 keeps its address, so `forward` can be captured into a CUDA graph and replayed
 with new routing (the endpoint tensor's contents change, its address does not).
 """
+from collections import deque
+from concurrent.futures import ThreadPoolExecutor
+
 import torch
 
 from . import binding as B
@@ -71,6 +74,29 @@ class MoEFFNLayer:
 
         self.w13, self.w13_sf = prep(w13, w13_sf, 2 * I, H, self.w13_format)
         self.w2, self.w2_sf = prep(w2, w2_sf, H, I, self.w_format)
+
+    def load_expert_weights(self, get_expert, stream=None, threads=8, window=16):
+        """Like load_weights, with the canonical arrays uploaded one expert at
+        a time: get_expert(e) -> (w13 [2I,H/2], w13_sf [2I,H/32], w2 [H,I/2],
+        w2_sf [H,I/32]) as host arrays, called from a few host threads; at most
+        `window` experts are held on the host at a time. The canonical device
+        copy of w13 is dropped once prepared."""
+        dev = self.out.device
+        E, H, I = self.E, self.H, self.I
+        u8 = torch.uint8
+        w13 = torch.empty((E, 2 * I, H // 2), dtype=u8, device=dev)
+        w13_sf = torch.empty((E, 2 * I, H // 32), dtype=u8, device=dev)
+        w2 = torch.empty((E, H, I // 2), dtype=u8, device=dev)
+        w2_sf = torch.empty((E, H, I // 32), dtype=u8, device=dev)
+        with ThreadPoolExecutor(threads) as ex:
+            pending = deque(ex.submit(get_expert, e) for e in range(min(window, E)))
+            for e in range(E):
+                parts = pending.popleft().result()
+                if e + window < E:
+                    pending.append(ex.submit(get_expert, e + window))
+                for dst, src in zip((w13, w13_sf, w2, w2_sf), parts):
+                    dst[e].copy_(torch.from_numpy(src))
+        self.load_weights(w13, w13_sf, w2, w2_sf, stream=stream)
 
     # ------------------------------------------------------------------ steps
     def route_scatter(self, x, logits=None, bias=None, stream=None):

@@ -9,7 +9,8 @@ Value recipes
   bf16 activations   fp32 N(0, std^2) rounded to bf16 (round to nearest even)
   router logits      fp32 N(0, 1); correction bias fp32 N(0, 0.1^2)
   MXFP4 weights      uniform random bytes: both e2m1 nibbles uniform over all
-                     16 codes (low nibble = even K index)
+                     16 codes (low nibble = even K index); the Kimi-shaped
+                     layer draws each expert from its own stream
   UE8M0 weight scale 127 + uniform integer exponent in [-6, -2]
   FP8 weights        e4m3 codes with random sign, exponent field uniform in
                      [4, 8] (magnitudes 2^-3 .. 2^1.9) and random mantissa --
@@ -100,6 +101,9 @@ class FFNConfig:
     clamp: bool = False
     limit: float = 0.0
     rsf: float = 1.0
+    # weights drawn expert by expert (expert_weights) instead of in one block,
+    # so that a consumer holds only the experts it needs on the host
+    per_expert_weights: bool = False
 
     @property
     def R(self):
@@ -117,7 +121,7 @@ DEEPSEEK = FFNConfig("DeepSeek-style W4A8 layer: E=32 top-6 T=4096 H=4096 I=2048
                      T=4096, E=32, k=6, H=4096, I=2048, seed=2)
 KIMI = FFNConfig("Kimi-K3-shaped layer: E=896 top-16 T=2048 H=3584 I=3072 clamp 25",
                  T=2048, E=896, k=16, H=3584, I=3072, seed=4, routing="sigmoid_bias",
-                 clamp=True, limit=25.0)
+                 clamp=True, limit=25.0, per_expert_weights=True)
 
 # The live-row activation-quant microbenchmark shape.
 ACTQ_ROWS = 28672
@@ -139,17 +143,41 @@ class FFNInputs:
 
 
 def ffn_inputs(cfg: FFNConfig, weights=True):
+    """Activations, router logits (+ correction bias) and, unless the config
+    draws its weights per expert, the four weight arrays."""
     g = rng(cfg.seed)
     x = bf16_normal(g, (cfg.T, cfg.H))
     logits = fp32_normal(g, (cfg.T, cfg.E))
     bias = fp32_normal(g, (cfg.E,), 0.1) if cfg.routing == "sigmoid_bias" else None
-    if not weights:
+    if not weights or cfg.per_expert_weights:
         return FFNInputs(x, logits, bias, None, None, None, None)
     w13 = e2m1_packed(g, (cfg.E, 2 * cfg.I, cfg.H // 2))
     w13_sf = ue8m0_bytes(g, (cfg.E, 2 * cfg.I, cfg.H // 32))
     w2 = e2m1_packed(g, (cfg.E, cfg.H, cfg.I // 2))
     w2_sf = ue8m0_bytes(g, (cfg.E, cfg.H, cfg.I // 32))
     return FFNInputs(x, logits, bias, w13, w13_sf, w2, w2_sf)
+
+
+def expert_weights(cfg: FFNConfig, e):
+    """MXFP4 weights of expert e alone, from its own stream (seed, 1, e):
+    w13 [2I, H/2], w13_sf [2I, H/32], w2 [H, I/2], w2_sf [H, I/32]. The byte
+    draws use Generator.bytes (uniform bytes, so both nibbles uniform)."""
+    g = rng([cfg.seed, 1, e])
+
+    def nibbles(shape):
+        return np.frombuffer(g.bytes(int(np.prod(shape))), np.uint8).reshape(shape).copy()
+
+    w13 = nibbles((2 * cfg.I, cfg.H // 2))
+    w13_sf = ue8m0_bytes(g, (2 * cfg.I, cfg.H // 32))
+    w2 = nibbles((cfg.H, cfg.I // 2))
+    w2_sf = ue8m0_bytes(g, (cfg.H, cfg.I // 32))
+    return w13, w13_sf, w2, w2_sf
+
+
+def stacked_expert_weights(cfg: FFNConfig, experts):
+    """expert_weights of the listed experts stacked along a new first axis."""
+    parts = [expert_weights(cfg, int(e)) for e in experts]
+    return tuple(np.stack([p[i] for p in parts]) for i in range(4))
 
 
 def actq_inputs(rows=ACTQ_ROWS, I=ACTQ_I, E=ACTQ_E, live=ACTQ_LIVE, seed=ACTQ_SEED, full=False):

@@ -216,6 +216,37 @@ def test_deepseek_layer_sampled_tokens(ctx, orc):
     check_ffn_tolerance(host_u16(out)[toks], ref)
 
 
+def test_kimi_layer_sampled_tokens(ctx, orc):
+    """Kimi-shaped layer at full size (E = 896, top-16, sigmoid + bias
+    routing, SiLU*mul with clamp 25, capacity 146,560 rows): routing, the
+    endpoint tensor and sampled output rows against the oracle. The oracle
+    takes each group of tokens with only the experts those tokens use."""
+    cfg = synth.KIMI
+    inp = synth.ffn_inputs(cfg)
+    layer = MoEFFNLayer(ctx, T=cfg.T, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I, A=cfg.A, cap=cfg.cap,
+                        routing=B.MOE_ROUTE_SIGMOID_BIAS_TOPK, act_kind=B.MOE_ACT_SILU_CLAMP,
+                        limit=cfg.limit, rsf=cfg.rsf)
+    layer.load_expert_weights(lambda e: synth.expert_weights(cfg, e))
+    out = layer.forward(dev_bf16(inp.x), dev(inp.logits), dev(inp.bias))
+    torch.cuda.synchronize()
+    assert B.moe_get_device_error(ctx) == 0
+    ids, w = orc.route_sigmoid_bias_topk(inp.logits, inp.bias, cfg.k)
+    assert np.array_equal(host(layer.topk_ids), ids)
+    _, ends = orc.endpoints(orc.expert_counts(ids, cfg.E), cfg.A)
+    assert np.array_equal(host(layer.expert_ends), ends)
+    got = host_u16(out)
+    toks = np.random.default_rng(15).choice(cfg.T, 16, replace=False).astype(np.int32)
+    for grp in toks.reshape(4, 4):
+        used = np.unique(ids[grp])
+        remap = np.full(cfg.E, -1, np.int32)
+        remap[used] = np.arange(used.size, dtype=np.int32)
+        w13, w13_sf, w2, w2_sf = synth.stacked_expert_weights(cfg, used)
+        ids_c = np.zeros_like(ids)
+        ids_c[grp] = remap[ids[grp]]
+        ref = orc.ffn_tokens(inp.x, ids_c, w, w13, w13_sf, w2, w2_sf, grp, clamp=True, limit=cfg.limit)
+        check_ffn_tolerance(got[grp], ref)
+
+
 def test_layer_graph_replay_permuted_routing_deterministic(ctx, orc):
     """Capture route+scatter+FFN once; replay with the logit columns permuted
     (new counts each time): equal to an eager run bit for bit."""
