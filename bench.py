@@ -40,11 +40,14 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extras", action="store_true")
-    p.add_argument("--profile-kernel", choices=["route_scatter", "gemm1_act", "gemm2", "combine", "act_quant"],
+    p.add_argument("--profile-kernel", choices=["route_scatter", "gemm1_act", "gemm2", "combine", "act_quant",
+                                                  "kimi_layer", "kimi_route_scatter"],
                    help="set up the layer, run one full step, then launch only this step's kernel "
                         "warmup + steps times and exit (for ncu captures); prints no JSON line. "
                         "act_quant launches the standalone live-row act-quant kernel at the "
-                        "microbench shape (3,072 live of 28,672 rows, I = 2,048)")
+                        "microbench shape (3,072 live of 28,672 rows, I = 2,048); kimi_layer runs "
+                        "the Kimi-shaped layer warmup + steps times and prints its timings; "
+                        "kimi_route_scatter launches only its routing + scatter (no weights)")
     return p.parse_args()
 
 
@@ -230,6 +233,31 @@ def run_ours(args):
     torch.cuda.set_device(local)
     if args.profile_kernel == "act_quant":
         profile_act_quant(args, B, synth, torch, np, local)
+        return
+    if args.profile_kernel == "kimi_route_scatter":
+        from moe_expert_ffn_scatter_gb300.layer import MoEFFNLayer
+        cfg = synth.KIMI
+        inp = synth.ffn_inputs(cfg)
+        L = MoEFFNLayer(B.Context(local), T=cfg.T, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I, A=cfg.A, cap=cfg.cap,
+                        routing=B.MOE_ROUTE_SIGMOID_BIAS_TOPK, act_kind=B.MOE_ACT_SILU_CLAMP, limit=cfg.limit)
+        x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).cuda()
+        logits, bias = torch.from_numpy(inp.logits).cuda(), torch.from_numpy(inp.bias).cuda()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for i in range(args.warmup + args.steps):
+            if i == args.warmup: ev[0].record()
+            L.route_scatter(x, logits, bias)
+        ev[1].record()
+        torch.cuda.synchronize()
+        if B.moe_get_device_error(L.ctx) != 0:
+            raise RuntimeError("device error")
+        print("route_scatter us %.2f" % (1e3 * ev[0].elapsed_time(ev[1]) / max(1, args.steps)))
+        return
+    if args.profile_kernel == "kimi_layer":
+        pk, _ = peaks()
+        fp8_peak = 2.0 * pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+        res = kimi_layer_bench(B.Context(local), B, synth, torch, np, pk["hbm_gbs"], fp8_peak,
+                               steps=args.steps, warmup=args.warmup)
+        print(json.dumps(res))
         return
     pg = None
     if world > 1:

@@ -7,19 +7,22 @@
 // [DG] §2.2.4 (compact layout: per-token-group quantisation, ep_scatter into
 // expert-contiguous segments) and 附录 C (src2dst).
 //
-// Three launches, all with grids fixed by (T, E, k, H) so a CUDA graph can
+// Four launches, all with grids fixed by (T, E, k, H) so a CUDA graph can
 // replay them while routing changes:
-//   1. route_count_kernel   one block per chunk of 64 tokens: routing (16
-//      warps, one token per warp at a time), then one warp ranks the chunk's
-//      routes per expert in row-major (token, slot) order with match_any and
-//      writes the rank inside the chunk to src2dst and the chunk histogram to
-//      the workspace.
-//   2. endpoints_kernel     one block: per expert, exclusive prefix of the
-//      chunk histograms (workspace becomes per-chunk row bases), block scan of
-//      the A-aligned counts -> start/end, expert_ends written.
-//   3. scatter_quant_kernel one warp per token: final src2dst, then the token
-//      row is quantised once (16 lanes per 128-column group, uint4 loads) and
-//      its codes and packed scale words are stored to each destination row.
+//   1. route_kernel         one warp per token: scores -> selection keys, top-k
+//      from per-lane sorted lists with warp max/min reductions, weights
+//      (skipped when the caller supplies the routing).
+//   2. rank_count_kernel    one block per chunk of 64 tokens: one warp ranks
+//      the chunk's routes per expert in row-major (token, slot) order with
+//      match_any; rank inside the chunk -> src2dst, chunk histogram ->
+//      workspace.
+//   3. endpoints_kernel     one block: per expert, exclusive prefix of the
+//      chunk histograms over chunks (coalesced, independent loads), then a
+//      block scan of the A-aligned counts -> expert_ends.
+//   4. scatter_quant_kernel one warp per token: final src2dst = start[e] +
+//      chunk prefix + rank, then the token row is quantised once (16 lanes per
+//      128-column group, uint4 loads) and its codes and packed scale words are
+//      stored to each destination row.
 #include <climits>
 #include <mutex>
 
@@ -32,50 +35,94 @@ namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
-// Routing of one token by one warp. Lane i holds logits e = i + 32 m.
+// Selection key of a routing score: a larger score has a larger key, +0 and
+// -0 share one key (they compare equal), NaN ranks below every number. Key 0
+// marks an entry that cannot be selected (already chosen, or e >= E).
+__device__ __forceinline__ uint32_t score_key(float s) {
+  if (s != s) return 1u;
+  uint32_t b = __float_as_uint(s);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// The lane's LN best selectable entries, best first. Slots are visited in
+// increasing order; a new entry goes in front of the first strictly smaller
+// key and the entries behind it move down one, so equal keys stay in slot
+// (= expert index) order.
+template <int EPL, int LN>
+__device__ __forceinline__ void build_list(const uint32_t (&key)[EPL], uint32_t removed, uint32_t (&lk)[LN],
+                                           int (&li)[LN]) {
+#pragma unroll
+  for (int p = 0; p < LN; ++p) {
+    lk[p] = 0u;
+    li[p] = 0;
+  }
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    uint32_t kk = ((removed >> i) & 1u) ? 0u : key[i];
+    int ii = i;
+    bool shifting = false;  // once the entry is placed, the rest move down one
+#pragma unroll
+    for (int p = 0; p < LN; ++p) {
+      const bool take = shifting || kk > lk[p];
+      shifting = take;
+      const uint32_t tk = lk[p];
+      const int ti = li[p];
+      lk[p] = take ? kk : tk;
+      li[p] = take ? ii : ti;
+      kk = take ? tk : kk;
+      ii = take ? ti : ii;
+    }
+  }
+}
+
+// Routing of one token by one warp. Lane i holds the scores of experts
+// e = i + 32 m as selection keys and keeps its best LN of them in a short
+// sorted list. Each of the k rounds takes the warp maximum of the list heads
+// (redux), the lowest expert index among the lanes holding it, and advances
+// the winner's list; a lane whose list runs dry rebuilds it from the entries
+// not yet chosen. The result is the top-k in descending score, ties to the
+// lower expert index.
 template <int EPL, int MODE>
 __device__ __forceinline__ void route_token(const float* __restrict__ l, const float* __restrict__ bias,
                                             int E, int k, int lane, int32_t* __restrict__ ids_out,
-                                            float* __restrict__ w_out, int32_t* ids_smem) {
-  float v[EPL];
-  uint32_t removed = 0;
+                                            float* __restrict__ w_out) {
+  constexpr int LN = EPL < 4 ? EPL : 4;
+  uint32_t key[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
-    float s = 0.0f;
+    uint32_t kk = 0u;
     if (e < E) {
-      const float x = l[e];
-      s = (MODE == MOE_ROUTE_SIGMOID_BIAS_TOPK) ? __fadd_rn(spec_sigmoid(x), bias[e]) : x;
-    } else {
-      removed |= 1u << i;
+      const float x = __ldg(l + e);
+      kk = score_key((MODE == MOE_ROUTE_SIGMOID_BIAS_TOPK) ? __fadd_rn(spec_sigmoid(x), __ldg(bias + e)) : x);
     }
-    v[i] = s;
+    key[i] = kk;
   }
+  uint32_t removed = 0u;
+  uint32_t lk[LN];
+  int li[LN];
+  build_list<EPL, LN>(key, removed, lk, li);
   int my_idx = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = 0.0f;
-    int bi = INT_MAX;
+    const uint32_t gmax = __reduce_max_sync(kFull, lk[0]);
+    const int cand = (lk[0] == gmax && gmax != 0u) ? lane + 32 * li[0] : INT_MAX;
+    const int gidx = __reduce_min_sync(kFull, cand);
+    if (lane == j) my_idx = gidx;
+    if (cand == gidx) {
+      removed |= 1u << li[0];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      if (!((removed >> i) & 1u) && (bi == INT_MAX || v[i] > bv)) {
-        bv = v[i];
-        bi = lane + 32 * i;
+      for (int p = 0; p + 1 < LN; ++p) {
+        lk[p] = lk[p + 1];
+        li[p] = li[p + 1];
       }
+      lk[LN - 1] = 0u;
+      if (LN < EPL && lk[0] == 0u) build_list<EPL, LN>(key, removed, lk, li);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, bv, o);
-      const int oi = __shfl_xor_sync(kFull, bi, o);
-      if (oi != INT_MAX && (bi == INT_MAX || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) removed |= 1u << (bi >> 5);
-    if (lane == j) my_idx = bi;
   }
   // Weights, slot j on lane j; sums run in slot order like the definition.
-  const float lj = (lane < k) ? l[my_idx] : 0.0f;
+  // (k <= E keeps a selectable entry in some list every round, so my_idx < E.)
+  const float lj = (lane < k && my_idx < E) ? l[my_idx] : 0.0f;
   float num;
   if (MODE == MOE_ROUTE_SIGMOID_BIAS_TOPK) {
     num = (lane < k) ? spec_sigmoid(lj) : 0.0f;
@@ -87,19 +134,28 @@ __device__ __forceinline__ void route_token(const float* __restrict__ l, const f
   for (int j = 0; j < k; ++j) s = __fadd_rn(s, __shfl_sync(kFull, num, j));
   if (lane < k) {
     ids_out[lane] = my_idx;
-    ids_smem[lane] = my_idx;
     w_out[lane] = __fdiv_rn(num, s);
   }
 }
 
+// One warp per token over the whole grid.
 template <int EPL, int MODE>
-__global__ void __launch_bounds__(512) route_count_kernel(const float* __restrict__ logits,
-                                                          const float* __restrict__ bias,
-                                                          int32_t* __restrict__ ids,
-                                                          float* __restrict__ topw,
-                                                          int32_t* __restrict__ s2d,
-                                                          int32_t* __restrict__ ws, int T, int E,
-                                                          int k) {
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits,
+                                                    const float* __restrict__ bias, int32_t* __restrict__ ids,
+                                                    float* __restrict__ topw, int T, int E, int k) {
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb)
+    route_token<EPL, MODE>(logits + (size_t)t * E, bias, E, k, lane, ids + (size_t)t * k, topw + (size_t)t * k);
+}
+
+// One block per chunk of kScatterChunk tokens: the chunk's routes are ranked
+// per expert in row-major (token, slot) order -- 32 at a time by one warp,
+// peers with the same expert ranked by lane via match_any -- and the rank
+// inside the chunk goes to src2dst, the chunk histogram to the workspace.
+__global__ void __launch_bounds__(256) rank_count_kernel(const int32_t* __restrict__ ids,
+                                                         int32_t* __restrict__ s2d, int32_t* __restrict__ ws,
+                                                         int T, int E, int k) {
   extern __shared__ int32_t smem_i32[];
   int32_t* cnt = smem_i32;                 // [E] running count per expert
   int32_t* ids_s = smem_i32 + E;           // [kScatterChunk * k] the chunk's expert ids
@@ -108,19 +164,10 @@ __global__ void __launch_bounds__(512) route_count_kernel(const float* __restric
   const int t1 = min(T, t0 + kScatterChunk);
   const int nr = (t1 - t0) * k;
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  if (MODE != MOE_ROUTE_PRECOMPUTED) {
-    for (int t = t0 + warp; t < t1; t += nwarps)
-      route_token<EPL, MODE>(logits + (size_t)t * E, bias, E, k, lane, ids + (size_t)t * k,
-                             topw + (size_t)t * k, ids_s + (t - t0) * k);
-  } else {
-    for (int r = threadIdx.x; r < nr; r += blockDim.x) ids_s[r] = ids[(size_t)t0 * k + r];
-  }
+  for (int r = threadIdx.x; r < nr; r += blockDim.x) ids_s[r] = ids[(size_t)t0 * k + r];
   __syncthreads();
-  if (warp == 0) {
-    // Stable rank of every route inside the chunk: routes in row-major
-    // (token, slot) order, 32 at a time; peers with the same expert are ranked
-    // by lane, then the group's count is added to the expert's running count.
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
     for (int base = 0; base < nr; base += 32) {
       const int r = base + lane;
       const int e = (r < nr) ? ids_s[r] : -1;
@@ -140,10 +187,12 @@ __global__ void __launch_bounds__(512) route_count_kernel(const float* __restric
 }
 
 // Endpoints. With `counts` given, count[e] = counts[e]; otherwise count[e] is
-// the sum of the chunk histograms, which are replaced by per-chunk row bases
-// (start[e] + routes of e in earlier chunks). One warp per expert scans the
-// chunk histograms (lanes over chunks); the block then scans the A-aligned
-// counts over experts.
+// the sum of the chunk histograms, which are replaced by their exclusive
+// prefix over chunks (routes of e in earlier chunks). P consecutive lanes
+// share an expert and split its chunks into P runs; each lane reads its run
+// with independent loads, the run totals are scanned across the P lanes, and
+// the run is written back. The block then scans the A-aligned counts over
+// experts: start[e] = align_up(end[e-1], A), end[e] = start[e] + count[e].
 __global__ void __launch_bounds__(1024) endpoints_kernel(const int32_t* __restrict__ counts,
                                                          int32_t* __restrict__ ws, int nchunks, int E,
                                                          int A, int32_t* __restrict__ ends, long cap,
@@ -151,26 +200,51 @@ __global__ void __launch_bounds__(1024) endpoints_kernel(const int32_t* __restri
   extern __shared__ int32_t cnt_s[];       // [E]
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) carry = 0;
   if (counts) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = counts[e];
   } else {
-    for (int e = warp; e < E; e += nwarps) {
-      int run = 0;
-      for (int c0 = 0; c0 < nchunks; c0 += 32) {
-        const int c = c0 + lane;
-        const int v = (c < nchunks) ? ws[(size_t)c * E + e] : 0;
-        int incl = v;
+    int P = 1;
+    while (P < 32 && E * P * 2 <= (int)blockDim.x) P *= 2;
+    const int sub = threadIdx.x & (P - 1);
+    const int groups = blockDim.x / P;
+    const int L = (nchunks + P - 1) / P;
+    const int c_lo = min(nchunks, sub * L), c_hi = min(nchunks, c_lo + L);
+    constexpr int U = 8;
+    const int iters = (E + groups - 1) / groups;  // the same in every lane of a warp
+    for (int it = 0; it < iters; ++it) {
+      const int e = it * groups + (int)threadIdx.x / P;
+      const bool ok = e < E;
+      int tot = 0;
+      if (ok) {
+        for (int c0 = c_lo; c0 < c_hi; c0 += U) {
+          int v[U];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int n = __shfl_up_sync(kFull, incl, o);
-          if (lane >= o) incl += n;
+          for (int u = 0; u < U; ++u) v[u] = (c0 + u < c_hi) ? ws[(size_t)(c0 + u) * E + e] : 0;
+#pragma unroll
+          for (int u = 0; u < U; ++u) tot += v[u];
         }
-        if (c < nchunks) ws[(size_t)c * E + e] = run + incl - v;
-        run += __shfl_sync(kFull, incl, 31);
       }
-      if (lane == 0) cnt_s[e] = run;
+      int incl = tot;
+      for (int o = 1; o < P; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, incl, o, P);
+        if (sub >= o) incl += n;
+      }
+      if (ok) {
+        int run = incl - tot;
+        for (int c0 = c_lo; c0 < c_hi; c0 += U) {
+          int v[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) v[u] = (c0 + u < c_hi) ? ws[(size_t)(c0 + u) * E + e] : 0;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            if (c0 + u < c_hi) ws[(size_t)(c0 + u) * E + e] = run;
+            run += v[u];
+          }
+        }
+        if (sub == P - 1) cnt_s[e] = incl;
+      }
     }
   }
   __syncthreads();
@@ -197,19 +271,10 @@ __global__ void __launch_bounds__(1024) endpoints_kernel(const int32_t* __restri
     }
     __syncthreads();
     const int start = carry + (v - aligned) + (warp > 0 ? warp_sums[warp - 1] : 0);
-    if (e < E) {
-      ends[e] = start + total;
-      cnt_s[e] = start;  // reused below as the expert's start row
-    }
+    if (e < E) ends[e] = start + total;
     __syncthreads();
     if (threadIdx.x == 0) carry += warp_sums[31];
     __syncthreads();
-  }
-  if (!counts) {
-    for (int e = warp; e < E; e += nwarps) {
-      const int start = cnt_s[e];
-      for (int c = lane; c < nchunks; c += 32) ws[(size_t)c * E + e] += start;
-    }
   }
   if (threadIdx.x == 0 && E > 0 && cap >= 0 && (long)ends[E - 1] > cap) raise_error(err, MOE_DEVERR_CAPACITY);
 }
@@ -223,9 +288,10 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(const uint16_t* __re
                                                             const int32_t* __restrict__ ids,
                                                             int32_t* __restrict__ s2d,
                                                             const int32_t* __restrict__ ws,
+                                                            const int32_t* __restrict__ ends,
                                                             uint8_t* __restrict__ a_fp8,
                                                             int32_t* __restrict__ a_sf, int T, int E,
-                                                            int k, int H, int ld_sf, long cap,
+                                                            int k, int A, int H, int ld_sf, long cap,
                                                             uint32_t* err) {
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
@@ -237,7 +303,8 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(const uint16_t* __re
       const int e = ids[(size_t)t * k + lane];
       const int lr = s2d[(size_t)t * k + lane];
       if (e >= 0 && e < E && lr >= 0) {
-        dst = ws[(size_t)(t / kScatterChunk) * E + e] + lr;
+        const int start = (e == 0) ? 0 : (int)align_up64(ends[e - 1], A);
+        dst = start + ws[(size_t)(t / kScatterChunk) * E + e] + lr;
         if ((long)dst >= cap) {
           raise_error(err, MOE_DEVERR_CAPACITY);
           dst = -1;
@@ -294,22 +361,22 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(const uint16_t* __re
 }
 
 template <int EPL, int MODE>
-cudaError_t launch_route_count(const moe_route_args& a, int nchunks, cudaStream_t st) {
-  const size_t smem = (size_t)(a.E + kScatterChunk * a.k) * sizeof(int32_t);
-  route_count_kernel<EPL, MODE><<<nchunks, 512, smem, st>>>(
-      a.logits, a.corr_bias, a.topk_ids, a.topk_w, a.src2dst, (int32_t*)a.workspace, a.T, a.E, a.k);
+cudaError_t launch_route(const moe_route_args& a, int num_sms, cudaStream_t st) {
+  const int blocks = (int)lmin((a.T + 7) / 8, (long)num_sms * 8);
+  route_kernel<EPL, MODE><<<blocks, 256, 0, st>>>(a.logits, a.corr_bias, a.topk_ids, a.topk_w, a.T, a.E, a.k);
   return cudaGetLastError();
 }
 
 template <int MODE>
-cudaError_t dispatch_epl(const moe_route_args& a, int nchunks, cudaStream_t st) {
+cudaError_t dispatch_epl(const moe_route_args& a, int num_sms, cudaStream_t st) {
   const int epl = (a.E + 31) / 32;
-  if (epl <= 1) return launch_route_count<1, MODE>(a, nchunks, st);
-  if (epl <= 2) return launch_route_count<2, MODE>(a, nchunks, st);
-  if (epl <= 4) return launch_route_count<4, MODE>(a, nchunks, st);
-  if (epl <= 8) return launch_route_count<8, MODE>(a, nchunks, st);
-  if (epl <= 16) return launch_route_count<16, MODE>(a, nchunks, st);
-  return launch_route_count<32, MODE>(a, nchunks, st);
+  if (epl <= 1) return launch_route<1, MODE>(a, num_sms, st);
+  if (epl <= 2) return launch_route<2, MODE>(a, num_sms, st);
+  if (epl <= 4) return launch_route<4, MODE>(a, num_sms, st);
+  if (epl <= 8) return launch_route<8, MODE>(a, num_sms, st);
+  if (epl <= 16) return launch_route<16, MODE>(a, num_sms, st);
+  if (epl <= 24) return launch_route<24, MODE>(a, num_sms, st);
+  return launch_route<32, MODE>(a, num_sms, st);
 }
 
 }  // namespace
@@ -330,14 +397,15 @@ cudaError_t launch_expert_ends(const int32_t* counts, int E, int A, int32_t* end
 cudaError_t launch_route_scatter(const moe_route_args& a, int num_sms, uint32_t* err, cudaStream_t st) {
   const int nchunks = (a.T + kScatterChunk - 1) / kScatterChunk;
   cudaError_t ce = cudaSuccess;
-  if (nchunks > 0) {
+  if (a.T > 0) {
     if (a.routing_mode == MOE_ROUTE_SOFTMAX_TOPK)
-      ce = dispatch_epl<MOE_ROUTE_SOFTMAX_TOPK>(a, nchunks, st);
+      ce = dispatch_epl<MOE_ROUTE_SOFTMAX_TOPK>(a, num_sms, st);
     else if (a.routing_mode == MOE_ROUTE_SIGMOID_BIAS_TOPK)
-      ce = dispatch_epl<MOE_ROUTE_SIGMOID_BIAS_TOPK>(a, nchunks, st);
-    else
-      ce = launch_route_count<1, MOE_ROUTE_PRECOMPUTED>(a, nchunks, st);
+      ce = dispatch_epl<MOE_ROUTE_SIGMOID_BIAS_TOPK>(a, num_sms, st);
     if (ce != cudaSuccess) return ce;
+    const size_t smem = (size_t)(a.E + kScatterChunk * a.k) * sizeof(int32_t);
+    rank_count_kernel<<<nchunks, 256, smem, st>>>(a.topk_ids, a.src2dst, (int32_t*)a.workspace, a.T, a.E, a.k);
+    if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
   }
   endpoints_kernel<<<1, 1024, (size_t)a.E * sizeof(int32_t), st>>>(nullptr, (int32_t*)a.workspace, nchunks,
                                                                    a.E, a.A, a.expert_ends, a.cap, err);
@@ -345,7 +413,7 @@ cudaError_t launch_route_scatter(const moe_route_args& a, int num_sms, uint32_t*
   if (a.T > 0) {
     const int blocks = (int)lmin((a.T + 7) / 8, (long)num_sms * 16);
     scatter_quant_kernel<<<blocks, 256, 0, st>>>(a.x, a.topk_ids, a.src2dst, (const int32_t*)a.workspace,
-                                                 a.a_fp8, a.a_sf, a.T, a.E, a.k, a.H,
+                                                 a.expert_ends, a.a_fp8, a.a_sf, a.T, a.E, a.k, a.A, a.H,
                                                  (int)align_up64(a.cap, 4), a.cap, err);
     ce = cudaGetLastError();
   }

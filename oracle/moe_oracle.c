@@ -220,15 +220,24 @@ static uint8_t unpack_scale(const int32_t* words, long ld, long row, int g) {
 /* ----------------------------------------------------------------- routing
  * Softmax top-k with renormalisation ([DG] §2.2.1 TopK; [SD] §1 topk_softmax):
  * softmax is monotone, so selection compares raw logits; ties go to the lower
- * expert index; slots are in selection order. Weights are
+ * expert index (+0 and -0 tie); NaN ranks last; slots are in selection order. Weights are
  * exp(l_j - l_max) / sum over the selected slots (slot order, fp32), which is
  * softmax followed by top-k and renormalisation. */
+/* a ranks strictly above b. The pages do not say how a NaN score ranks; here
+ * it ranks below every number (and NaNs tie), so a NaN router output can only
+ * fill slots that no number is left for. */
+static int ranks_above(float a, float b) {
+    if (a != a) return 0;
+    if (b != b) return 1;
+    return a > b;
+}
+
 static void select_topk(const float* score, int E, int k, unsigned char* taken, int32_t* ids) {
     memset(taken, 0, (size_t)E);
     for (int j = 0; j < k; j++) {
         int best = -1;
         for (int e = 0; e < E; e++)
-            if (!taken[e] && (best < 0 || score[e] > score[best])) best = e;
+            if (!taken[e] && (best < 0 || ranks_above(score[e], score[best]))) best = e;
         taken[best] = 1;
         ids[j] = best;
     }

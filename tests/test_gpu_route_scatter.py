@@ -96,6 +96,46 @@ def test_all_masked_and_empty_batch(ctx, orc):
     assert np.all(res[4] == 0xAB)
 
 
+def topk_edge_cases():
+    g = np.random.default_rng(31)
+    cases = []
+    l = synth.fp32_normal(g, (8, 896))
+    l[:, 5::32] += 10.0  # every winner in one lane: its sorted list runs dry and is rebuilt
+    cases.append(("one_lane", l, 16, None))
+    l = g.integers(-3, 4, size=(64, 700)).astype(np.float32)  # ties inside and across lanes
+    l[g.random(l.shape) < 0.05] = np.nan
+    l[g.random(l.shape) < 0.01] = np.inf
+    l[g.random(l.shape) < 0.01] = -np.inf
+    cases.append(("ties_nan_inf", l, 16, None))
+    l = g.integers(-2, 3, size=(64, 200)).astype(np.float32)
+    cases.append(("sigmoid_ties", l, 8, np.zeros(200, np.float32)))
+    l = np.array([[np.nan, 1.0, np.nan, -np.inf, 2.0, np.inf, -0.0, 0.0] * 4,
+                  [-0.0, 0.0] * 16, [np.nan] * 32], np.float32)
+    cases.append(("k_equals_E", l, 32, None))
+    cases.append(("E1024_k32", synth.fp32_normal(g, (40, 1024)), 32, None))
+    return cases
+
+
+@pytest.mark.parametrize("name,logits,k,bias", topk_edge_cases(), ids=[c[0] for c in topk_edge_cases()])
+def test_topk_selection_edge_cases(ctx, orc, name, logits, k, bias):
+    """Selection order bit-exact against the oracle with ties, NaN, +-inf,
+    signed zeros, all winners in one lane, k = E and E = 1024; weights
+    bit-exact on the rows whose selected logits are all finite."""
+    T, E = logits.shape
+    x = synth.bf16_normal(np.random.default_rng(1), (T, 128))
+    cap = synth.align_up(T * k + E * 127, 128)
+    if bias is None:
+        ids_ref, w_ref = orc.route_softmax_topk(logits, k)
+        mode = B.MOE_ROUTE_SOFTMAX_TOPK
+    else:
+        ids_ref, w_ref = orc.route_sigmoid_bias_topk(logits, bias, k)
+        mode = B.MOE_ROUTE_SIGMOID_BIAS_TOPK
+    res = gpu_route_scatter(ctx, x, E, k, 128, cap, mode, logits=logits, bias=bias)
+    check_against_oracle(orc, res, ids_ref, x, E, 128, cap)
+    finite = np.all(np.isfinite(np.take_along_axis(logits, ids_ref, axis=1)), axis=1)
+    assert np.array_equal(res[1][finite].view(np.uint32), w_ref[finite].view(np.uint32))
+
+
 def test_skewed_routing_one_hot_expert(ctx, orc):
     """Every token prefers expert 3: one long segment, the rest small."""
     g = np.random.default_rng(5)

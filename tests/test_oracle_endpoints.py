@@ -166,6 +166,41 @@ def test_topk_ties_prefer_lower_index(orc):
     assert np.allclose(w, 1 / 3, atol=1e-7)
 
 
+def brute_topk(scores, k):
+    """Top-k by enumeration: order experts by (score descending, index
+    ascending) with every NaN after every number; +0 and -0 are equal."""
+    out = []
+    for row in scores:
+        key = [(1, 0.0, e) if np.isnan(v) else (0, -float(v) + 0.0, e) for e, v in enumerate(row)]
+        out.append([e for _, _, e in sorted(key)[:k]])
+    return np.array(out, np.int32)
+
+
+def test_topk_nan_inf_and_signed_zero(orc):
+    nan, inf = np.nan, np.inf
+    logits = np.array([
+        [nan, 1.0, nan, -inf, 2.0, inf, -0.0, 0.0],
+        [nan, nan, nan, nan, -inf, nan, nan, nan],
+        [-0.0, 0.0, -0.0, 0.0, nan, -1.0, 1.0, -0.0],
+        [nan, nan, nan, nan, nan, nan, nan, nan],
+    ], np.float32)
+    for k in (1, 3, 5, 8):
+        ids, _ = orc.route_softmax_topk(logits, k)
+        assert np.array_equal(ids, brute_topk(logits, k)), k
+    ids, _ = orc.route_softmax_topk(logits, 8)
+    assert ids[0].tolist() == [5, 4, 1, 6, 7, 3, 0, 2]
+    assert ids[2].tolist()[:6] == [6, 0, 1, 2, 3, 7]
+
+
+def test_topk_random_ties_match_enumeration(orc):
+    g = np.random.default_rng(21)
+    logits = g.integers(-3, 4, size=(40, 100)).astype(np.float32)  # many ties
+    logits[g.random((40, 100)) < 0.05] = np.nan
+    for k in (1, 7, 16, 100):
+        ids, _ = orc.route_softmax_topk(logits, k)
+        assert np.array_equal(ids, brute_topk(logits, k))
+
+
 def test_sigmoid_bias_selects_biased_weights_unbiased(orc):
     g = np.random.default_rng(4)
     T, E, k = 200, 896, 16
