@@ -118,7 +118,10 @@ MOE_API int moe_expert_ends_from_counts(moe_ctx* ctx, const int32_t* counts, int
  * moe_ffn_forward). */
 typedef struct moe_act_params {
     int32_t kind;  /* MOE_ACT_* */
-    float limit;   /* L for SILU_CLAMP */
+    float limit;   /* L for SILU_CLAMP: > 0 (+inf allowed); other values are
+                      rejected with MOE_ERR_INVALID_ARG. Gate: min(g, L), up:
+                      clamp(u, -L, L), a NaN operand of min / max yielding the
+                      other one (IEEE minNum / maxNum). */
 } moe_act_params;
 
 /* ------------------------------------------------------ route + scatter

@@ -231,6 +231,7 @@ MOE_API int moe_grouped_gemm_act_quant(moe_ctx* ctx, const uint8_t* a, const int
                                        moe_stream_t stream) {
   if (!ctx || !act || A != 128 || !(w_format & MOE_GEMM_W_GATEUP_BLOCK128)) return MOE_ERR_INVALID_ARG;
   if (act->kind != MOE_ACT_SILU && act->kind != MOE_ACT_SILU_CLAMP) return MOE_ERR_INVALID_ARG;
+  if (act->kind == MOE_ACT_SILU_CLAMP && !(act->limit > 0.0f)) return MOE_ERR_INVALID_ARG;
   if (I < 128 || I % 128 != 0) return MOE_ERR_INVALID_ARG;
   moe::GemmArgs g{a, a_sf, ld_sf, expert_ends, E, cap, w13, w13_sf, w_format & MOE_GEMM_W_E4M3, 2 * I, K, nullptr};
   g.epi = (act->kind == MOE_ACT_SILU_CLAMP) ? 2 : 1;
@@ -254,6 +255,7 @@ MOE_API int moe_act_quant(moe_ctx* ctx, const uint16_t* gateup, uint8_t* out, in
   if (M_alloc > 0 && (!gateup || !out || !out_sf)) return MOE_ERR_INVALID_ARG;
   if (expert_ends && (E < 1 || E > 65535)) return MOE_ERR_INVALID_ARG;
   if (act->kind != MOE_ACT_SILU && act->kind != MOE_ACT_SILU_CLAMP) return MOE_ERR_INVALID_ARG;
+  if (act->kind == MOE_ACT_SILU_CLAMP && !(act->limit > 0.0f)) return MOE_ERR_INVALID_ARG;
   if (!al(gateup, 16) || !al(out, 16) || !al(out_sf, 4)) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
   return cuda_status(moe::launch_act_quant(gateup, out, out_sf, expert_ends, E, A, M_alloc, I, act->kind,
@@ -278,6 +280,7 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* a, moe_stream_t st
   if ((!fused && !a->gateup) || !a->act_fp8 || !a->act_sf || !a->down || !a->topk_w || !a->src2dst || !a->out)
     return MOE_ERR_INVALID_ARG;
   if (a->act.kind != MOE_ACT_SILU && a->act.kind != MOE_ACT_SILU_CLAMP) return MOE_ERR_INVALID_ARG;
+  if (a->act.kind == MOE_ACT_SILU_CLAMP && !(a->act.limit > 0.0f)) return MOE_ERR_INVALID_ARG;
   const int ld = (int)align4l(a->cap);
   const int fmt = a->w_format & MOE_GEMM_W_E4M3;
   moe::GemmArgs g1{a->a_fp8, a->a_sf, ld, a->expert_ends, a->E, a->cap, a->w13, a->w13_sf, fmt,

@@ -402,12 +402,28 @@ void orc_grouped_gemm(const uint8_t* a, const int32_t* a_sf, int ld_sf, int K,
  * L the gate is clamped from above and up on both sides ([DG] §2.4.1 default
  * branch: "up 双向钳、gate 只钳上限"); h = silu(gate) * up kept in fp32
  * (silu_mul_keep_fp32), then group-128 quantisation with packed UE8M0 scales. */
+/* min(a, b) and max(a, b) in which a NaN operand, quiet or signalling, yields
+ * the other operand (IEEE minNum / maxNum): the reading taken for the pages'
+ * min(gate, L) and clamp(up, -L, L). Written out because the C library's
+ * min/max treat a signalling NaN differently from one platform to the next. */
+static float min_num(float a, float b) {
+    if (a != a) return b;
+    if (b != b) return a;
+    return b < a ? b : a;
+}
+
+static float max_num(float a, float b) {
+    if (a != a) return b;
+    if (b != b) return a;
+    return b > a ? b : a;
+}
+
 static void act_quant_row(const uint16_t* row, int I, int clamp, float limit, float* h, uint8_t* q,
                           uint8_t* sf) {
     for (int j = 0; j < I; j++) {
         float g = orc_bf16_to_float(row[j]);
         float u = orc_bf16_to_float(row[I + j]);
-        if (clamp) { g = fminf(g, limit); u = fminf(fmaxf(u, -limit), limit); }
+        if (clamp) { g = min_num(g, limit); u = min_num(max_num(u, -limit), limit); }
         h[j] = orc_silu_spec(g) * u;
     }
     orc_group_quant_row(h, I, 128, q, sf);
@@ -570,7 +586,7 @@ void orc_ffn_dense(const uint16_t* x, int T, int H, int I, const int32_t* ids, c
  * beta=1, limit=7 and the interleaved layout, [KM] Phase 1 差异矩阵):
  *   g = min(g, L); u = clamp(u, -L, L); act = (g * sigmoid(alpha g)) * (u + beta). */
 float orc_glu_oai(float g, float u, float alpha, float beta, float limit) {
-    if (limit > 0.0f) { g = fminf(g, limit); u = fminf(fmaxf(u, -limit), limit); }
+    if (limit > 0.0f) { g = min_num(g, limit); u = min_num(max_num(u, -limit), limit); }
     float s = orc_sigmoid_spec(alpha * g);
     return (g * s) * (u + beta);
 }

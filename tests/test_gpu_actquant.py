@@ -107,6 +107,28 @@ def test_special_values(ctx, orc):
     assert np.array_equal(host(out), ref) and np.array_equal(host(out_sf), ref_sf)
 
 
+@pytest.mark.parametrize("kind,limit", [(B.MOE_ACT_SILU, 0.0), (B.MOE_ACT_SILU_CLAMP, 7.0)], ids=["silu", "clamp"])
+def test_every_gate_bit_pattern(ctx, orc, kind, limit):
+    """Each of the 65,536 bf16 gate patterns once (NaN, inf, subnormal, both
+    zeros, every exponent inside and outside the shared-memory window), up
+    drawn N(0,1): codes and scales bit-exact."""
+    I = 2048
+    rows = 65536 // I
+    g = np.random.default_rng(9)
+    gate = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    g.shuffle(gate)
+    up = synth.bf16_normal(g, (rows, I))
+    gateup = np.concatenate([gate.reshape(rows, I), up], axis=1)
+    out, out_sf, _ = run_gpu(ctx, gateup, [rows], I, kind=kind, limit=limit)
+    ref, ref_sf = orc.act_quant(gateup, np.array([rows], np.int32), 128, clamp=kind == B.MOE_ACT_SILU_CLAMP,
+                                limit=limit)
+    got = host(out)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, [(int(r), int(c), hex(gateup[r, c]), hex(gateup[r, I + c]), int(got[r, c]),
+                            int(ref[r, c])) for r, c in bad[:8]]
+    assert np.array_equal(host(out_sf), ref_sf)
+
+
 def test_graph_replay_with_reversed_counts(ctx, orc):
     """Capture endpoints + act-quant once; replay after reversing the counts
     (and refreshing the inputs in place): live outputs bit-exact, padding of
@@ -165,3 +187,6 @@ def test_invalid_arguments_rejected(ctx):
     t = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(B.MoeError):
         B.moe_act_quant(ctx, t, t, t, None, 1, 128, 4, 100)  # I not a multiple of 128
+    for bad_limit in (0.0, -1.0, float("nan")):  # the clamp needs L > 0
+        with pytest.raises(B.MoeError):
+            B.moe_act_quant(ctx, t, t, t, None, 1, 128, 4, 128, B.MOE_ACT_SILU_CLAMP, bad_limit)

@@ -135,3 +135,25 @@ def test_act_quant_clamp_semantics(orc):
     rc, rsf = ref_group_quant(h)
     assert unpack_scale_bytes(sf, 1, 1)[0, 0] == rsf[0]
     assert np.sum(out[0] != rc) <= 1
+
+
+def test_act_quant_clamp_nan_gate_and_up(orc):
+    """A NaN gate or up value, quiet or signalling, is the missing operand of
+    min / max: gate NaN -> L, up NaN -> -L (max(NaN, -L) = -L, then min with L).
+    The row with NaNs must equal the row with those values replaced."""
+    I = 128
+    L = 3.0
+    g = np.random.default_rng(2)
+    base = synth.f32_to_bf16_bits(g.standard_normal(2 * I).astype(np.float32))
+    row = base.copy()
+    nan_patterns = [0x7FC0, 0xFFC0, 0x7F81, 0xFF93, 0x7FB3, 0xFFBE]  # quiet and signalling
+    for j, p in enumerate(nan_patterns):
+        row[j] = p              # gate
+        row[I + 40 + j] = p     # up
+    repl = base.copy()
+    repl[:len(nan_patterns)] = synth.f32_to_bf16_bits(np.array([L], np.float32))[0]
+    repl[I + 40:I + 40 + len(nan_patterns)] = synth.f32_to_bf16_bits(np.array([-L], np.float32))[0]
+    a, asf = orc.act_quant(row[None, :], None, 128, clamp=True, limit=L)
+    b, bsf = orc.act_quant(repl[None, :], None, 128, clamp=True, limit=L)
+    assert np.array_equal(a, b) and np.array_equal(asf, bsf)
+
