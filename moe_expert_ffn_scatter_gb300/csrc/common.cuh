@@ -171,7 +171,6 @@ __device__ __forceinline__ float silu_of_bf16(const float* __restrict__ tbl, uin
   return __ldg(tbl + (gbits & 0xFFFFu));
 }
 
-
 // ------------------------------------------------------------------- e2m1
 // e2m1 nibble -> fp32: 1 sign, 2 exponent (bias 1), 1 mantissa bit.
 __device__ __forceinline__ float e2m1_to_f32(uint32_t nib) {
