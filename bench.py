@@ -41,13 +41,15 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--profile-kernel", choices=["route_scatter", "gemm1_act", "gemm2", "combine", "act_quant",
-                                                  "kimi_layer", "kimi_route_scatter"],
+                                                  "kimi_layer", "kimi_route_scatter", "decode_fp8",
+                                                  "decode_mxfp4"],
                    help="set up the layer, run one full step, then launch only this step's kernel "
                         "warmup + steps times and exit (for ncu captures); prints no JSON line. "
                         "act_quant launches the standalone live-row act-quant kernel at the "
                         "microbench shape (3,072 live of 28,672 rows, I = 2,048); kimi_layer runs "
                         "the Kimi-shaped layer warmup + steps times and prints its timings; "
-                        "kimi_route_scatter launches only its routing + scatter (no weights)")
+                        "kimi_route_scatter launches only its routing + scatter (no weights); "
+                        "decode_fp8 / decode_mxfp4 run the T=1 sparse decode over 2 layers")
     return p.parse_args()
 
 
@@ -233,6 +235,12 @@ def run_ours(args):
     torch.cuda.set_device(local)
     if args.profile_kernel == "act_quant":
         profile_act_quant(args, B, synth, torch, np, local)
+        return
+    if args.profile_kernel in ("decode_fp8", "decode_mxfp4"):
+        ctx = B.Context(local)
+        wfmt = B.MOE_WFMT_FP8_PER_EXPERT if args.profile_kernel == "decode_fp8" else B.MOE_WFMT_MXFP4_G32
+        decode_microbench(ctx, B, synth, torch, np, peaks()[0]["hbm_gbs"], n_layers=2,
+                          reps=args.warmup + args.steps, fmts=(wfmt,), tokens=(1,), use_graph=False)
         return
     if args.profile_kernel == "kimi_route_scatter":
         from moe_expert_ffn_scatter_gb300.layer import MoEFFNLayer
@@ -528,7 +536,7 @@ def actq_microbench(ctx, B, synth, torch, np, hbm, reps=50):
     return res
 
 
-def decode_microbench(ctx, B, synth, torch, np, hbm, n_layers=24, reps=5):
+def decode_microbench(ctx, B, synth, torch, np, hbm, n_layers=24, reps=5, fmts=None, tokens=(1, 8), use_graph=True):
     """gpt-oss-shaped sparse decode (E=32, top-4, H=I=2,880), FP8-per-expert and
     MXFP4 weights, T in {1, 8}: 24 layers with their own weight copies run in
     sequence, so L2 (126 MB) cannot serve the 0.4-0.8 GB of weights per layer.
@@ -537,13 +545,15 @@ def decode_microbench(ctx, B, synth, torch, np, hbm, n_layers=24, reps=5):
     E, k, H, I = synth.DECODE_E, synth.DECODE_K, synth.DECODE_H, synth.DECODE_I
     res = {}
     for fmt_name, wfmt, W in (("fp8", B.MOE_WFMT_FP8_PER_EXPERT, d.fp8), ("mxfp4", B.MOE_WFMT_MXFP4_G32, d.mxfp4)):
+        if fmts is not None and wfmt not in fmts:
+            continue
         layers = []
         base = {kk: torch.from_numpy(np.ascontiguousarray(v)).cuda() for kk, v in W.items()}
         for _ in range(n_layers):
             layers.append({kk: v.clone() for kk, v in base.items()})
         del base
         per_expert = sum(v[0].numel() * v.element_size() for kk, v in layers[0].items() if kk not in ("gu_scale", "d_scale"))
-        for T in (1, 8):
+        for T in tokens:
             x = torch.from_numpy(d.x[:T].view(np.int16)).view(torch.bfloat16).cuda()
             # routing is an input of this call: the 4 largest generator logits per token,
             # slot weights 1/4 each (the decode GEMVs' cost does not depend on them)
@@ -565,6 +575,11 @@ def decode_microbench(ctx, B, synth, torch, np, hbm, n_layers=24, reps=5):
             # in a CUDA graph (the layer calls only enqueue fixed grids) and replay
             run_layers()
             torch.cuda.synchronize()
+            if not use_graph:  # plain launches, for profilers
+                for _ in range(reps):
+                    run_layers()
+                torch.cuda.synchronize()
+                continue
             gs = torch.cuda.Stream()
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=gs):

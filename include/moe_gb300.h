@@ -346,7 +346,12 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* args, moe_stream_t
  *   MXFP4_G32:      w_gu [n_local][2I][H/2], w_gu_sf [n_local][2I][H/32],
  *                   w_d [n_local][H][I/2], w_d_sf [n_local][H][I/32]
  *   b_gu [n_local][2I] bf16, b_d [n_local][H] bf16.
- * Requires H % 32 == 0, I % 32 == 0, T <= 64, k <= 32. */
+ * Requires H % 32 == 0, I % 32 == 0, T <= 64, k <= 32; w_gu, w_d, the MXFP4
+ * scale arrays and the biases 16-byte aligned, x and act 8-byte aligned.
+ * T <= 8 with H % 64 == 0 and I % 64 == 0 runs on the tensor cores: each
+ * selected expert's weights are read once for all tokens (m16n8k16 f16 MMA
+ * on exactly converted weights against token columns scaled per token by a
+ * power of two). y1 / y2 of non-local slots are never written. */
 typedef struct moe_decode_args {
     const uint16_t* x;
     const int32_t* topk_ids;

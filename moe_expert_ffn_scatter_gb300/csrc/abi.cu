@@ -87,7 +87,8 @@ MOE_API int moe_ctx_create(moe_ctx** out, int device) {
     free(c);
     return MOE_ERR_CUDA;
   }
-  if (moe::init_grouped_gemm() != cudaSuccess || cudaMemset(c->d_err, 0, sizeof(uint32_t)) != cudaSuccess ||
+  if (moe::init_grouped_gemm() != cudaSuccess || moe::init_decode() != cudaSuccess ||
+      cudaMemset(c->d_err, 0, sizeof(uint32_t)) != cudaSuccess ||
       moe::launch_silu_table(c->d_silu, 0) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(c->d_silu);
     cudaFree(c->d_err);
@@ -326,11 +327,14 @@ MOE_API int moe_sparse_gemv_decode(moe_ctx* ctx, const moe_decode_args* a, moe_s
         !a->act || !a->y2 || !a->out)
       return MOE_ERR_INVALID_ARG;
     if (a->wfmt == MOE_WFMT_FP8_PER_EXPERT && (!a->w_gu_scale || !a->w_d_scale)) return MOE_ERR_INVALID_ARG;
-    if (a->wfmt == MOE_WFMT_MXFP4_G32 && (!a->w_gu_sf || !a->w_d_sf)) return MOE_ERR_INVALID_ARG;
-    if (!al(a->w_gu, 16) || !al(a->w_d, 16) || !al(a->x, 8) || !al(a->act, 8)) return MOE_ERR_INVALID_ARG;
+    if (a->wfmt == MOE_WFMT_MXFP4_G32 && (!a->w_gu_sf || !a->w_d_sf || !al(a->w_gu_sf, 16) || !al(a->w_d_sf, 16)))
+      return MOE_ERR_INVALID_ARG;
+    if (!al(a->w_gu, 16) || !al(a->w_d, 16) || !al(a->b_gu, 16) || !al(a->b_d, 16) || !al(a->x, 8) ||
+        !al(a->act, 8))
+      return MOE_ERR_INVALID_ARG;
   }
   DeviceGuard g(ctx->device);
-  return cuda_status(moe::launch_decode(*a, S(stream)));
+  return cuda_status(moe::launch_decode(*a, ctx->num_sms, ctx->d_err, S(stream)));
 }
 
 }  // extern "C"

@@ -65,6 +65,7 @@ cudaError_t init_grouped_gemm();
 int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, uint32_t* err,
                         cudaStream_t st);
 
-cudaError_t launch_decode(const moe_decode_args& a, cudaStream_t st);
+cudaError_t init_decode();
+cudaError_t launch_decode(const moe_decode_args& a, int num_sms, uint32_t* err, cudaStream_t st);
 
 }  // namespace moe

@@ -6,7 +6,7 @@ import torch
 
 from moe_expert_ffn_scatter_gb300 import binding as B
 from moe_expert_ffn_scatter_gb300 import synth
-from tests.gpu_util import check_ffn_tolerance, dev, dev_bf16, host_u16
+from tests.gpu_util import check_decode_tolerance, dev, dev_bf16, host_u16
 from tests.refs import bf16_bits_to_f64, bf16_ulp
 
 pytestmark = pytest.mark.gpu
@@ -56,7 +56,7 @@ def test_decode_gpt_oss_shape(ctx, orc, wfmt, T):
     # first GEMV: fp32 accumulation against one fp64 sum
     a, b = bf16_bits_to_f64(y1), bf16_bits_to_f64(ry1)
     assert np.mean(np.abs(a - b) <= bf16_ulp(b) * 1.0001) > 0.99
-    check_ffn_tolerance(out, rout)
+    check_decode_tolerance(out, rout)
 
 
 @pytest.mark.parametrize("wfmt", [B.MOE_WFMT_FP8_PER_EXPERT, B.MOE_WFMT_MXFP4_G32], ids=["fp8", "mxfp4"])
@@ -75,4 +75,4 @@ def test_decode_expert_parallel_slice_skips_nonlocal(ctx, orc, wfmt):
     assert np.all(np.isfinite(bf16_bits_to_f64(out)))
     _, _, _, rout = orc.decode(d.x, ids, w, loc, wfmt, I, expert_start=es, n_local=nl)
     local_any = ~nonlocal_.all(axis=1)
-    check_ffn_tolerance(out[local_any], rout[local_any])
+    check_decode_tolerance(out[local_any], rout[local_any])
