@@ -50,6 +50,9 @@ def _declare(L):
         "orc_exp_spec": (_F, [_F]),
         "orc_silu_spec": (_F, [_F]),
         "orc_sigmoid_spec": (_F, [_F]),
+        "orc_tanh_spec": (_F, [_F]),
+        "orc_situ_gate_spec": (_F, [_F, _F]),
+        "orc_situ_up_spec": (_F, [_F, _F]),
         "orc_glu_oai": (_F, [_F, _F, _F, _F, _F]),
         "orc_group_quant_row": (None, [_P, _I, _I, _P, _P]),
         "orc_route_softmax_topk": (None, [_P, _I, _I, _I, _P, _P]),
@@ -58,10 +61,10 @@ def _declare(L):
         "orc_endpoints": (None, [_P, _I, _I, _P, _P]),
         "orc_scatter": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
         "orc_grouped_gemm": (None, [_P, _P, _I, _I, _P, _I, _I, _P, _P, _I, _P]),
-        "orc_act_quant": (None, [_P, _I, _I, _P, _I, _I, _I, _F, _P, _P, _I]),
+        "orc_act_quant": (None, [_P, _I, _I, _P, _I, _I, _I, _F, _F, _F, _P, _P, _I]),
         "orc_combine": (None, [_P, _I, _P, _P, _I, _I, _F, _P]),
-        "orc_ffn_tokens": (None, [_P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _F, _F, _P, _I, _P]),
-        "orc_ffn_dense": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _F, _F, _P]),
+        "orc_ffn_tokens": (None, [_P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _F, _F, _F, _F, _P, _I, _P]),
+        "orc_ffn_dense": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _F, _F, _F, _F, _P]),
         "orc_decode": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
                               _I, _F, _F, _F, _P, _P, _P, _P]),
         "orc_decode_dense": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
@@ -98,6 +101,17 @@ def ue8m0_ceil(s): return lib().orc_ue8m0_ceil(float(s))
 def exp_spec(x): return lib().orc_exp_spec(float(x))
 def silu_spec(x): return lib().orc_silu_spec(float(x))
 def sigmoid_spec(x): return lib().orc_sigmoid_spec(float(x))
+def tanh_spec(x): return lib().orc_tanh_spec(float(x))
+def situ_gate_spec(g, beta_s=4.0): return lib().orc_situ_gate_spec(float(g), float(beta_s))
+def situ_up_spec(u, beta_l=25.0): return lib().orc_situ_up_spec(float(u), float(beta_l))
+
+
+def _act(clamp, limit, situ):
+    """(kind, limit, beta_s, beta_l): SiLU, SiLU with the clamp, or SiTU when
+    situ = (beta_s, beta_l) is given."""
+    if situ is not None:
+        return 2, 0.0, float(situ[0]), float(situ[1])
+    return (1 if clamp else 0), float(limit), 0.0, 0.0
 def glu_oai(g, u, alpha, beta, limit): return lib().orc_glu_oai(g, u, alpha, beta, limit)
 def num_threads(): return lib().orc_num_threads()
 
@@ -189,7 +203,7 @@ def grouped_gemm(a, a_sf, expert_ends, A, w, w_sf, out=None):
     return out
 
 
-def act_quant(gateup, expert_ends, A, clamp=False, limit=0.0, out=None, out_sf=None, fill=0xAB):
+def act_quant(gateup, expert_ends, A, clamp=False, limit=0.0, out=None, out_sf=None, fill=0xAB, situ=None):
     gateup = _c(gateup, np.uint16)
     M, I2 = gateup.shape
     I = I2 // 2
@@ -201,7 +215,7 @@ def act_quant(gateup, expert_ends, A, clamp=False, limit=0.0, out=None, out_sf=N
         out_sf = np.full((G4, ld), fill * 0x01010101, np.uint32).view(np.int32)
     ends = None if expert_ends is None else _c(expert_ends, np.int32)
     E = 0 if ends is None else ends.shape[0]
-    lib().orc_act_quant(_p(gateup), M, I, _p(ends), E, A, int(bool(clamp)), float(limit), _p(out), _p(out_sf), ld)
+    lib().orc_act_quant(_p(gateup), M, I, _p(ends), E, A, *_act(clamp, limit, situ), _p(out), _p(out_sf), ld)
     return out, out_sf
 
 
@@ -216,7 +230,7 @@ def combine(down, topk_w, src2dst, rsf=1.0):
     return out
 
 
-def ffn_tokens(x, ids, topk_w, w13, w13_sf, w2, w2_sf, tokens, clamp=False, limit=0.0, rsf=1.0):
+def ffn_tokens(x, ids, topk_w, w13, w13_sf, w2, w2_sf, tokens, clamp=False, limit=0.0, rsf=1.0, situ=None):
     x = _c(x, np.uint16)
     ids = _c(ids, np.int32)
     topk_w = _c(topk_w, np.float32)
@@ -227,11 +241,11 @@ def ffn_tokens(x, ids, topk_w, w13, w13_sf, w2, w2_sf, tokens, clamp=False, limi
     out = np.zeros((tokens.shape[0], H), np.uint16)
     lib().orc_ffn_tokens(_p(x), H, I2 // 2, _p(ids), _p(topk_w), k, E, _p(_c(w13, np.uint8)),
                          _p(_c(w13_sf, np.uint8)), _p(_c(w2, np.uint8)), _p(_c(w2_sf, np.uint8)),
-                         int(bool(clamp)), float(limit), float(rsf), _p(tokens), tokens.shape[0], _p(out))
+                         *_act(clamp, limit, situ), float(rsf), _p(tokens), tokens.shape[0], _p(out))
     return out
 
 
-def ffn_dense(x, ids, topk_w, w13, w13_sf, w2, w2_sf, clamp=False, limit=0.0, rsf=1.0):
+def ffn_dense(x, ids, topk_w, w13, w13_sf, w2, w2_sf, clamp=False, limit=0.0, rsf=1.0, situ=None):
     x = _c(x, np.uint16)
     ids = _c(ids, np.int32)
     topk_w = _c(topk_w, np.float32)
@@ -241,7 +255,7 @@ def ffn_dense(x, ids, topk_w, w13, w13_sf, w2, w2_sf, clamp=False, limit=0.0, rs
     out = np.zeros((T, H), np.uint16)
     lib().orc_ffn_dense(_p(x), T, H, I2 // 2, _p(ids), _p(topk_w), k, E, _p(_c(w13, np.uint8)),
                         _p(_c(w13_sf, np.uint8)), _p(_c(w2, np.uint8)), _p(_c(w2_sf, np.uint8)),
-                        int(bool(clamp)), float(limit), float(rsf), _p(out))
+                        *_act(clamp, limit, situ), float(rsf), _p(out))
     return out
 
 

@@ -178,6 +178,57 @@ float orc_sigmoid_spec(float x) {
     return 1.0f / d;
 }
 
+/* ------------------------------------------------------- tanh specification
+ * The pages use tanh in SiTU without defining it; both sides implement this
+ * one definition independently:
+ *   |y| < 2^-12          y  (tanh y = y (1 - y^2/3 + ...), the correction is
+ *                        below half an fp32 ulp)
+ *   |y| < 1/4            y + (y y^2) P(y^2), P the Taylor series of
+ *                        (tanh y - y) / y^3 to the y^8 term: coefficients
+ *                        fl(-1/3), fl(2/15), fl(-17/315), fl(62/2835),
+ *                        fl(-1382/155925), Horner with one fma per step,
+ *                        the last step fma(y y^2, P, y)
+ *   |y| >= 9             sign(y)
+ *   otherwise            sign(y) (1 - e) / (1 + e), e = exp_spec(-2|y|)
+ *   NaN                  NaN */
+static float g_tanh_c[5];
+
+__attribute__((constructor)) static void tanh_spec_init(void) {
+    g_tanh_c[0] = (float)(-1.0 / 3.0);
+    g_tanh_c[1] = (float)(2.0 / 15.0);
+    g_tanh_c[2] = (float)(-17.0 / 315.0);
+    g_tanh_c[3] = (float)(62.0 / 2835.0);
+    g_tanh_c[4] = (float)(-1382.0 / 155925.0);
+}
+
+float orc_tanh_spec(float y) {
+    if (isnan(y)) return y;
+    float a = fabsf(y);
+    if (a < 0x1p-12f) return y;
+    if (a < 0.25f) {
+        float z = y * y;
+        float p = g_tanh_c[4];
+        for (int i = 3; i >= 0; i--) p = fmaf(p, z, g_tanh_c[i]);
+        return fmaf(y * z, p, y);
+    }
+    if (a >= 9.0f) return copysignf(1.0f, y);
+    float e = orc_exp_spec(-2.0f * a);
+    float t = (1.0f - e) / (1.0f + e);
+    return copysignf(t, y);
+}
+
+/* SiTU ([KM] reference formula and the [DG] §2.4.1 situ branch; the LaTeX
+ * there prints tan, the code tanh -- tanh is taken):
+ *   gate' = (beta_s * tanh(g / beta_s)) * sigmoid(g)
+ *   up'   = beta_l * tanh(u / beta_l)
+ * each operation one IEEE fp32 operation, in this order. */
+float orc_situ_gate_spec(float g, float beta_s) {
+    float t = orc_tanh_spec(g / beta_s);
+    return (beta_s * t) * orc_sigmoid_spec(g);
+}
+
+float orc_situ_up_spec(float u, float beta_l) { return beta_l * orc_tanh_spec(u / beta_l); }
+
 /* ------------------------------------------------ group quantisation
  * Per 128-column group ([DG] §2.4.1, DeepGEMM convention, and §2.2.4
  * "per-token-group quant"): amax = max |v| (NaN ignored, like IEEE maxNum);
@@ -401,7 +452,9 @@ void orc_grouped_gemm(const uint8_t* a, const int32_t* a_sf, int ld_sf, int K,
  * up = gateup[r, I + j] ([DG] §2.4.1, [gate; up] halves); with a clamp limit
  * L the gate is clamped from above and up on both sides ([DG] §2.4.1 default
  * branch: "up 双向钳、gate 只钳上限"); h = silu(gate) * up kept in fp32
- * (silu_mul_keep_fp32), then group-128 quantisation with packed UE8M0 scales. */
+ * (silu_mul_keep_fp32), or with SiTU h = gate'(gate) * up'(up) (next row
+ * f2, the situ branch of [DG] §2.4.1); then group-128 quantisation with
+ * packed UE8M0 scales. */
 /* min(a, b) and max(a, b) in which a NaN operand, quiet or signalling, yields
  * the other operand (IEEE minNum / maxNum): the reading taken for the pages'
  * min(gate, L) and clamp(up, -L, L). Written out because the C library's
@@ -418,19 +471,23 @@ static float max_num(float a, float b) {
     return b > a ? b : a;
 }
 
-static void act_quant_row(const uint16_t* row, int I, int clamp, float limit, float* h, uint8_t* q,
-                          uint8_t* sf) {
-    for (int j = 0; j < I; j++) {
-        float g = orc_bf16_to_float(row[j]);
-        float u = orc_bf16_to_float(row[I + j]);
-        if (clamp) { g = min_num(g, limit); u = min_num(max_num(u, -limit), limit); }
-        h[j] = orc_silu_spec(g) * u;
-    }
+/* h for one (gate, up) pair: kind 0 SiLU, 1 SiLU with the clamp, 2 SiTU. */
+static float act_value(float g, float u, const orc_act* act) {
+    if (act->kind == 2) return orc_situ_gate_spec(g, act->beta_s) * orc_situ_up_spec(u, act->beta_l);
+    if (act->kind == 1) { g = min_num(g, act->limit); u = min_num(max_num(u, -act->limit), act->limit); }
+    return orc_silu_spec(g) * u;
+}
+
+static void act_quant_row(const uint16_t* row, int I, const orc_act* act, float* h, uint8_t* q, uint8_t* sf) {
+    for (int j = 0; j < I; j++)
+        h[j] = act_value(orc_bf16_to_float(row[j]), orc_bf16_to_float(row[I + j]), act);
     orc_group_quant_row(h, I, 128, q, sf);
 }
 
 void orc_act_quant(const uint16_t* gateup, int M_alloc, int I, const int32_t* expert_ends, int E,
-                   int A, int clamp, float limit, uint8_t* out, int32_t* out_sf, int ld_sf) {
+                   int A, int act_kind, float limit, float beta_s, float beta_l, uint8_t* out, int32_t* out_sf,
+                   int ld_sf) {
+    const orc_act act = {act_kind, limit, beta_s, beta_l};
     int G = (I + 127) / 128;
     int nseg = expert_ends ? E : 1;
     int32_t* start = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
@@ -444,7 +501,7 @@ void orc_act_quant(const uint16_t* gateup, int M_alloc, int I, const int32_t* ex
             uint8_t* sf = (uint8_t*)malloc((size_t)G + 1);
 #pragma omp for
             for (int r = r0; r < r1; r++) {
-                act_quant_row(gateup + (long)r * 2 * I, I, clamp, limit, h, out + (long)r * I, sf);
+                act_quant_row(gateup + (long)r * 2 * I, I, &act, h, out + (long)r * I, sf);
                 pack_scales(sf, G, out_sf, ld_sf, r);
             }
             free(h); free(sf);
@@ -480,11 +537,10 @@ void orc_combine(const uint16_t* down, int H, const float* topk_w, const int32_t
  * layout depends only on its own token). Used to check samples of large
  * configurations, and pinned against the layout path on small ones. */
 static void expert_chain(const double* a_deq, int H, int I, int e, const uint8_t* w13,
-                         const uint8_t* w13_sf, const uint8_t* w2, const uint8_t* w2_sf, int clamp,
-                         float limit, uint16_t* gu, float* h, uint8_t* q, uint8_t* sf, double* act_deq,
-                         uint16_t* down_row) {
+                         const uint8_t* w13_sf, const uint8_t* w2, const uint8_t* w2_sf, const orc_act* act,
+                         uint16_t* gu, float* h, uint8_t* q, uint8_t* sf, double* act_deq, uint16_t* down_row) {
     gemm_row(a_deq, H, e, w13, w13_sf, 2 * I, gu);
-    act_quant_row(gu, I, clamp, limit, h, q, sf);
+    act_quant_row(gu, I, act, h, q, sf);
     for (int i = 0; i < I; i++) act_deq[i] = orc_e4m3_value(q[i]) * orc_ue8m0_value(sf[i / 128]);
     gemm_row(act_deq, I, e, w2, w2_sf, H, down_row);
 }
@@ -497,8 +553,9 @@ static void token_input(const uint16_t* xrow, int H, float* v, uint8_t* q, uint8
 
 void orc_ffn_tokens(const uint16_t* x, int H, int I, const int32_t* ids, const float* topk_w, int k,
                     int E, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
-                    const uint8_t* w2_sf, int clamp, float limit, float rsf,
+                    const uint8_t* w2_sf, int act_kind, float limit, float beta_s, float beta_l, float rsf,
                     const int32_t* tokens, int n_tokens, uint16_t* out) {
+    const orc_act act = {act_kind, limit, beta_s, beta_l};
     int maxd = H > 2 * I ? H : 2 * I;
 #pragma omp parallel
     {
@@ -518,7 +575,7 @@ void orc_ffn_tokens(const uint16_t* x, int H, int I, const int32_t* ids, const f
                 int e = ids[(long)t * k + j];
                 valid[j] = (e >= 0 && e < E);
                 if (!valid[j]) continue;
-                expert_chain(a_deq, H, I, e, w13, w13_sf, w2, w2_sf, clamp, limit, gu, v, q, sf,
+                expert_chain(a_deq, H, I, e, w13, w13_sf, w2, w2_sf, &act, gu, v, q, sf,
                              act_deq, down + (long)j * H);
             }
             for (int hh = 0; hh < H; hh++) {
@@ -539,7 +596,9 @@ void orc_ffn_tokens(const uint16_t* x, int H, int I, const int32_t* ids, const f
  * equivalent bit for bit). */
 void orc_ffn_dense(const uint16_t* x, int T, int H, int I, const int32_t* ids, const float* topk_w,
                    int k, int E, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
-                   const uint8_t* w2_sf, int clamp, float limit, float rsf, uint16_t* out) {
+                   const uint8_t* w2_sf, int act_kind, float limit, float beta_s, float beta_l, float rsf,
+                   uint16_t* out) {
+    const orc_act act = {act_kind, limit, beta_s, beta_l};
     int maxd = H > 2 * I ? H : 2 * I;
     uint16_t* all_down = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)T * E * H);
 #pragma omp parallel
@@ -554,7 +613,7 @@ void orc_ffn_dense(const uint16_t* x, int T, int H, int I, const int32_t* ids, c
         for (int t = 0; t < T; t++) {
             token_input(x + (long)t * H, H, v, q, sf, a_deq);
             for (int e = 0; e < E; e++)
-                expert_chain(a_deq, H, I, e, w13, w13_sf, w2, w2_sf, clamp, limit, gu, v, q, sf,
+                expert_chain(a_deq, H, I, e, w13, w13_sf, w2, w2_sf, &act, gu, v, q, sf,
                              act_deq, all_down + ((long)t * E + e) * H);
         }
         free(v); free(q); free(sf); free(a_deq); free(act_deq); free(gu);

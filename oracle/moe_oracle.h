@@ -38,6 +38,16 @@ uint8_t  orc_ue8m0_ceil(float s);
 float orc_exp_spec(float x);
 float orc_silu_spec(float g);
 float orc_sigmoid_spec(float x);
+float orc_tanh_spec(float y);
+float orc_situ_gate_spec(float g, float beta_s);
+float orc_situ_up_spec(float u, float beta_l);
+
+/* activation between the GEMMs: kind 0 SiLU, 1 SiLU with clamp limit,
+ * 2 SiTU with beta_s (gate) and beta_l (up) */
+typedef struct orc_act {
+    int kind;
+    float limit, beta_s, beta_l;
+} orc_act;
 
 /* group-128 e4m3 quantisation of one fp32 row */
 void orc_group_quant_row(const float* v, int K, int group, uint8_t* codes, uint8_t* scales);
@@ -60,7 +70,8 @@ void orc_grouped_gemm(const uint8_t* a, const int32_t* a_sf, int ld_sf, int K,
 
 /* live-row SiLU*mul + e4m3/UE8M0 quantisation; expert_ends == NULL means every row */
 void orc_act_quant(const uint16_t* gateup, int M_alloc, int I, const int32_t* expert_ends, int E,
-                   int A, int clamp, float limit, uint8_t* out, int32_t* out_sf, int ld_sf);
+                   int A, int act_kind, float limit, float beta_s, float beta_l, uint8_t* out, int32_t* out_sf,
+                   int ld_sf);
 
 /* top-k weighted combine */
 void orc_combine(const uint16_t* down, int H, const float* topk_w, const int32_t* src2dst, int T,
@@ -69,13 +80,14 @@ void orc_combine(const uint16_t* down, int H, const float* topk_w, const int32_t
 /* whole layer, per token, computing only the selected experts (used for samples) */
 void orc_ffn_tokens(const uint16_t* x, int H, int I, const int32_t* ids, const float* topk_w, int k,
                     int E, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
-                    const uint8_t* w2_sf, int clamp, float limit, float rsf,
+                    const uint8_t* w2_sf, int act_kind, float limit, float beta_s, float beta_l, float rsf,
                     const int32_t* tokens, int n_tokens, uint16_t* out);
 
 /* dense twin: every expert on every token, then select by routing and sum */
 void orc_ffn_dense(const uint16_t* x, int T, int H, int I, const int32_t* ids, const float* topk_w,
                    int k, int E, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
-                   const uint8_t* w2_sf, int clamp, float limit, float rsf, uint16_t* out);
+                   const uint8_t* w2_sf, int act_kind, float limit, float beta_s, float beta_l, float rsf,
+                   uint16_t* out);
 
 /* decode GEMV path (bf16 activations, FP8-per-expert or MXFP4 weights) */
 float orc_glu_oai(float g, float u, float alpha, float beta, float limit);

@@ -56,3 +56,52 @@ def test_sigmoid_spec(orc):
         x = float(x)
         ref = 1.0 / (1.0 + math.exp(-x))
         assert abs(orc.sigmoid_spec(x) - ref) <= 3 * fp32_ulp(ref) + 2.0 ** -149
+
+
+# ------------------------------------------------------------------ tanh / SiTU
+def tanh_sweep():
+    rng = np.random.default_rng(7)
+    parts = [rng.uniform(2.0 ** -20, 2.0 ** -12, 500), rng.uniform(2.0 ** -12, 0.25, 4000),
+             np.linspace(0.2, 0.3, 2001), rng.uniform(0.25, 9.0, 4000), np.linspace(8.5, 12.0, 501)]
+    xs = np.concatenate(parts).astype(np.float32)
+    return np.concatenate([xs, -xs])
+
+
+def test_tanh_spec_error_within_4ulp(orc):
+    """Each branch of the definition (identity, Taylor polynomial, exp form,
+    saturation) against fp64 tanh; a wrong coefficient, sign or threshold in
+    any branch moves the error far past 4 ulp."""
+    for x in tanh_sweep():
+        y = orc.tanh_spec(float(x))
+        ref = math.tanh(float(x))
+        assert abs(y - ref) <= 4 * fp32_ulp(ref), (x, y, ref)
+
+
+def test_tanh_spec_odd_monotone_special(orc):
+    xs = np.sort(np.abs(tanh_sweep()))
+    ys = np.array([orc.tanh_spec(float(x)) for x in xs])
+    assert np.all(np.diff(ys) >= 0)
+    for x in xs[::7]:
+        assert orc.tanh_spec(-float(x)) == -orc.tanh_spec(float(x))
+    assert orc.tanh_spec(0.0) == 0.0 and math.copysign(1.0, orc.tanh_spec(-0.0)) == -1.0
+    assert orc.tanh_spec(math.inf) == 1.0 and orc.tanh_spec(-math.inf) == -1.0
+    assert math.isnan(orc.tanh_spec(math.nan))
+    assert orc.tanh_spec(1e-5) == np.float32(1e-5)  # below 2^-12 tanh y rounds to y
+
+
+def test_situ_specs_against_fp64(orc):
+    """gate' = 4 tanh(g/4) sigmoid(g), up' = 25 tanh(u/25): within 6 ulp of the
+    fp64 formula over all finite bf16 inputs of moderate size."""
+    vals = all_finite_bf16()
+    vals = vals[np.abs(vals) < 80]
+    for g in vals[::5]:
+        g = float(g)
+        ref = 4.0 * math.tanh(g / 4.0) / (1.0 + math.exp(-g))
+        got = orc.situ_gate_spec(g, 4.0)
+        assert abs(got - ref) <= 6 * fp32_ulp(ref) + 1e-40, (g, got, ref)
+        ref_u = 25.0 * math.tanh(g / 25.0)
+        got_u = orc.situ_up_spec(g, 25.0)
+        assert abs(got_u - ref_u) <= 6 * fp32_ulp(ref_u) + 1e-40, (g, got_u, ref_u)
+    assert orc.situ_gate_spec(math.inf, 4.0) == 4.0
+    assert orc.situ_gate_spec(-math.inf, 4.0) == 0.0
+    assert orc.situ_up_spec(math.inf, 25.0) == 25.0 and orc.situ_up_spec(-math.inf, 25.0) == -25.0

@@ -157,3 +157,23 @@ def test_act_quant_clamp_nan_gate_and_up(orc):
     b, bsf = orc.act_quant(repl[None, :], None, 128, clamp=True, limit=L)
     assert np.array_equal(a, b) and np.array_equal(asf, bsf)
 
+
+def test_act_quant_situ_against_fp64(orc):
+    """SiTU h = (4 tanh(g/4) sigmoid(g)) (25 tanh(u/25)) through the group
+    quantisation: scales equal to the fp64 recipe's, codes equal except where
+    the fp64 and fp32 products straddle an e4m3 rounding boundary."""
+    I = 256
+    rng = np.random.default_rng(12)
+    vals = (rng.standard_normal((64, 2 * I)) * 3).astype(np.float32)
+    row = synth.f32_to_bf16_bits(vals)
+    out, sf = orc.act_quant(row, None, 128, situ=(4.0, 25.0))
+    g = (row[:, :I].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    u = (row[:, I:].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    h = (4.0 * np.tanh(g / 4.0) / (1.0 + np.exp(-g))) * (25.0 * np.tanh(u / 25.0))
+    bad = 0
+    for r in range(h.shape[0]):
+        rc, rsf = ref_group_quant(h[r].astype(np.float32))
+        assert np.array_equal(unpack_scale_bytes(sf, r + 1, 2)[r], rsf[:2])
+        bad += int(np.sum(out[r] != rc))
+    assert bad <= 0.005 * out.size
+
