@@ -83,6 +83,7 @@ typedef void* moe_stream_t; /* cudaStream_t */
 /* activation kinds between the GEMMs */
 #define MOE_ACT_SILU 0                 /* h = silu(gate) * up */
 #define MOE_ACT_SILU_CLAMP 1           /* gate = min(gate, L); up = clamp(up, -L, L) first */
+#define MOE_ACT_SITU 2                 /* h = (bs tanh(g/bs) sigmoid(g)) * (bl tanh(u/bl)) */
 
 /* decode weight formats */
 #define MOE_WFMT_FP8_PER_EXPERT 0      /* e4m3 [E,N,K] + fp32 scale [E] */
@@ -122,6 +123,17 @@ typedef struct moe_act_params {
                       rejected with MOE_ERR_INVALID_ARG. Gate: min(g, L), up:
                       clamp(u, -L, L), a NaN operand of min / max yielding the
                       other one (IEEE minNum / maxNum). */
+    float situ_beta_s; /* SITU: beta_s of the gate half (Kimi: 4), > 0, finite */
+    float situ_beta_l; /* SITU: beta_l of the up half (Kimi: 25), > 0, finite.
+                          SiTU ([DG] §2.4.1 situ branch, [KM] reference
+                          formula; the pages print tan in the formula and tanh
+                          in the code, tanh is taken): gate' = (bs tanh(g/bs))
+                          sigmoid(g), up' = bl tanh(u/bl), h = gate' up', with
+                          the library's exp and tanh definitions. The context
+                          keeps the two 65,536-entry tables of one (bs, bl)
+                          pair and refills them on the call's stream when a
+                          call asks for another pair, so calls with different
+                          pairs must not overlap on different streams. */
 } moe_act_params;
 
 /* ------------------------------------------------------ route + scatter

@@ -19,6 +19,7 @@ MOE_ROUTE_SIGMOID_BIAS_TOPK = 1
 MOE_ROUTE_PRECOMPUTED = 2
 MOE_ACT_SILU = 0
 MOE_ACT_SILU_CLAMP = 1
+MOE_ACT_SITU = 2
 MOE_WFMT_FP8_PER_EXPERT = 0
 MOE_WFMT_MXFP4_G32 = 1
 MOE_GLU_HALVES = 0
@@ -51,7 +52,12 @@ class moe_route_args(ctypes.Structure):
 
 
 class moe_act_params(ctypes.Structure):
-    _fields_ = [("kind", _I32), ("limit", _F)]
+    _fields_ = [("kind", _I32), ("limit", _F), ("situ_beta_s", _F), ("situ_beta_l", _F)]
+
+
+def act_params(kind=0, limit=0.0, situ=(4.0, 25.0)):
+    """moe_act_params for SiLU / SiLU with clamp limit / SiTU (situ = (beta_s, beta_l))."""
+    return moe_act_params(kind, limit, float(situ[0]), float(situ[1]))
 
 
 class moe_ffn_args(ctypes.Structure):
@@ -207,8 +213,8 @@ def moe_grouped_gemm(ctx, a, a_sf, ld_sf, expert_ends, E, A, cap, w, w_sf, w_for
 
 
 def moe_grouped_gemm_act_quant(ctx, a, a_sf, ld_sf, expert_ends, E, A, cap, w13, w13_sf, w_format, I, K,
-                               out_fp8, out_sf, kind=MOE_ACT_SILU, limit=0.0, stream=None):
-    p = moe_act_params(kind, limit)
+                               out_fp8, out_sf, kind=MOE_ACT_SILU, limit=0.0, stream=None, situ=(4.0, 25.0)):
+    p = act_params(kind, limit, situ)
     _check("moe_grouped_gemm_act_quant",
            load().moe_grouped_gemm_act_quant(ctx.handle, ptr(a), ptr(a_sf), ld_sf, ptr(expert_ends), E, A, cap,
                                              ptr(w13), ptr(w13_sf), w_format, I, K, ctypes.byref(p), ptr(out_fp8),
@@ -216,8 +222,8 @@ def moe_grouped_gemm_act_quant(ctx, a, a_sf, ld_sf, expert_ends, E, A, cap, w13,
 
 
 def moe_act_quant(ctx, gateup, out, out_sf, expert_ends, E, A, M_alloc, I, kind=MOE_ACT_SILU, limit=0.0,
-                  stream=None):
-    p = moe_act_params(kind, limit)
+                  stream=None, situ=(4.0, 25.0)):
+    p = act_params(kind, limit, situ)
     _check("moe_act_quant",
            load().moe_act_quant(ctx.handle, ptr(gateup), ptr(out), ptr(out_sf), ptr(expert_ends), E, A, M_alloc,
                                 I, ctypes.byref(p), cur_stream(stream)))
@@ -231,10 +237,10 @@ def moe_combine(ctx, down, H, topk_w, src2dst, T, k, rsf, out, stream=None):
 
 def moe_ffn_forward(ctx, *, a_fp8, a_sf, expert_ends, w13, w13_sf, w2, w2_sf, gateup, act_fp8, act_sf, down,
                     topk_w, src2dst, out, T, E, k, H, I, A, cap, w_format=MOE_GEMM_W_E2M1, act_kind=MOE_ACT_SILU,
-                    limit=0.0, rsf=1.0, stream=None):
+                    limit=0.0, rsf=1.0, stream=None, situ=(4.0, 25.0)):
     a = moe_ffn_args(ptr(a_fp8), ptr(a_sf), ptr(expert_ends), ptr(w13), ptr(w13_sf), ptr(w2), ptr(w2_sf),
                      ptr(gateup), ptr(act_fp8), ptr(act_sf), ptr(down), ptr(topk_w), ptr(src2dst), ptr(out),
-                     T, E, k, H, I, A, cap, w_format, moe_act_params(act_kind, limit), rsf)
+                     T, E, k, H, I, A, cap, w_format, act_params(act_kind, limit, situ), rsf)
     _check("moe_ffn_forward", load().moe_ffn_forward(ctx.handle, ctypes.byref(a), cur_stream(stream)))
 
 

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <math.h>
 #include <stdlib.h>
 
 #include "moe_gb300.h"
@@ -13,6 +14,8 @@ struct moe_ctx {
   int num_sms;
   uint32_t* d_err;
   float* d_silu;  // 65,536-entry SiLU table of the exp/SiLU specification
+  float* d_situ;  // 2 x 65,536-entry SiTU tables (gate', up') for situ_bs / situ_bl
+  float situ_bs, situ_bl;
   moe::EncodeTiledFn encode;
 };
 
@@ -87,9 +90,20 @@ MOE_API int moe_ctx_create(moe_ctx** out, int device) {
     free(c);
     return MOE_ERR_CUDA;
   }
+  if (cudaMalloc(&c->d_situ, 2 * 65536 * sizeof(float)) != cudaSuccess) {
+    cudaFree(c->d_silu);
+    cudaFree(c->d_err);
+    free(c);
+    return MOE_ERR_CUDA;
+  }
+  c->situ_bs = 4.0f;  // Kimi's SiTU pair, filled now so that ordinary use never refills
+  c->situ_bl = 25.0f;
   if (moe::init_grouped_gemm() != cudaSuccess || moe::init_decode() != cudaSuccess ||
       cudaMemset(c->d_err, 0, sizeof(uint32_t)) != cudaSuccess ||
-      moe::launch_silu_table(c->d_silu, 0) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+      moe::launch_silu_table(c->d_silu, 0) != cudaSuccess ||
+      moe::launch_situ_table(c->d_situ, c->situ_bs, c->situ_bl, 0) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(c->d_situ);
     cudaFree(c->d_silu);
     cudaFree(c->d_err);
     free(c);
@@ -103,6 +117,7 @@ MOE_API int moe_ctx_destroy(moe_ctx* ctx) {
   if (!ctx) return MOE_OK;
   DeviceGuard g(ctx->device);
   cudaFree(ctx->d_silu);
+  cudaFree(ctx->d_situ);
   cudaFree(ctx->d_err);
   free(ctx);
   return MOE_OK;
@@ -225,18 +240,46 @@ MOE_API int moe_grouped_gemm(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf
   return moe::launch_grouped_gemm(g, ctx->encode, ctx->num_sms, ctx->d_err, S(stream));
 }
 
+// Activation parameters: SiLU, SiLU with a clamp limit L > 0, or SiTU with
+// finite positive betas.
+static int check_act(const moe_act_params* act) {
+  if (act->kind == MOE_ACT_SILU) return MOE_OK;
+  if (act->kind == MOE_ACT_SILU_CLAMP) return (act->limit > 0.0f) ? MOE_OK : MOE_ERR_INVALID_ARG;
+  if (act->kind == MOE_ACT_SITU)
+    return (act->situ_beta_s > 0.0f && act->situ_beta_s < INFINITY && act->situ_beta_l > 0.0f &&
+            act->situ_beta_l < INFINITY)
+               ? MOE_OK
+               : MOE_ERR_INVALID_ARG;
+  return MOE_ERR_INVALID_ARG;
+}
+
+// SiTU tables for the requested betas, refilled on the call's stream when
+// they differ from the ones the context holds.
+static int prepare_act(moe_ctx* ctx, const moe_act_params* act, cudaStream_t st) {
+  if (act->kind != MOE_ACT_SITU) return MOE_OK;
+  if (act->situ_beta_s == ctx->situ_bs && act->situ_beta_l == ctx->situ_bl) return MOE_OK;
+  if (moe::launch_situ_table(ctx->d_situ, act->situ_beta_s, act->situ_beta_l, st) != cudaSuccess) return MOE_ERR_CUDA;
+  ctx->situ_bs = act->situ_beta_s;
+  ctx->situ_bl = act->situ_beta_l;
+  return MOE_OK;
+}
+
+static int epi_of(const moe_act_params* act) {
+  return act->kind == MOE_ACT_SITU ? 3 : (act->kind == MOE_ACT_SILU_CLAMP ? 2 : 1);
+}
+
 MOE_API int moe_grouped_gemm_act_quant(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf, int ld_sf,
                                        const int32_t* expert_ends, int E, int A, int cap, const uint8_t* w13,
                                        const uint32_t* w13_sf, int w_format, int I, int K,
                                        const moe_act_params* act, uint8_t* out_fp8, int32_t* out_sf,
                                        moe_stream_t stream) {
   if (!ctx || !act || A != 128 || !(w_format & MOE_GEMM_W_GATEUP_BLOCK128)) return MOE_ERR_INVALID_ARG;
-  if (act->kind != MOE_ACT_SILU && act->kind != MOE_ACT_SILU_CLAMP) return MOE_ERR_INVALID_ARG;
-  if (act->kind == MOE_ACT_SILU_CLAMP && !(act->limit > 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (check_act(act) != MOE_OK) return MOE_ERR_INVALID_ARG;
   if (I < 128 || I % 128 != 0) return MOE_ERR_INVALID_ARG;
   moe::GemmArgs g{a, a_sf, ld_sf, expert_ends, E, cap, w13, w13_sf, w_format & MOE_GEMM_W_E4M3, 2 * I, K, nullptr};
-  g.epi = (act->kind == MOE_ACT_SILU_CLAMP) ? 2 : 1;
+  g.epi = epi_of(act);
   g.silu_tbl = ctx->d_silu;
+  g.situ_tbl = ctx->d_situ;
   g.out_q = out_fp8;
   g.out_sf = out_sf;
   g.ld_out_sf = (int)align4l(cap);
@@ -246,6 +289,7 @@ MOE_API int moe_grouped_gemm_act_quant(moe_ctx* ctx, const uint8_t* a, const int
   if (!al(out_sf, 4)) return MOE_ERR_INVALID_ARG;
   if (cap == 0) return MOE_OK;
   DeviceGuard dg(ctx->device);
+  if ((rc = prepare_act(ctx, act, S(stream))) != MOE_OK) return rc;
   return moe::launch_grouped_gemm(g, ctx->encode, ctx->num_sms, ctx->d_err, S(stream));
 }
 
@@ -255,12 +299,14 @@ MOE_API int moe_act_quant(moe_ctx* ctx, const uint16_t* gateup, uint8_t* out, in
   if (!ctx || !act || M_alloc < 0 || I < 128 || I % 128 != 0 || A < 1) return MOE_ERR_INVALID_ARG;
   if (M_alloc > 0 && (!gateup || !out || !out_sf)) return MOE_ERR_INVALID_ARG;
   if (expert_ends && (E < 1 || E > 65535)) return MOE_ERR_INVALID_ARG;
-  if (act->kind != MOE_ACT_SILU && act->kind != MOE_ACT_SILU_CLAMP) return MOE_ERR_INVALID_ARG;
-  if (act->kind == MOE_ACT_SILU_CLAMP && !(act->limit > 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (check_act(act) != MOE_OK) return MOE_ERR_INVALID_ARG;
   if (!al(gateup, 16) || !al(out, 16) || !al(out_sf, 4)) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
+  const int rc = prepare_act(ctx, act, S(stream));
+  if (rc != MOE_OK) return rc;
   return cuda_status(moe::launch_act_quant(gateup, out, out_sf, expert_ends, E, A, M_alloc, I, act->kind,
-                                           act->limit, ctx->d_silu, ctx->num_sms, ctx->d_err, S(stream)));
+                                           act->limit, ctx->d_silu, ctx->d_situ, ctx->num_sms, ctx->d_err,
+                                           S(stream)));
 }
 
 MOE_API int moe_combine(moe_ctx* ctx, const uint16_t* down, int H, const float* topk_w,
@@ -280,15 +326,15 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* a, moe_stream_t st
   const bool fused = (a->w_format & MOE_GEMM_W_GATEUP_BLOCK128) != 0;
   if ((!fused && !a->gateup) || !a->act_fp8 || !a->act_sf || !a->down || !a->topk_w || !a->src2dst || !a->out)
     return MOE_ERR_INVALID_ARG;
-  if (a->act.kind != MOE_ACT_SILU && a->act.kind != MOE_ACT_SILU_CLAMP) return MOE_ERR_INVALID_ARG;
-  if (a->act.kind == MOE_ACT_SILU_CLAMP && !(a->act.limit > 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (check_act(&a->act) != MOE_OK) return MOE_ERR_INVALID_ARG;
   const int ld = (int)align4l(a->cap);
   const int fmt = a->w_format & MOE_GEMM_W_E4M3;
   moe::GemmArgs g1{a->a_fp8, a->a_sf, ld, a->expert_ends, a->E, a->cap, a->w13, a->w13_sf, fmt,
                    2 * a->I, a->H, a->gateup};
   if (fused) {
     g1.silu_tbl = ctx->d_silu;
-    g1.epi = (a->act.kind == MOE_ACT_SILU_CLAMP) ? 2 : 1;
+    g1.situ_tbl = ctx->d_situ;
+    g1.epi = epi_of(&a->act);
     g1.out_q = a->act_fp8;
     g1.out_sf = a->act_sf;
     g1.ld_out_sf = ld;
@@ -302,12 +348,13 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* a, moe_stream_t st
       !al(a->out, 16))
     return MOE_ERR_INVALID_ARG;
   DeviceGuard dg(ctx->device);
+  if ((rc = prepare_act(ctx, &a->act, S(stream))) != MOE_OK) return rc;
   if (a->cap > 0) {
     if ((rc = moe::launch_grouped_gemm(g1, ctx->encode, ctx->num_sms, ctx->d_err, S(stream))) != MOE_OK) return rc;
     if (!fused &&
         (rc = cuda_status(moe::launch_act_quant(a->gateup, a->act_fp8, a->act_sf, a->expert_ends, a->E, a->A,
                                                 a->cap, a->I, a->act.kind, a->act.limit, ctx->d_silu,
-                                                ctx->num_sms, ctx->d_err, S(stream)))) != MOE_OK)
+                                                ctx->d_situ, ctx->num_sms, ctx->d_err, S(stream)))) != MOE_OK)
       return rc;
     if ((rc = moe::launch_grouped_gemm(g2, ctx->encode, ctx->num_sms, ctx->d_err, S(stream))) != MOE_OK) return rc;
   }

@@ -11,7 +11,8 @@
 // 4w..4w+3. One warp per item, 16 columns per lane (two uint4 loads from the
 // gate half, two from the up half); a group of 128 columns is 8 lanes, its
 // amax a 3-step xor reduction; lane 0 assembles the four scale bytes into the
-// int32 word of the MN-major scale array.
+// int32 word of the MN-major scale array. SiTU (next row f2) reads gate' and
+// up' from two per-context tables over all bf16 patterns.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -22,14 +23,18 @@ namespace {
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kThreads = 256;
 
-template <bool kLive, bool kClamp>
+// kAct: 0 SiLU, 1 SiLU with the clamp, 2 SiTU (situ_tbl: gate' then up'
+// tables over all bf16 patterns, for the context's beta_s / beta_l).
+template <bool kLive, int kAct>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __restrict__ gateup,
                                                              uint8_t* __restrict__ out,
                                                              int32_t* __restrict__ out_sf,
                                                              const int32_t* __restrict__ ends, int E,
                                                              int A, int M_alloc, int I, int ld_sf,
                                                              float limit, const float* __restrict__ silu_tbl,
+                                                             const float* __restrict__ situ_tbl,
                                                              uint32_t* err) {
+  constexpr bool kClamp = kAct == 1;
   const float silu_limit = kClamp ? spec_silu(limit) : 0.0f;
   int r0 = 0, r1 = M_alloc;
   if (kLive) {
@@ -69,12 +74,20 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
       for (int i = 0; i < 8; ++i) {
         const float ga = bf16_lo(gw[i]), gb = bf16_hi(gw[i]);
         float ua = bf16_lo(uw[i]), ub = bf16_hi(uw[i]);
-        if (kClamp) {
-          ua = fminf(fmaxf(ua, -limit), limit);
-          ub = fminf(fmaxf(ub, -limit), limit);
+        float sa, sb;
+        if (kAct == 2) {
+          sa = __ldg(situ_tbl + (gw[i] & 0xFFFFu));
+          sb = __ldg(situ_tbl + (gw[i] >> 16));
+          ua = __ldg(situ_tbl + 65536 + (uw[i] & 0xFFFFu));
+          ub = __ldg(situ_tbl + 65536 + (uw[i] >> 16));
+        } else {
+          if (kClamp) {
+            ua = fminf(fmaxf(ua, -limit), limit);
+            ub = fminf(fmaxf(ub, -limit), limit);
+          }
+          sa = silu_of_bf16<kClamp>(silu_tbl, gw[i], ga, limit, silu_limit);
+          sb = silu_of_bf16<kClamp>(silu_tbl, gw[i] >> 16, gb, limit, silu_limit);
         }
-        const float sa = silu_of_bf16<kClamp>(silu_tbl, gw[i], ga, limit, silu_limit);
-        const float sb = silu_of_bf16<kClamp>(silu_tbl, gw[i] >> 16, gb, limit, silu_limit);
         const float2 hh = mul2(make_float2(sa, sb), make_float2(ua, ub));
         h[2 * i] = hh.x;
         h[2 * i + 1] = hh.y;
@@ -103,14 +116,17 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
 template <bool kLive>
 cudaError_t launch_kind(const uint16_t* gateup, uint8_t* out, int32_t* out_sf, const int32_t* ends,
                         int E, int A, int M_alloc, int I, int kind, float limit, const float* silu_tbl,
-                        dim3 grid, uint32_t* err, cudaStream_t st) {
+                        const float* situ_tbl, dim3 grid, uint32_t* err, cudaStream_t st) {
   const int ld = (int)align_up64(M_alloc, 4);
   if (kind == MOE_ACT_SILU_CLAMP)
-    act_quant_kernel<kLive, true><<<grid, kThreads, 0, st>>>(gateup, out, out_sf, ends, E, A, M_alloc, I,
-                                                           ld, limit, silu_tbl, err);
+    act_quant_kernel<kLive, 1><<<grid, kThreads, 0, st>>>(gateup, out, out_sf, ends, E, A, M_alloc, I, ld, limit,
+                                                        silu_tbl, situ_tbl, err);
+  else if (kind == MOE_ACT_SITU)
+    act_quant_kernel<kLive, 2><<<grid, kThreads, 0, st>>>(gateup, out, out_sf, ends, E, A, M_alloc, I, ld, limit,
+                                                        silu_tbl, situ_tbl, err);
   else
-    act_quant_kernel<kLive, false><<<grid, kThreads, 0, st>>>(gateup, out, out_sf, ends, E, A, M_alloc,
-                                                            I, ld, limit, silu_tbl, err);
+    act_quant_kernel<kLive, 0><<<grid, kThreads, 0, st>>>(gateup, out, out_sf, ends, E, A, M_alloc, I, ld, limit,
+                                                        silu_tbl, situ_tbl, err);
   return cudaGetLastError();
 }
 
@@ -118,6 +134,16 @@ cudaError_t launch_kind(const uint16_t* gateup, uint8_t* out, int32_t* out_sf, c
 __global__ void silu_table_kernel(float* __restrict__ tbl) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < 65536) tbl[i] = spec_silu(bf16_to_f32((uint16_t)i));
+}
+
+// Entries i and 65536 + i: SiTU gate' and up' of the bf16 value with bits i.
+__global__ void situ_table_kernel(float* __restrict__ tbl, float beta_s, float beta_l) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < 65536) {
+    const float v = bf16_to_f32((uint16_t)i);
+    tbl[i] = spec_situ_gate(v, beta_s);
+    tbl[65536 + i] = spec_situ_up(v, beta_l);
+  }
 }
 
 }  // namespace
@@ -131,19 +157,25 @@ cudaError_t launch_silu_table(float* tbl, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_situ_table(float* tbl, float beta_s, float beta_l, cudaStream_t st) {
+  situ_table_kernel<<<256, 256, 0, st>>>(tbl, beta_s, beta_l);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_act_quant(const uint16_t* gateup, uint8_t* out, int32_t* out_sf,
                              const int32_t* expert_ends, int E, int A, int M_alloc, int I, int kind,
-                             float limit, const float* silu_tbl, int num_sms, uint32_t* err, cudaStream_t st) {
+                             float limit, const float* silu_tbl, const float* situ_tbl, int num_sms, uint32_t* err,
+                             cudaStream_t st) {
   if (M_alloc == 0) return cudaSuccess;
   if (expert_ends) {
     if (E == 0) return cudaSuccess;
     const int gy = (int)lmin(lmax(2, (4L * num_sms + E - 1) / E), 65535);
-    return launch_kind<true>(gateup, out, out_sf, expert_ends, E, A, M_alloc, I, kind, limit, silu_tbl,
+    return launch_kind<true>(gateup, out, out_sf, expert_ends, E, A, M_alloc, I, kind, limit, silu_tbl, situ_tbl,
                              dim3(1, gy, E), err, st);
   }
   const long items = (long)M_alloc * (((I / 128) + 3) / 4);
   const int gy = (int)lmin((items + 7) / 8, 8L * num_sms);
-  return launch_kind<false>(gateup, out, out_sf, nullptr, 0, A, M_alloc, I, kind, limit, silu_tbl,
+  return launch_kind<false>(gateup, out, out_sf, nullptr, 0, A, M_alloc, I, kind, limit, silu_tbl, situ_tbl,
                             dim3(1, gy, 1), err, st);
 }
 

@@ -134,6 +134,48 @@ __device__ __forceinline__ float spec_sigmoid(float x) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, spec_exp(-x)));
 }
 
+// tanh specification (the pages use tanh in SiTU without defining it; the
+// oracle implements the same definition independently):
+//   |y| < 2^-12  -> y
+//   |y| < 1/4    -> fma(y*y^2, P(y^2), y), P the Taylor series of
+//                   (tanh y - y)/y^3 through the y^8 term, coefficients the
+//                   fp32 roundings of -1/3, 2/15, -17/315, 62/2835,
+//                   -1382/155925, Horner with one fma per step
+//   |y| >= 9     -> sign(y)
+//   otherwise    -> sign(y) (1 - e) / (1 + e), e = spec_exp(-2|y|)
+constexpr float kTanhP0 = (float)(-1.0 / 3.0);
+constexpr float kTanhP1 = (float)(2.0 / 15.0);
+constexpr float kTanhP2 = (float)(-17.0 / 315.0);
+constexpr float kTanhP3 = (float)(62.0 / 2835.0);
+constexpr float kTanhP4 = (float)(-1382.0 / 155925.0);
+
+__device__ __forceinline__ float spec_tanh(float y) {
+  if (isnan(y)) return y;
+  const float a = fabsf(y);
+  if (a < 0x1p-12f) return y;
+  if (a < 0.25f) {
+    const float z = __fmul_rn(y, y);
+    float p = kTanhP4;
+    p = __fmaf_rn(p, z, kTanhP3);
+    p = __fmaf_rn(p, z, kTanhP2);
+    p = __fmaf_rn(p, z, kTanhP1);
+    p = __fmaf_rn(p, z, kTanhP0);
+    return __fmaf_rn(__fmul_rn(y, z), p, y);
+  }
+  if (a >= 9.0f) return copysignf(1.0f, y);
+  const float e = spec_exp(__fmul_rn(-2.0f, a));
+  return copysignf(__fdiv_rn(__fsub_rn(1.0f, e), __fadd_rn(1.0f, e)), y);
+}
+
+// SiTU halves: gate' = (beta_s * tanh(g / beta_s)) * sigmoid(g) and
+// up' = beta_l * tanh(u / beta_l), one IEEE operation each, in this order.
+__device__ __forceinline__ float spec_situ_gate(float g, float beta_s) {
+  return __fmul_rn(__fmul_rn(beta_s, spec_tanh(__fdiv_rn(g, beta_s))), spec_sigmoid(g));
+}
+__device__ __forceinline__ float spec_situ_up(float u, float beta_l) {
+  return __fmul_rn(beta_l, spec_tanh(__fdiv_rn(u, beta_l)));
+}
+
 // ------------------------------------------------ packed pairs (f32x2)
 // Blackwell executes fp32 add / mul / fma on register pairs; each half is the
 // ordinary IEEE round-to-nearest operation, so results are bitwise those of

@@ -209,15 +209,17 @@ __device__ __forceinline__ int expert_of_tile(const int32_t* ends, int E, int m0
 
 // Epilogue kinds: bf16 output, or (GEMM1 with gate/up rows interleaved in
 // blocks of 128) SiLU*mul + e4m3/UE8M0 quantisation of the bf16-rounded
-// accumulators, optionally with the gate/up clamp.
-constexpr int kEpiBf16 = 0, kEpiSilu = 1, kEpiSiluClamp = 2;
+// accumulators, optionally with the gate/up clamp, or SiTU (gate' and up'
+// from the per-context tables) + the same quantisation.
+constexpr int kEpiBf16 = 0, kEpiSilu = 1, kEpiSiluClamp = 2, kEpiSitu = 3;
 
 template <bool kBfp4, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
     const int32_t* __restrict__ a_sf, int ld_sf, const int32_t* __restrict__ ends, int E, int cap,
     const uint32_t* __restrict__ w_sf, int N, int K, uint16_t* __restrict__ out, uint8_t* __restrict__ out_q,
-    int32_t* __restrict__ out_sf, int ld_out_sf, float limit, const float* __restrict__ silu_tbl, uint32_t* err) {
+    int32_t* __restrict__ out_sf, int ld_out_sf, float limit, const float* __restrict__ silu_tbl,
+    const float* __restrict__ situ_tbl, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -412,12 +414,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
         for (int i = 0; i < 64; ++i) {
           const float ga = bf16_lo(packed[i]), gb = bf16_hi(packed[i]);
           float ua = bf16_lo(packed[64 + i]), ub = bf16_hi(packed[64 + i]);
-          if (kEpi == kEpiSiluClamp) {
-            ua = fminf(fmaxf(ua, -limit), limit);
-            ub = fminf(fmaxf(ub, -limit), limit);
+          float sa, sb;
+          if (kEpi == kEpiSitu) {
+            sa = __ldg(situ_tbl + (packed[i] & 0xFFFFu));
+            sb = __ldg(situ_tbl + (packed[i] >> 16));
+            ua = __ldg(situ_tbl + 65536 + (packed[64 + i] & 0xFFFFu));
+            ub = __ldg(situ_tbl + 65536 + (packed[64 + i] >> 16));
+          } else {
+            if (kEpi == kEpiSiluClamp) {
+              ua = fminf(fmaxf(ua, -limit), limit);
+              ub = fminf(fmaxf(ub, -limit), limit);
+            }
+            sa = silu_of_bf16<kEpi == kEpiSiluClamp>(silu_tbl, packed[i], ga, limit, silu_limit);
+            sb = silu_of_bf16<kEpi == kEpiSiluClamp>(silu_tbl, packed[i] >> 16, gb, limit, silu_limit);
           }
-          const float sa = silu_of_bf16<kEpi == kEpiSiluClamp>(silu_tbl, packed[i], ga, limit, silu_limit);
-          const float sb = silu_of_bf16<kEpi == kEpiSiluClamp>(silu_tbl, packed[i] >> 16, gb, limit, silu_limit);
           const float2 hh = mul2(make_float2(sa, sb), make_float2(ua, ub));
           packed[i] = __float_as_uint(hh.x);       // h[2i]
           packed[64 + i] = __float_as_uint(hh.y);  // h[2i + 1]
@@ -489,7 +499,7 @@ int launch_impl(const GemmArgs& g, EncodeTiledFn encode, int num_sms, uint32_t* 
   if (grid <= 0) return MOE_OK;
   grouped_gemm_kernel<kBfp4, kEpi><<<grid, kThreads, SMEM_BYTES, st>>>(
       tmA, tmB, g.a_sf, g.ld_sf, g.expert_ends, g.E, g.cap, g.w_sf, g.N, g.K, g.out, g.out_q, g.out_sf,
-      g.ld_out_sf, g.limit, g.silu_tbl, err);
+      g.ld_out_sf, g.limit, g.silu_tbl, g.situ_tbl, err);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -505,7 +515,8 @@ cudaError_t init_grouped_gemm() {
   const void* fns[] = {
       (const void*)grouped_gemm_kernel<true, kEpiBf16>,  (const void*)grouped_gemm_kernel<false, kEpiBf16>,
       (const void*)grouped_gemm_kernel<true, kEpiSilu>,  (const void*)grouped_gemm_kernel<false, kEpiSilu>,
-      (const void*)grouped_gemm_kernel<true, kEpiSiluClamp>, (const void*)grouped_gemm_kernel<false, kEpiSiluClamp>};
+      (const void*)grouped_gemm_kernel<true, kEpiSiluClamp>, (const void*)grouped_gemm_kernel<false, kEpiSiluClamp>,
+      (const void*)grouped_gemm_kernel<true, kEpiSitu>,  (const void*)grouped_gemm_kernel<false, kEpiSitu>};
   for (const void* f : fns) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -516,6 +527,7 @@ cudaError_t init_grouped_gemm() {
 int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, uint32_t* err, cudaStream_t st) {
   if (g.epi == 1) return launch_fmt<kEpiSilu>(g, encode, num_sms, err, st);
   if (g.epi == 2) return launch_fmt<kEpiSiluClamp>(g, encode, num_sms, err, st);
+  if (g.epi == 3) return launch_fmt<kEpiSitu>(g, encode, num_sms, err, st);
   return launch_fmt<kEpiBf16>(g, encode, num_sms, err, st);
 }
 

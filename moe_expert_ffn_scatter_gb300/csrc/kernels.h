@@ -24,9 +24,12 @@ cudaError_t launch_expert_ends(const int32_t* counts, int E, int A, int32_t* end
 cudaError_t launch_route_scatter(const moe_route_args& a, int num_sms, uint32_t* err, cudaStream_t st);
 // 65,536-entry table of spec_silu over all bf16 bit patterns (per context).
 cudaError_t launch_silu_table(float* tbl, cudaStream_t st);
+// 2 x 65,536 entries: SiTU gate' then up' over all bf16 bit patterns.
+cudaError_t launch_situ_table(float* tbl, float beta_s, float beta_l, cudaStream_t st);
 cudaError_t launch_act_quant(const uint16_t* gateup, uint8_t* out, int32_t* out_sf,
                              const int32_t* expert_ends, int E, int A, int M_alloc, int I, int kind,
-                             float limit, const float* silu_tbl, int num_sms, uint32_t* err, cudaStream_t st);
+                             float limit, const float* silu_tbl, const float* situ_tbl, int num_sms, uint32_t* err,
+                             cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* down, int H, const float* topk_w, const int32_t* src2dst,
                            int T, int k, float rsf, uint16_t* out, int num_sms, cudaStream_t st);
 cudaError_t launch_prepare_weights(const uint8_t* w_in, const uint8_t* sf_in, int E, int N, int K,
@@ -58,6 +61,7 @@ struct GemmArgs {
   int ld_out_sf = 0;
   float limit = 0.0f;
   const float* silu_tbl = nullptr;
+  const float* situ_tbl = nullptr;
 };
 // Per-device set-up (shared-memory opt-in); called once per context.
 cudaError_t init_grouped_gemm();

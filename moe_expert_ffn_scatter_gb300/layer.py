@@ -22,7 +22,7 @@ def ceil_div(a, b):
 class MoEFFNLayer:
     def __init__(self, ctx, *, T, E, k, H, I, A=128, cap=None, routing=B.MOE_ROUTE_SOFTMAX_TOPK,
                  act_kind=B.MOE_ACT_SILU, limit=0.0, rsf=1.0, w_format=B.MOE_GEMM_W_E2M1, fused=True,
-                 device="cuda"):
+                 situ=(4.0, 25.0), device="cuda"):
         """fused: run SiLU*mul and the quantisation in GEMM1's epilogue (w13 is
         prepared with gate/up rows interleaved in blocks of 128); otherwise
         GEMM1 writes the bf16 gate/up buffer and the act-quant kernel follows."""
@@ -32,7 +32,7 @@ class MoEFFNLayer:
             cap = ceil_div(T * k + E * (A - 1), A) * A
         self.cap = cap
         self.routing = routing
-        self.act_kind, self.limit, self.rsf = act_kind, limit, rsf
+        self.act_kind, self.limit, self.rsf, self.situ = act_kind, limit, rsf, situ
         self.w_format = w_format
         self.fused = fused
         self.w13_format = w_format | (B.MOE_GEMM_W_GATEUP_BLOCK128 if fused else 0)
@@ -111,7 +111,7 @@ class MoEFFNLayer:
                           act_fp8=self.act_fp8, act_sf=self.act_sf, down=self.down, topk_w=self.topk_w,
                           src2dst=self.src2dst, out=self.out, T=self.T, E=self.E, k=self.k, H=self.H, I=self.I,
                           A=self.A, cap=self.cap, w_format=self.w13_format, act_kind=self.act_kind,
-                          limit=self.limit, rsf=self.rsf, stream=stream)
+                          limit=self.limit, rsf=self.rsf, stream=stream, situ=self.situ)
 
     def forward(self, x, logits=None, bias=None, stream=None):
         """x [T,H] bf16, logits [T,E] fp32 (device) -> self.out [T,H] bf16."""

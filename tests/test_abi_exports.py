@@ -5,6 +5,7 @@ import ctypes
 import glob
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -65,9 +66,25 @@ def test_host_validation_without_device(lib):
     assert lib.moe_route_scatter_workspace_size(-1, 32, 6) == 0
 
 
-def test_struct_layouts_match_header():
-    """ctypes mirrors of the argument structs have the C sizes (LP64)."""
-    assert ctypes.sizeof(B.moe_route_args) == 120
-    assert ctypes.sizeof(B.moe_act_params) == 8
-    assert ctypes.sizeof(B.moe_ffn_args) == 14 * 8 + 8 * 4 + 8 + 4 + 4
-    assert B.moe_decode_args.T.offset > B.moe_decode_args.out.offset
+def test_struct_layouts_match_header(tmp_path):
+    """The ctypes mirrors of the argument structs have the sizes and field
+    offsets that a C compiler gives the header's structs."""
+    structs = {"moe_route_args": B.moe_route_args, "moe_act_params": B.moe_act_params,
+               "moe_ffn_args": B.moe_ffn_args, "moe_decode_args": B.moe_decode_args}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moe_gb300.h"', 'int main(void) {']
+    for name, cls in structs.items():
+        lines.append('printf("%s %%zu\\n", sizeof(%s));' % (name, name))
+        for fname, _ in cls._fields_:
+            lines.append('printf("%s.%s %%zu\\n", offsetof(%s, %s));' % (name, fname, name, fname))
+    lines += ['return 0;', '}']
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.run(["gcc", "-I", inc, str(src), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    for name, cls in structs.items():
+        assert int(got[name]) == ctypes.sizeof(cls), name
+        for fname, _ in cls._fields_:
+            assert int(got["%s.%s" % (name, fname)]) == getattr(cls, fname).offset, (name, fname)

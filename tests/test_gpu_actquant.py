@@ -27,7 +27,7 @@ def nan_padding(orc, gateup, counts, A=128):
     return g, live
 
 
-def run_gpu(ctx, gateup_u16, counts, I, A=128, dense=False, kind=B.MOE_ACT_SILU, limit=0.0):
+def run_gpu(ctx, gateup_u16, counts, I, A=128, dense=False, kind=B.MOE_ACT_SILU, limit=0.0, situ=(4.0, 25.0)):
     M = gateup_u16.shape[0]
     E = len(counts)
     g = dev_bf16(gateup_u16)
@@ -37,7 +37,7 @@ def run_gpu(ctx, gateup_u16, counts, I, A=128, dense=False, kind=B.MOE_ACT_SILU,
     if not dense:
         ends = torch.full((E,), -7, dtype=torch.int32, device="cuda")
         B.moe_expert_ends_from_counts(ctx, dev(np.asarray(counts, np.int32)), A, ends)
-    B.moe_act_quant(ctx, g, out, out_sf, ends, E, A, M, I, kind, limit)
+    B.moe_act_quant(ctx, g, out, out_sf, ends, E, A, M, I, kind, limit, situ=situ)
     torch.cuda.synchronize()
     assert B.moe_get_device_error(ctx) == 0
     return out, out_sf, ends
@@ -129,6 +129,40 @@ def test_every_gate_bit_pattern(ctx, orc, kind, limit):
     assert np.array_equal(host(out_sf), ref_sf)
 
 
+@pytest.mark.parametrize("betas", [(4.0, 25.0), (1.5, 7.0)], ids=["kimi", "other"])
+def test_situ_microbench_shape_bit_exact(ctx, orc, betas):
+    """SiTU (next row f2) over the live rows: codes and scales bit-exact, the
+    padding untouched; a second beta pair refills the context's tables."""
+    gateup, counts = synth.actq_inputs()
+    gateup, live = nan_padding(orc, gateup, counts)
+    out, out_sf, ends = run_gpu(ctx, gateup, counts, synth.ACTQ_I, kind=B.MOE_ACT_SITU, situ=betas)
+    _, ref_end = orc.endpoints(counts, 128)
+    ref, ref_sf = orc.act_quant(gateup, ref_end, 128, situ=betas)
+    assert np.array_equal(host(out), ref)
+    assert np.array_equal(host(out_sf), ref_sf)
+    assert np.all(host(out)[~live] == 0xAB)
+
+
+@pytest.mark.parametrize("half", ["gate", "up"])
+def test_situ_every_bit_pattern(ctx, orc, half):
+    """Each of the 65,536 bf16 patterns once in the gate (or the up) half
+    under SiTU, the other half N(0,1): bit-exact."""
+    I = 2048
+    rows = 65536 // I
+    g = np.random.default_rng(10)
+    pat = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    g.shuffle(pat)
+    other = synth.bf16_normal(g, (rows, I))
+    halves = [pat.reshape(rows, I), other] if half == "gate" else [other, pat.reshape(rows, I)]
+    gateup = np.concatenate(halves, axis=1)
+    out, out_sf, _ = run_gpu(ctx, gateup, [rows], I, kind=B.MOE_ACT_SITU)
+    ref, ref_sf = orc.act_quant(gateup, np.array([rows], np.int32), 128, situ=(4.0, 25.0))
+    got = host(out)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, [(int(r), int(c), int(got[r, c]), int(ref[r, c])) for r, c in bad[:8]]
+    assert np.array_equal(host(out_sf), ref_sf)
+
+
 def test_graph_replay_with_reversed_counts(ctx, orc):
     """Capture endpoints + act-quant once; replay after reversing the counts
     (and refreshing the inputs in place): live outputs bit-exact, padding of
@@ -190,3 +224,8 @@ def test_invalid_arguments_rejected(ctx):
     for bad_limit in (0.0, -1.0, float("nan")):  # the clamp needs L > 0
         with pytest.raises(B.MoeError):
             B.moe_act_quant(ctx, t, t, t, None, 1, 128, 4, 128, B.MOE_ACT_SILU_CLAMP, bad_limit)
+    for bad in ((0.0, 25.0), (4.0, -1.0), (float("inf"), 25.0), (4.0, float("nan"))):  # SiTU betas
+        with pytest.raises(B.MoeError):
+            B.moe_act_quant(ctx, t, t, t, None, 1, 128, 4, 128, B.MOE_ACT_SITU, situ=bad)
+    with pytest.raises(B.MoeError):
+        B.moe_act_quant(ctx, t, t, t, None, 1, 128, 4, 128, 7)  # unknown kind

@@ -129,11 +129,12 @@ def test_combine_bit_exact(ctx, orc):
 
 
 # ------------------------------------------------------------ whole layer
-def make_layer(ctx, cfg, inp, fmt=B.MOE_GEMM_W_E2M1, fused=True):
+def make_layer(ctx, cfg, inp, fmt=B.MOE_GEMM_W_E2M1, fused=True, act_kind=None):
     routing = B.MOE_ROUTE_SIGMOID_BIAS_TOPK if cfg.routing == "sigmoid_bias" else B.MOE_ROUTE_SOFTMAX_TOPK
+    if act_kind is None:
+        act_kind = B.MOE_ACT_SILU_CLAMP if cfg.clamp else B.MOE_ACT_SILU
     layer = MoEFFNLayer(ctx, T=cfg.T, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I, A=cfg.A, cap=cfg.cap, routing=routing,
-                        act_kind=B.MOE_ACT_SILU_CLAMP if cfg.clamp else B.MOE_ACT_SILU, limit=cfg.limit,
-                        rsf=cfg.rsf, w_format=fmt, fused=fused)
+                        act_kind=act_kind, limit=cfg.limit, rsf=cfg.rsf, w_format=fmt, fused=fused)
     layer.load_weights(inp.w13, inp.w13_sf, inp.w2, inp.w2_sf)
     return layer
 
@@ -173,19 +174,21 @@ def test_tiny_layer_vs_oracle(ctx, orc, fused):
     check_ffn_tolerance(host_u16(out), ref)
 
 
-@pytest.mark.parametrize("clamp", [False, True], ids=["silu", "silu_clamp"])
+@pytest.mark.parametrize("act", ["silu", "silu_clamp", "situ"])
 @pytest.mark.parametrize("fmt", [B.MOE_GEMM_W_E2M1, B.MOE_GEMM_W_E4M3], ids=["e2m1", "e4m3"])
-def test_fused_act_quant_equals_separate_kernel(ctx, clamp, fmt):
+def test_fused_act_quant_equals_separate_kernel(ctx, act, fmt):
     """GEMM1 with SiLU*mul + quant in its epilogue gives bit for bit what
     GEMM1 -> bf16 gate/up -> act-quant gives: codes, packed scales (including
     the zero bytes of the last word when I/128 is not a multiple of 4) and the
     layer output. I = 384: three groups of 128."""
+    clamp = act == "silu_clamp"
+    kind = {"silu": B.MOE_ACT_SILU, "silu_clamp": B.MOE_ACT_SILU_CLAMP, "situ": B.MOE_ACT_SITU}[act]
     cfg = synth.FFNConfig("fused", T=700, E=6, k=3, H=512, I=384, seed=14, clamp=clamp,
                           limit=2.5 if clamp else 0.0)
     inp = synth.ffn_inputs(cfg)
     res = []
     for fused in (False, True):
-        layer = make_layer(ctx, cfg, inp, fmt=fmt, fused=fused)
+        layer = make_layer(ctx, cfg, inp, fmt=fmt, fused=fused, act_kind=kind)
         layer.act_fp8.fill_(0xAB)
         layer.act_sf.view(torch.uint8).fill_(0xAB)
         layer.forward(dev_bf16(inp.x), dev(inp.logits))
@@ -200,6 +203,20 @@ def test_fused_act_quant_equals_separate_kernel(ctx, clamp, fmt):
     assert np.array_equal(o0, o1)
     live = live_rows(e0, cfg.cap)
     assert np.all(a1[~live] == 0xAB)
+
+
+def test_tiny_layer_situ_vs_oracle(ctx, orc):
+    """Layer with the SiTU activation (next row f2), fused GEMM1 epilogue."""
+    cfg = synth.FFNConfig("tiny situ", T=64, E=4, k=2, H=256, I=128, seed=16)
+    inp = synth.ffn_inputs(cfg)
+    layer = make_layer(ctx, cfg, inp, act_kind=B.MOE_ACT_SITU)
+    out = layer.forward(dev_bf16(inp.x), dev(inp.logits))
+    torch.cuda.synchronize()
+    assert B.moe_get_device_error(ctx) == 0
+    ids, w = oracle_layer(orc, cfg, inp)
+    ref = orc.ffn_tokens(inp.x, ids, w, inp.w13, inp.w13_sf, inp.w2, inp.w2_sf,
+                         np.arange(cfg.T, dtype=np.int32), situ=(4.0, 25.0))
+    check_ffn_tolerance(host_u16(out), ref)
 
 
 def test_deepseek_layer_sampled_tokens(ctx, orc):
