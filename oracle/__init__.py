@@ -59,12 +59,14 @@ def _declare(L):
         "orc_route_sigmoid_bias_topk": (None, [_P, _P, _I, _I, _I, _P, _P]),
         "orc_expert_counts": (None, [_P, _L, _I, _P]),
         "orc_endpoints": (None, [_P, _I, _I, _P, _P]),
-        "orc_scatter": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
-        "orc_grouped_gemm": (None, [_P, _P, _I, _I, _P, _I, _I, _P, _P, _I, _P]),
-        "orc_act_quant": (None, [_P, _I, _I, _P, _I, _I, _I, _F, _F, _F, _P, _P, _I]),
+        "orc_scatter": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+        "orc_grouped_gemm": (None, [_P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _I, _I, _P]),
+        "orc_expand_block_scales": (None, [_P, _I, _I, _I, _P]),
+        "orc_act_quant": (None, [_P, _I, _I, _P, _I, _I, _I, _F, _F, _F, _I, _P, _P, _I]),
         "orc_combine": (None, [_P, _I, _P, _P, _I, _I, _F, _P]),
-        "orc_ffn_tokens": (None, [_P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _F, _F, _F, _F, _P, _I, _P]),
-        "orc_ffn_dense": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _F, _F, _F, _F, _P]),
+        "orc_ffn_tokens": (None, [_P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _F, _F, _F, _F, _P, _I,
+                                   _P]),
+        "orc_ffn_dense": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _F, _F, _F, _F, _P]),
         "orc_decode": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
                               _I, _F, _F, _F, _P, _P, _P, _P]),
         "orc_decode_dense": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
@@ -170,26 +172,28 @@ def align4(n):
     return (n + 3) // 4 * 4
 
 
-def scatter(ids, x_bf16, E, A, cap, fp8_fill=0xAB, sf_fill=None):
-    """Returns expert_ends, src2dst, a_fp8 [cap,H], a_sf [G4, align4(cap)].
-    Non-live rows keep the fill value (the oracle only writes live rows)."""
+def scatter(ids, x_bf16, E, A, cap, fp8_fill=0xAB, sf_fill=None, group=128):
+    """Returns expert_ends, src2dst, a_fp8 [cap,H], a_sf [G4, align4(cap)]
+    (G4 = ceil(H/group/4)). Non-live rows keep the fill value (the oracle only
+    writes live rows)."""
     ids = _c(ids, np.int32)
     x = _c(x_bf16, np.uint16)
     T, k = ids.shape
     H = x.shape[1]
-    G4 = (H // 128 + 3) // 4
+    G4 = (H // group + 3) // 4
     ld = align4(cap)
     ends = np.zeros(E, np.int32)
     s2d = np.zeros((T, k), np.int32)
     a = np.full((cap, H), fp8_fill, np.uint8)
     sf = np.full((G4, ld), fp8_fill * 0x01010101 if sf_fill is None else sf_fill, np.uint32).view(np.int32)
-    rc = lib().orc_scatter(_p(ids), _p(x), T, k, E, H, A, cap, ld, _p(ends), _p(s2d), _p(a), _p(sf))
+    rc = lib().orc_scatter(_p(ids), _p(x), T, k, E, H, A, cap, ld, group, _p(ends), _p(s2d), _p(a), _p(sf))
     if rc != 0:
         raise ValueError("capacity exceeded")
     return ends, s2d, a, sf
 
 
-def grouped_gemm(a, a_sf, expert_ends, A, w, w_sf, out=None):
+def grouped_gemm(a, a_sf, expert_ends, A, w, w_sf, out=None, a_group=128, wfmt=0):
+    """wfmt 0: w packed e2m1 [E,N,K/2]; 1: w e4m3 [E,N,K]. w_sf [E,N,K/32]."""
     a = _c(a, np.uint8)
     a_sf = _c(a_sf, np.int32)
     ends = _c(expert_ends, np.int32)
@@ -199,15 +203,26 @@ def grouped_gemm(a, a_sf, expert_ends, A, w, w_sf, out=None):
     E, N = w.shape[0], w.shape[1]
     if out is None:
         out = np.zeros((cap, N), np.uint16)
-    lib().orc_grouped_gemm(_p(a), _p(a_sf), a_sf.shape[1], K, _p(ends), E, A, _p(w), _p(w_sf), N, _p(out))
+    lib().orc_grouped_gemm(_p(a), _p(a_sf), a_sf.shape[1], K, a_group, _p(ends), E, A, _p(w), _p(w_sf), wfmt, N,
+                           _p(out))
     return out
 
 
-def act_quant(gateup, expert_ends, A, clamp=False, limit=0.0, out=None, out_sf=None, fill=0xAB, situ=None):
+def expand_block_scales(sf_blk, N, K):
+    """FP8-block128 scales [E, ceil(N/128), K/128] -> per-(row, 32-K) [E, N, K/32]."""
+    sf_blk = _c(sf_blk, np.uint8)
+    E = sf_blk.shape[0]
+    out = np.zeros((E, N, K // 32), np.uint8)
+    lib().orc_expand_block_scales(_p(sf_blk), E, N, K, _p(out))
+    return out
+
+
+def act_quant(gateup, expert_ends, A, clamp=False, limit=0.0, out=None, out_sf=None, fill=0xAB, situ=None,
+              group=128):
     gateup = _c(gateup, np.uint16)
     M, I2 = gateup.shape
     I = I2 // 2
-    G4 = ((I + 127) // 128 + 3) // 4
+    G4 = ((I + group - 1) // group + 3) // 4
     ld = align4(M)
     if out is None:
         out = np.full((M, I), fill, np.uint8)
@@ -215,7 +230,8 @@ def act_quant(gateup, expert_ends, A, clamp=False, limit=0.0, out=None, out_sf=N
         out_sf = np.full((G4, ld), fill * 0x01010101, np.uint32).view(np.int32)
     ends = None if expert_ends is None else _c(expert_ends, np.int32)
     E = 0 if ends is None else ends.shape[0]
-    lib().orc_act_quant(_p(gateup), M, I, _p(ends), E, A, *_act(clamp, limit, situ), _p(out), _p(out_sf), ld)
+    lib().orc_act_quant(_p(gateup), M, I, _p(ends), E, A, *_act(clamp, limit, situ), group, _p(out), _p(out_sf),
+                        ld)
     return out, out_sf
 
 
@@ -230,7 +246,10 @@ def combine(down, topk_w, src2dst, rsf=1.0):
     return out
 
 
-def ffn_tokens(x, ids, topk_w, w13, w13_sf, w2, w2_sf, tokens, clamp=False, limit=0.0, rsf=1.0, situ=None):
+def ffn_tokens(x, ids, topk_w, w13, w13_sf, w2, w2_sf, tokens, clamp=False, limit=0.0, rsf=1.0, situ=None,
+               wfmt=0, group=128):
+    """wfmt 0: packed e2m1 weights, 1: e4m3; group: activation quantisation
+    group (input and act-quant) 128, or 32 for the MXFP8 recipe."""
     x = _c(x, np.uint16)
     ids = _c(ids, np.int32)
     topk_w = _c(topk_w, np.float32)
@@ -241,11 +260,12 @@ def ffn_tokens(x, ids, topk_w, w13, w13_sf, w2, w2_sf, tokens, clamp=False, limi
     out = np.zeros((tokens.shape[0], H), np.uint16)
     lib().orc_ffn_tokens(_p(x), H, I2 // 2, _p(ids), _p(topk_w), k, E, _p(_c(w13, np.uint8)),
                          _p(_c(w13_sf, np.uint8)), _p(_c(w2, np.uint8)), _p(_c(w2_sf, np.uint8)),
-                         *_act(clamp, limit, situ), float(rsf), _p(tokens), tokens.shape[0], _p(out))
+                         wfmt, group, *_act(clamp, limit, situ), float(rsf), _p(tokens), tokens.shape[0], _p(out))
     return out
 
 
-def ffn_dense(x, ids, topk_w, w13, w13_sf, w2, w2_sf, clamp=False, limit=0.0, rsf=1.0, situ=None):
+def ffn_dense(x, ids, topk_w, w13, w13_sf, w2, w2_sf, clamp=False, limit=0.0, rsf=1.0, situ=None, wfmt=0,
+              group=128):
     x = _c(x, np.uint16)
     ids = _c(ids, np.int32)
     topk_w = _c(topk_w, np.float32)
@@ -255,7 +275,7 @@ def ffn_dense(x, ids, topk_w, w13, w13_sf, w2, w2_sf, clamp=False, limit=0.0, rs
     out = np.zeros((T, H), np.uint16)
     lib().orc_ffn_dense(_p(x), T, H, I2 // 2, _p(ids), _p(topk_w), k, E, _p(_c(w13, np.uint8)),
                         _p(_c(w13_sf, np.uint8)), _p(_c(w2, np.uint8)), _p(_c(w2_sf, np.uint8)),
-                        *_act(clamp, limit, situ), float(rsf), _p(out))
+                        wfmt, group, *_act(clamp, limit, situ), float(rsf), _p(out))
     return out
 
 

@@ -365,7 +365,7 @@ static void starts_from_ends(const int32_t* ends, int E, int A, int32_t* start) 
  * (src2dst = -1). Each token row is quantised once and copied to its rows.
  * Only live rows of a_fp8 / a_sf are written. Returns -1 if end[E-1] > cap. */
 int orc_scatter(const int32_t* ids, const uint16_t* x, int T, int k, int E, int H, int A, int cap,
-                int ld_sf, int32_t* expert_ends, int32_t* src2dst, uint8_t* a_fp8, int32_t* a_sf) {
+                int ld_sf, int group, int32_t* expert_ends, int32_t* src2dst, uint8_t* a_fp8, int32_t* a_sf) {
     long R = (long)T * k;
     int32_t* counts = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
     int32_t* start = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
@@ -378,7 +378,7 @@ int orc_scatter(const int32_t* ids, const uint16_t* x, int T, int k, int E, int 
         if (e < 0 || e >= E) { src2dst[i] = -1; continue; }
         src2dst[i] = start[e] + fill[e]++;
     }
-    int G = H / 128;
+    int G = H / group;
 #pragma omp parallel
     {
         float* v = (float*)malloc(sizeof(float) * (size_t)H);
@@ -387,7 +387,7 @@ int orc_scatter(const int32_t* ids, const uint16_t* x, int T, int k, int E, int 
 #pragma omp for
         for (int t = 0; t < T; t++) {
             for (int h = 0; h < H; h++) v[h] = orc_bf16_to_float(x[(long)t * H + h]);
-            orc_group_quant_row(v, H, 128, q, sf);
+            orc_group_quant_row(v, H, group, q, sf);
             for (int j = 0; j < k; j++) {
                 long dst = src2dst[(long)t * k + j];
                 if (dst < 0) continue;
@@ -408,24 +408,37 @@ int orc_scatter(const int32_t* ids, const uint16_t* x, int T, int k, int E, int 
  * layout; [DG] §2.1.3 recipes (1,128) for activations, (1,32) for MXFP4
  * weights). Weights: w[e][n][k/2] packed, low nibble = even k; scales
  * w_sf[e][n][k/32]. Rows outside [start[e], end[e]) are not written. */
-static double dq_w(const uint8_t* w, const uint8_t* w_sf, int N, int K, int e, int n, int kk) {
+static double dq_w(const uint8_t* w, const uint8_t* w_sf, int wfmt, int N, int K, int e, int n, int kk) {
+    const double s = orc_ue8m0_value(w_sf[((long)e * N + n) * (K / 32) + kk / 32]);
+    if (wfmt == 1) return orc_e4m3_value(w[((long)e * N + n) * K + kk]) * s;
     uint8_t byte = w[((long)e * N + n) * (K / 2) + kk / 2];
     uint8_t nib = (kk & 1) ? (byte >> 4) : (byte & 0xF);
-    return orc_e2m1_value(nib) * orc_ue8m0_value(w_sf[((long)e * N + n) * (K / 32) + kk / 32]);
+    return orc_e2m1_value(nib) * s;
 }
 
-static void gemm_row(const double* a_deq, int K, int e, const uint8_t* w, const uint8_t* w_sf, int N,
+static void gemm_row(const double* a_deq, int K, int e, const uint8_t* w, const uint8_t* w_sf, int wfmt, int N,
                      uint16_t* out_row) {
     for (int n = 0; n < N; n++) {
         double acc = 0.0;
-        for (int kk = 0; kk < K; kk++) acc += a_deq[kk] * dq_w(w, w_sf, N, K, e, n, kk);
+        for (int kk = 0; kk < K; kk++) acc += a_deq[kk] * dq_w(w, w_sf, wfmt, N, K, e, n, kk);
         out_row[n] = orc_bf16_from_double(acc);
     }
 }
 
-void orc_grouped_gemm(const uint8_t* a, const int32_t* a_sf, int ld_sf, int K,
+/* FP8-block128 weight scales ([DG] §6 "FP8 block128": one UE8M0 scale per
+ * 128 x 128 weight block, sf_blk[e][n/128][k/128]) as per-(row, 32-K) bytes:
+ * sf32[e][n][j] = sf_blk[e][n/128][j/4]. */
+void orc_expand_block_scales(const uint8_t* sf_blk, int E, int N, int K, uint8_t* sf32) {
+    for (int e = 0; e < E; e++)
+        for (int n = 0; n < N; n++)
+            for (int j = 0; j < K / 32; j++)
+                sf32[((long)e * N + n) * (K / 32) + j] =
+                    sf_blk[((long)e * ((N + 127) / 128) + n / 128) * (K / 128) + j / 4];
+}
+
+void orc_grouped_gemm(const uint8_t* a, const int32_t* a_sf, int ld_sf, int K, int a_group,
                       const int32_t* expert_ends, int E, int A,
-                      const uint8_t* w, const uint8_t* w_sf, int N, uint16_t* out) {
+                      const uint8_t* w, const uint8_t* w_sf, int wfmt, int N, uint16_t* out) {
     int32_t* start = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
     starts_from_ends(expert_ends, E, A, start);
     for (int e = 0; e < E; e++) {
@@ -437,8 +450,8 @@ void orc_grouped_gemm(const uint8_t* a, const int32_t* a_sf, int ld_sf, int K,
             for (int r = r0; r < r1; r++) {
                 for (int kk = 0; kk < K; kk++)
                     ad[kk] = orc_e4m3_value(a[(long)r * K + kk]) *
-                             orc_ue8m0_value(unpack_scale(a_sf, ld_sf, r, kk / 128));
-                gemm_row(ad, K, e, w, w_sf, N, out + (long)r * N);
+                             orc_ue8m0_value(unpack_scale(a_sf, ld_sf, r, kk / a_group));
+                gemm_row(ad, K, e, w, w_sf, wfmt, N, out + (long)r * N);
             }
             free(ad);
         }
@@ -481,14 +494,14 @@ static float act_value(float g, float u, const orc_act* act) {
 static void act_quant_row(const uint16_t* row, int I, const orc_act* act, float* h, uint8_t* q, uint8_t* sf) {
     for (int j = 0; j < I; j++)
         h[j] = act_value(orc_bf16_to_float(row[j]), orc_bf16_to_float(row[I + j]), act);
-    orc_group_quant_row(h, I, 128, q, sf);
+    orc_group_quant_row(h, I, act->group, q, sf);
 }
 
 void orc_act_quant(const uint16_t* gateup, int M_alloc, int I, const int32_t* expert_ends, int E,
-                   int A, int act_kind, float limit, float beta_s, float beta_l, uint8_t* out, int32_t* out_sf,
-                   int ld_sf) {
-    const orc_act act = {act_kind, limit, beta_s, beta_l};
-    int G = (I + 127) / 128;
+                   int A, int act_kind, float limit, float beta_s, float beta_l, int group, uint8_t* out,
+                   int32_t* out_sf, int ld_sf) {
+    const orc_act act = {act_kind, limit, beta_s, beta_l, group};
+    int G = (I + group - 1) / group;
     int nseg = expert_ends ? E : 1;
     int32_t* start = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
     if (expert_ends) starts_from_ends(expert_ends, E, A, start);
@@ -537,31 +550,33 @@ void orc_combine(const uint16_t* down, int H, const float* topk_w, const int32_t
  * layout depends only on its own token). Used to check samples of large
  * configurations, and pinned against the layout path on small ones. */
 static void expert_chain(const double* a_deq, int H, int I, int e, const uint8_t* w13,
-                         const uint8_t* w13_sf, const uint8_t* w2, const uint8_t* w2_sf, const orc_act* act,
-                         uint16_t* gu, float* h, uint8_t* q, uint8_t* sf, double* act_deq, uint16_t* down_row) {
-    gemm_row(a_deq, H, e, w13, w13_sf, 2 * I, gu);
+                         const uint8_t* w13_sf, const uint8_t* w2, const uint8_t* w2_sf, int wfmt,
+                         const orc_act* act, uint16_t* gu, float* h, uint8_t* q, uint8_t* sf, double* act_deq,
+                         uint16_t* down_row) {
+    gemm_row(a_deq, H, e, w13, w13_sf, wfmt, 2 * I, gu);
     act_quant_row(gu, I, act, h, q, sf);
-    for (int i = 0; i < I; i++) act_deq[i] = orc_e4m3_value(q[i]) * orc_ue8m0_value(sf[i / 128]);
-    gemm_row(act_deq, I, e, w2, w2_sf, H, down_row);
+    for (int i = 0; i < I; i++) act_deq[i] = orc_e4m3_value(q[i]) * orc_ue8m0_value(sf[i / act->group]);
+    gemm_row(act_deq, I, e, w2, w2_sf, wfmt, H, down_row);
 }
 
-static void token_input(const uint16_t* xrow, int H, float* v, uint8_t* q, uint8_t* sf, double* a_deq) {
+static void token_input(const uint16_t* xrow, int H, int group, float* v, uint8_t* q, uint8_t* sf,
+                        double* a_deq) {
     for (int i = 0; i < H; i++) v[i] = orc_bf16_to_float(xrow[i]);
-    orc_group_quant_row(v, H, 128, q, sf);
-    for (int i = 0; i < H; i++) a_deq[i] = orc_e4m3_value(q[i]) * orc_ue8m0_value(sf[i / 128]);
+    orc_group_quant_row(v, H, group, q, sf);
+    for (int i = 0; i < H; i++) a_deq[i] = orc_e4m3_value(q[i]) * orc_ue8m0_value(sf[i / group]);
 }
 
 void orc_ffn_tokens(const uint16_t* x, int H, int I, const int32_t* ids, const float* topk_w, int k,
                     int E, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
-                    const uint8_t* w2_sf, int act_kind, float limit, float beta_s, float beta_l, float rsf,
-                    const int32_t* tokens, int n_tokens, uint16_t* out) {
-    const orc_act act = {act_kind, limit, beta_s, beta_l};
+                    const uint8_t* w2_sf, int wfmt, int group, int act_kind, float limit, float beta_s,
+                    float beta_l, float rsf, const int32_t* tokens, int n_tokens, uint16_t* out) {
+    const orc_act act = {act_kind, limit, beta_s, beta_l, group};
     int maxd = H > 2 * I ? H : 2 * I;
 #pragma omp parallel
     {
         float* v = (float*)malloc(sizeof(float) * (size_t)maxd);
         uint8_t* q = (uint8_t*)malloc((size_t)maxd);
-        uint8_t* sf = (uint8_t*)malloc((size_t)maxd / 128 + 2);
+        uint8_t* sf = (uint8_t*)malloc((size_t)maxd / 32 + 2);
         double* a_deq = (double*)malloc(sizeof(double) * (size_t)H);
         double* act_deq = (double*)malloc(sizeof(double) * (size_t)I);
         uint16_t* gu = (uint16_t*)malloc(sizeof(uint16_t) * 2 * (size_t)I);
@@ -570,12 +585,12 @@ void orc_ffn_tokens(const uint16_t* x, int H, int I, const int32_t* ids, const f
 #pragma omp for schedule(dynamic, 1)
         for (int s = 0; s < n_tokens; s++) {
             int t = tokens[s];
-            token_input(x + (long)t * H, H, v, q, sf, a_deq);
+            token_input(x + (long)t * H, H, group, v, q, sf, a_deq);
             for (int j = 0; j < k; j++) {
                 int e = ids[(long)t * k + j];
                 valid[j] = (e >= 0 && e < E);
                 if (!valid[j]) continue;
-                expert_chain(a_deq, H, I, e, w13, w13_sf, w2, w2_sf, &act, gu, v, q, sf,
+                expert_chain(a_deq, H, I, e, w13, w13_sf, w2, w2_sf, wfmt, &act, gu, v, q, sf,
                              act_deq, down + (long)j * H);
             }
             for (int hh = 0; hh < H; hh++) {
@@ -596,24 +611,24 @@ void orc_ffn_tokens(const uint16_t* x, int H, int I, const int32_t* ids, const f
  * equivalent bit for bit). */
 void orc_ffn_dense(const uint16_t* x, int T, int H, int I, const int32_t* ids, const float* topk_w,
                    int k, int E, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
-                   const uint8_t* w2_sf, int act_kind, float limit, float beta_s, float beta_l, float rsf,
-                   uint16_t* out) {
-    const orc_act act = {act_kind, limit, beta_s, beta_l};
+                   const uint8_t* w2_sf, int wfmt, int group, int act_kind, float limit, float beta_s,
+                   float beta_l, float rsf, uint16_t* out) {
+    const orc_act act = {act_kind, limit, beta_s, beta_l, group};
     int maxd = H > 2 * I ? H : 2 * I;
     uint16_t* all_down = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)T * E * H);
 #pragma omp parallel
     {
         float* v = (float*)malloc(sizeof(float) * (size_t)maxd);
         uint8_t* q = (uint8_t*)malloc((size_t)maxd);
-        uint8_t* sf = (uint8_t*)malloc((size_t)maxd / 128 + 2);
+        uint8_t* sf = (uint8_t*)malloc((size_t)maxd / 32 + 2);
         double* a_deq = (double*)malloc(sizeof(double) * (size_t)H);
         double* act_deq = (double*)malloc(sizeof(double) * (size_t)I);
         uint16_t* gu = (uint16_t*)malloc(sizeof(uint16_t) * 2 * (size_t)I);
 #pragma omp for
         for (int t = 0; t < T; t++) {
-            token_input(x + (long)t * H, H, v, q, sf, a_deq);
+            token_input(x + (long)t * H, H, group, v, q, sf, a_deq);
             for (int e = 0; e < E; e++)
-                expert_chain(a_deq, H, I, e, w13, w13_sf, w2, w2_sf, &act, gu, v, q, sf,
+                expert_chain(a_deq, H, I, e, w13, w13_sf, w2, w2_sf, wfmt, &act, gu, v, q, sf,
                              act_deq, all_down + ((long)t * E + e) * H);
         }
         free(v); free(q); free(sf); free(a_deq); free(act_deq); free(gu);

@@ -47,6 +47,7 @@ float orc_situ_up_spec(float u, float beta_l);
 typedef struct orc_act {
     int kind;
     float limit, beta_s, beta_l;
+    int group; /* quantisation group of the result: 128, or 32 (MXFP8 recipe) */
 } orc_act;
 
 /* group-128 e4m3 quantisation of one fp32 row */
@@ -61,17 +62,20 @@ void orc_route_sigmoid_bias_topk(const float* logits, const float* bias, int T, 
 void orc_expert_counts(const int32_t* ids, long R, int E, int32_t* counts);
 void orc_endpoints(const int32_t* counts, int E, int A, int32_t* start, int32_t* end);
 int  orc_scatter(const int32_t* ids, const uint16_t* x, int T, int k, int E, int H, int A, int cap,
-                 int ld_sf, int32_t* expert_ends, int32_t* src2dst, uint8_t* a_fp8, int32_t* a_sf);
+                 int ld_sf, int group, int32_t* expert_ends, int32_t* src2dst, uint8_t* a_fp8, int32_t* a_sf);
 
-/* grouped block-scaled GEMM over live rows (fp64 accumulation, one bf16 rounding) */
-void orc_grouped_gemm(const uint8_t* a, const int32_t* a_sf, int ld_sf, int K,
+/* grouped block-scaled GEMM over live rows (fp64 accumulation, one bf16
+ * rounding); a_group 128 or 32; wfmt 0 packed e2m1 [E][N][K/2], 1 e4m3 [E][N][K];
+ * weight scales per (row, 32-K) bytes [E][N][K/32] */
+void orc_grouped_gemm(const uint8_t* a, const int32_t* a_sf, int ld_sf, int K, int a_group,
                       const int32_t* expert_ends, int E, int A,
-                      const uint8_t* w, const uint8_t* w_sf, int N, uint16_t* out);
+                      const uint8_t* w, const uint8_t* w_sf, int wfmt, int N, uint16_t* out);
+void orc_expand_block_scales(const uint8_t* sf_blk, int E, int N, int K, uint8_t* sf32);
 
 /* live-row SiLU*mul + e4m3/UE8M0 quantisation; expert_ends == NULL means every row */
 void orc_act_quant(const uint16_t* gateup, int M_alloc, int I, const int32_t* expert_ends, int E,
-                   int A, int act_kind, float limit, float beta_s, float beta_l, uint8_t* out, int32_t* out_sf,
-                   int ld_sf);
+                   int A, int act_kind, float limit, float beta_s, float beta_l, int group, uint8_t* out,
+                   int32_t* out_sf, int ld_sf);
 
 /* top-k weighted combine */
 void orc_combine(const uint16_t* down, int H, const float* topk_w, const int32_t* src2dst, int T,
@@ -80,14 +84,14 @@ void orc_combine(const uint16_t* down, int H, const float* topk_w, const int32_t
 /* whole layer, per token, computing only the selected experts (used for samples) */
 void orc_ffn_tokens(const uint16_t* x, int H, int I, const int32_t* ids, const float* topk_w, int k,
                     int E, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
-                    const uint8_t* w2_sf, int act_kind, float limit, float beta_s, float beta_l, float rsf,
-                    const int32_t* tokens, int n_tokens, uint16_t* out);
+                    const uint8_t* w2_sf, int wfmt, int group, int act_kind, float limit, float beta_s,
+                    float beta_l, float rsf, const int32_t* tokens, int n_tokens, uint16_t* out);
 
 /* dense twin: every expert on every token, then select by routing and sum */
 void orc_ffn_dense(const uint16_t* x, int T, int H, int I, const int32_t* ids, const float* topk_w,
                    int k, int E, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
-                   const uint8_t* w2_sf, int act_kind, float limit, float beta_s, float beta_l, float rsf,
-                   uint16_t* out);
+                   const uint8_t* w2_sf, int wfmt, int group, int act_kind, float limit, float beta_s,
+                   float beta_l, float rsf, uint16_t* out);
 
 /* decode GEMV path (bf16 activations, FP8-per-expert or MXFP4 weights) */
 float orc_glu_oai(float g, float u, float alpha, float beta, float limit);

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 from moe_expert_ffn_scatter_gb300 import synth
-from tests.refs import (bf16_bits_to_f64, bf16_ulp, e2m1_decode, e4m3_decode_torch,
+from tests.refs import (bf16_bits_to_f64, bf16_ulp, e2m1_decode, e4m3_decode_torch, e4m3_encode_torch,
                         unpack_scale_bytes)
 
 
@@ -43,6 +43,55 @@ def test_grouped_gemm_matches_numpy_matmul(orc):
         # fp64 sum rounded once to bf16: within half a bf16 ulp of the exact product
         assert np.all(np.abs(got - ref) <= 0.5 * bf16_ulp(ref) + 1e-300)
     assert np.all(out[~live] == 0xDEAD)
+
+
+@pytest.mark.parametrize("recipe", ["mxfp8", "fp8_block128"])
+def test_grouped_gemm_fp8_weight_recipes_match_numpy(orc, recipe):
+    """e4m3 weights with per-(row, 32-K) scales (MXFP8, with group-32
+    activation scales) or with one scale per 128 x 128 block (FP8 block128,
+    group-128 activations): against an fp64 matmul of operands decoded here."""
+    g = np.random.default_rng(5)
+    E, K, N, A = 2, 256, 256, 128
+    counts = np.array([40, 130], np.int32)
+    start, end = orc.endpoints(counts, A)
+    cap = 384
+    group = 32 if recipe == "mxfp8" else 128
+    a = synth.e4m3_codes(g, (cap, K), exp_lo=1, exp_hi=14)
+    sfb = synth.ue8m0_bytes(g, (cap, K // group), -3, 3)
+    a_sf = synth.pack_scale_words(sfb, synth.align4(cap))
+    w = synth.e4m3_codes(g, (E, N, K))
+    if recipe == "mxfp8":
+        w_sf = synth.ue8m0_bytes(g, (E, N, K // 32))
+        wscale = np.repeat(np.ldexp(1.0, w_sf.astype(int) - 127), 32, axis=2)
+    else:
+        blk = synth.ue8m0_bytes(g, (E, N // 128, K // 128))
+        w_sf = orc.expand_block_scales(blk, N, K)
+        wscale = np.repeat(np.repeat(np.ldexp(1.0, blk.astype(int) - 127), 128, axis=1), 128, axis=2)
+    out = orc.grouped_gemm(a, a_sf, end, A, w, w_sf, a_group=group, wfmt=1)
+    wd = e4m3_decode_torch(w) * wscale
+    ad = e4m3_decode_torch(a) * np.repeat(np.ldexp(1.0, sfb.astype(int) - 127), group, axis=1)
+    for e in range(E):
+        r0, r1 = start[e], end[e]
+        ref = ad[r0:r1] @ wd[e].T
+        got = bf16_bits_to_f64(out[r0:r1])
+        assert np.all(np.abs(got - ref) <= 0.5 * bf16_ulp(ref) + 1e-300)
+
+
+def test_e4m3_reencoding_of_e2m1_weights_gives_the_same_gemm(orc):
+    """Every e2m1 value is an e4m3 value: the e4m3 path on the re-encoded
+    weights equals the packed e2m1 path bit for bit."""
+    g = np.random.default_rng(6)
+    E, K, N, A = 2, 256, 128, 128
+    counts = np.array([7, 99], np.int32)
+    _, end = orc.endpoints(counts, A)
+    a, _, a_sf = random_a(g, 256, K)
+    w = synth.e2m1_packed(g, (E, N, K // 2))
+    w_sf = synth.ue8m0_bytes(g, (E, N, K // 32))
+    vals = e2m1_decode(w, K)
+    w8 = e4m3_encode_torch(vals.astype(np.float32))
+    assert np.array_equal(e4m3_decode_torch(w8), vals)
+    assert np.array_equal(orc.grouped_gemm(a, a_sf, end, A, w, w_sf),
+                          orc.grouped_gemm(a, a_sf, end, A, w8, w_sf, wfmt=1))
 
 
 def test_grouped_gemm_identity_weights_return_dequantised_a(orc):
@@ -121,6 +170,27 @@ def test_layout_path_equals_dense_twin_bitwise(orc, clamp, limit):
     assert np.array_equal(out, dense)
     toks = np.array([0, 3, 7, 23], np.int32)
     per = orc.ffn_tokens(inp.x, ids, w, inp.w13, inp.w13_sf, inp.w2, inp.w2_sf, toks, clamp, limit, 1.25)
+    assert np.array_equal(per, out[toks])
+
+
+def test_mxfp8_recipe_layout_path_equals_dense_twin_bitwise(orc):
+    """MXFP8 recipe (group-32 activations, e4m3 weights with per-32 scales):
+    the layout path (scatter -> GEMM -> act-quant -> GEMM -> combine) equals
+    the dense twin and the per-token path bit for bit."""
+    cfg = synth.FFNConfig("tiny", T=24, E=4, k=2, H=256, I=128, seed=0)
+    inp, ids, w = small_layer(cfg, orc)
+    g = np.random.default_rng(8)
+    w13 = synth.e4m3_codes(g, (cfg.E, 2 * cfg.I, cfg.H))
+    w2 = synth.e4m3_codes(g, (cfg.E, cfg.H, cfg.I))
+    ends, s2d, a, a_sf = orc.scatter(ids, inp.x, cfg.E, cfg.A, cfg.cap, group=32)
+    gu = orc.grouped_gemm(a, a_sf, ends, cfg.A, w13, inp.w13_sf, a_group=32, wfmt=1)
+    act, act_sf = orc.act_quant(gu, ends, cfg.A, group=32)
+    down = orc.grouped_gemm(act, act_sf, ends, cfg.A, w2, inp.w2_sf, a_group=32, wfmt=1)
+    out = orc.combine(down, w, s2d)
+    dense = orc.ffn_dense(inp.x, ids, w, w13, inp.w13_sf, w2, inp.w2_sf, wfmt=1, group=32)
+    assert np.array_equal(out, dense)
+    toks = np.array([0, 5, 23], np.int32)
+    per = orc.ffn_tokens(inp.x, ids, w, w13, inp.w13_sf, w2, inp.w2_sf, toks, wfmt=1, group=32)
     assert np.array_equal(per, out[toks])
 
 

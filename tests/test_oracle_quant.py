@@ -45,12 +45,13 @@ def ref_group_quant(v32, group=128):
     return codes, sf
 
 
+@pytest.mark.parametrize("group", [128, 32])
 @pytest.mark.parametrize("seed,scale", [(0, 1.0), (1, 2.0 ** -20), (2, 2.0 ** 30), (3, 1e-38)])
-def test_group_quant_matches_definition(orc, seed, scale):
+def test_group_quant_matches_definition(orc, seed, scale, group):
     g = np.random.default_rng(seed)
     v = (g.standard_normal(1024) * scale).astype(np.float32)
-    codes, sf = orc.group_quant_row(v)
-    rc, rsf = ref_group_quant(v)
+    codes, sf = orc.group_quant_row(v, group)
+    rc, rsf = ref_group_quant(v, group)
     assert np.array_equal(sf, rsf)
     assert np.array_equal(codes, rc)
 
@@ -176,4 +177,34 @@ def test_act_quant_situ_against_fp64(orc):
         assert np.array_equal(unpack_scale_bytes(sf, r + 1, 2)[r], rsf[:2])
         bad += int(np.sum(out[r] != rc))
     assert bad <= 0.005 * out.size
+
+
+def test_scatter_and_act_quant_group32(orc):
+    """The MXFP8 activation recipe (group 32): the scattered rows and the
+    act-quant output carry one scale per 32 columns, packed four per word,
+    each equal to the recipe applied to that 32-column slice."""
+    g = np.random.default_rng(17)
+    T, E, k, H, A = 16, 3, 2, 256, 128
+    x = synth.bf16_normal(g, (T, H))
+    ids = synth.ids_with_counts(g, [10, 0, 22], k)
+    cap = synth.align_up(T * k + E * (A - 1), A)
+    ends, s2d, a, a_sf = orc.scatter(ids, x, E, A, cap, group=32)
+    assert a_sf.shape[0] == H // 128
+    xv = (x.astype(np.uint32) << 16).view(np.float32)
+    for t in range(T):
+        rc, rsf = ref_group_quant(xv[t], 32)
+        for j in range(k):
+            d = s2d[t, j]
+            assert np.array_equal(a[d], rc)
+            assert np.array_equal(unpack_scale_bytes(a_sf, d + 1, H // 32)[d], rsf)
+    I = 256
+    gu = synth.bf16_normal(g, (8, 2 * I))
+    out, out_sf = orc.act_quant(gu, None, 128, group=32)
+    gate = (gu[:, :I].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    up = (gu[:, I:].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    h = (gate / (1.0 + np.exp(-gate)) * up).astype(np.float32)
+    for r in range(8):
+        rc, rsf = ref_group_quant(h[r], 32)
+        assert np.array_equal(unpack_scale_bytes(out_sf, r + 1, I // 32)[r], rsf)
+        assert np.sum(out[r] != rc) <= 2
 
