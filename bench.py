@@ -208,14 +208,16 @@ def layer_parts(B, ctx, L, cfg, stream, x, logits, bias=None):
     def route_scatter():
         L.route_scatter(x, logits, bias, stream=stream)
 
+    g2_format = L.w_format | (B.MOE_GEMM_A_GROUP32 if L.group == 32 else 0)
+
     def gemm1_act():
         B.moe_grouped_gemm_act_quant(ctx, L.a_fp8, L.a_sf, ld, L.expert_ends, cfg.E, cfg.A, cfg.cap, L.w13,
-                                     L.w13_sf, L.w13_format, cfg.I, cfg.H, L.act_fp8, L.act_sf,
-                                     kind=L.act_kind, limit=L.limit, stream=stream)
+                                     L.w13_sf, L.gemm1_format, cfg.I, cfg.H, L.act_fp8, L.act_sf,
+                                     kind=L.act_kind, limit=L.limit, stream=stream, situ=L.situ, group=L.group)
 
     def gemm2():
         B.moe_grouped_gemm(ctx, L.act_fp8, L.act_sf, ld, L.expert_ends, cfg.E, cfg.A, cfg.cap, L.w2, L.w2_sf,
-                           L.w_format, cfg.H, cfg.I, L.down, stream=stream)
+                           g2_format, cfg.H, cfg.I, L.down, stream=stream)
 
     def combine():
         B.moe_combine(ctx, L.down, cfg.H, L.topk_w, L.src2dst, cfg.T, cfg.k, cfg.rsf, L.out, stream=stream)

@@ -134,6 +134,9 @@ typedef struct moe_act_params {
                           pair and refills them on the call's stream when a
                           call asks for another pair, so calls with different
                           pairs must not overlap on different streams. */
+    int32_t quant_group; /* group of the e4m3 result: 128 (also 0), or 32 for
+                            the MXFP8 recipe (next row f4): out_sf is then
+                            [I/128][align4(rows)], four group-32 bytes a word */
 } moe_act_params;
 
 /* ------------------------------------------------------ route + scatter
@@ -182,6 +185,10 @@ typedef struct moe_route_args {
     void* workspace;
     size_t workspace_bytes;
     int32_t T, E, k, H, A, cap;
+    int32_t quant_group; /* input quantisation group: 128 (also 0), or 32 for
+                            the MXFP8 recipe (next row f4); a_sf then holds
+                            the four group-32 scale bytes of each 128 columns
+                            in one word: [H/128][align4(cap)] */
 } moe_route_args;
 
 MOE_API size_t moe_route_scatter_workspace_size(int T, int E, int k);
@@ -231,11 +238,22 @@ MOE_API int moe_route_scatter_noalloc(moe_ctx* ctx, const moe_route_args* args, 
  * are gate rows 128b..128b+127 and rows 256b+128..256b+255 are up rows
  * I+128b..: every 256-column GEMM tile then holds one matching gate/up group,
  * which lets moe_ffn_forward run SiLU*mul and the quantisation inside GEMM1.
+ * FP8 weights (next row f4, [DG] §6 recipes) are prepared with the output
+ * format MOE_GEMM_W_E4M3 and the input flag MOE_GEMM_W_IN_E4M3: w_in is
+ * e4m3 [E][N][K] and is copied (rows reordered with the gate/up flag). Their
+ * scales are per (row, 32-K) bytes [E][N][K/32] (MXFP8 recipe), or, with the
+ * input flag MOE_GEMM_W_SF_BLOCK128, one UE8M0 byte per 128 x 128 block,
+ * [E][ceil(N/128)][K/128] (FP8 block128 recipe), given to every 32-K slot of
+ * the block. The two input flags are for this call only; the GEMMs take the
+ * format without them.
  * Requires K % 128 == 0, N % 128 == 0 (N % 256 with the flag); w_out must not
  * overlap sf_out, and must differ from w_in when widening or reordering. */
 #define MOE_GEMM_W_E2M1 0
 #define MOE_GEMM_W_E4M3 1
 #define MOE_GEMM_W_GATEUP_BLOCK128 2 /* flag, or-ed with the format: w13 only */
+#define MOE_GEMM_W_IN_E4M3 4         /* moe_prepare_weights input flag: w_in is e4m3 [E][N][K] */
+#define MOE_GEMM_W_SF_BLOCK128 8     /* moe_prepare_weights input flag: 128 x 128 block scales */
+#define MOE_GEMM_A_GROUP32 16        /* GEMM flag: the A scales are group-32 words (MXFP8 recipe) */
 MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t* sf_in, int E, int N,
                                 int K, int w_format, uint8_t* w_out, uint32_t* sf_out,
                                 moe_stream_t stream);
@@ -247,7 +265,9 @@ MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t
  *   out[r, n] = bf16( sum_k e4m3(a[r,k]) 2^(sa(r,k/128)-127)
  *                           * e2m1(w[e,n,k]) 2^(sw(e,n,k/32)-127) )
  * for r in [start[e], expert_ends[e]) only; fp32 accumulation in tensor
- * memory (tcgen05, sm_103a). a [cap,K] e4m3; a_sf ASF [ceil(K/512)][ld_sf];
+ * memory (tcgen05, sm_103a). a [cap,K] e4m3; a_sf ASF [ceil(K/512)][ld_sf],
+ * or with the flag MOE_GEMM_A_GROUP32 in w_format (MXFP8 recipe, next row
+ * f4: sa(r, k/32)) [K/128][ld_sf], four group-32 bytes per word;
  * w, w_sf prepared by moe_prepare_weights in format w_format ([E][N][K/2]
  * packed e2m1 or [E][N][K] e4m3; scales [E][K/128][N]); out [cap,N] bf16.
  * Requires 1 <= E <= 4096, K % 128 == 0, N % 256 == 0, cap % 128 == 0,

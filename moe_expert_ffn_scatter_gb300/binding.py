@@ -27,6 +27,9 @@ MOE_GLU_INTERLEAVED = 1
 MOE_GEMM_W_E2M1 = 0
 MOE_GEMM_W_E4M3 = 1
 MOE_GEMM_W_GATEUP_BLOCK128 = 2
+MOE_GEMM_W_IN_E4M3 = 4
+MOE_GEMM_W_SF_BLOCK128 = 8
+MOE_GEMM_A_GROUP32 = 16
 MOE_DEVERR_EXPERT_ID = 0x1
 MOE_DEVERR_CAPACITY = 0x2
 MOE_DEVERR_WAIT_TIMEOUT = 0x4
@@ -48,16 +51,18 @@ class moe_route_args(ctypes.Structure):
     _fields_ = [("routing_mode", _I32), ("logits", _P), ("corr_bias", _P), ("topk_ids", _P), ("topk_w", _P),
                 ("x", _P), ("a_fp8", _P), ("a_sf", _P), ("expert_ends", _P), ("src2dst", _P),
                 ("workspace", _P), ("workspace_bytes", ctypes.c_size_t),
-                ("T", _I32), ("E", _I32), ("k", _I32), ("H", _I32), ("A", _I32), ("cap", _I32)]
+                ("T", _I32), ("E", _I32), ("k", _I32), ("H", _I32), ("A", _I32), ("cap", _I32),
+                ("quant_group", _I32)]
 
 
 class moe_act_params(ctypes.Structure):
-    _fields_ = [("kind", _I32), ("limit", _F), ("situ_beta_s", _F), ("situ_beta_l", _F)]
+    _fields_ = [("kind", _I32), ("limit", _F), ("situ_beta_s", _F), ("situ_beta_l", _F), ("quant_group", _I32)]
 
 
-def act_params(kind=0, limit=0.0, situ=(4.0, 25.0)):
-    """moe_act_params for SiLU / SiLU with clamp limit / SiTU (situ = (beta_s, beta_l))."""
-    return moe_act_params(kind, limit, float(situ[0]), float(situ[1]))
+def act_params(kind=0, limit=0.0, situ=(4.0, 25.0), group=128):
+    """moe_act_params for SiLU / SiLU with clamp limit / SiTU (situ = (beta_s,
+    beta_l)); group: quantisation group of the result, 128 or 32 (MXFP8)."""
+    return moe_act_params(kind, limit, float(situ[0]), float(situ[1]), group)
 
 
 class moe_ffn_args(ctypes.Structure):
@@ -183,19 +188,21 @@ def moe_route_scatter_workspace_size(T, E, k):
 
 
 def moe_route_scatter(ctx, *, routing_mode, x, topk_ids, expert_ends, src2dst, a_fp8, a_sf, workspace,
-                      T, E, k, H, A, cap, logits=None, corr_bias=None, topk_w=None, stream=None):
+                      T, E, k, H, A, cap, logits=None, corr_bias=None, topk_w=None, stream=None, quant_group=128):
     a = moe_route_args(routing_mode, ptr(logits), ptr(corr_bias), ptr(topk_ids), ptr(topk_w), ptr(x),
                        ptr(a_fp8), ptr(a_sf), ptr(expert_ends), ptr(src2dst), ptr(workspace),
-                       workspace.numel() * workspace.element_size(), T, E, k, H, A, cap)
+                       workspace.numel() * workspace.element_size(), T, E, k, H, A, cap, quant_group)
     _check("moe_route_scatter", load().moe_route_scatter(ctx.handle, ctypes.byref(a), cur_stream(stream)))
 
 
 def moe_route_scatter_noalloc(ctx, *, routing_mode, x, topk_ids, expert_ends, src2dst, a_fp8, a_sf,
-                              T, E, k, H, A, cap, logits=None, corr_bias=None, topk_w=None, stream=None):
+                              T, E, k, H, A, cap, logits=None, corr_bias=None, topk_w=None, stream=None,
+                              quant_group=128):
     """moe_route_scatter without a caller workspace: the library's built-in
     scratch array is used (for callers that cannot allocate device memory)."""
     a = moe_route_args(routing_mode, ptr(logits), ptr(corr_bias), ptr(topk_ids), ptr(topk_w), ptr(x),
-                       ptr(a_fp8), ptr(a_sf), ptr(expert_ends), ptr(src2dst), None, 0, T, E, k, H, A, cap)
+                       ptr(a_fp8), ptr(a_sf), ptr(expert_ends), ptr(src2dst), None, 0, T, E, k, H, A, cap,
+                       quant_group)
     _check("moe_route_scatter_noalloc",
            load().moe_route_scatter_noalloc(ctx.handle, ctypes.byref(a), cur_stream(stream)))
 
@@ -213,8 +220,9 @@ def moe_grouped_gemm(ctx, a, a_sf, ld_sf, expert_ends, E, A, cap, w, w_sf, w_for
 
 
 def moe_grouped_gemm_act_quant(ctx, a, a_sf, ld_sf, expert_ends, E, A, cap, w13, w13_sf, w_format, I, K,
-                               out_fp8, out_sf, kind=MOE_ACT_SILU, limit=0.0, stream=None, situ=(4.0, 25.0)):
-    p = act_params(kind, limit, situ)
+                               out_fp8, out_sf, kind=MOE_ACT_SILU, limit=0.0, stream=None, situ=(4.0, 25.0),
+                               group=128):
+    p = act_params(kind, limit, situ, group)
     _check("moe_grouped_gemm_act_quant",
            load().moe_grouped_gemm_act_quant(ctx.handle, ptr(a), ptr(a_sf), ld_sf, ptr(expert_ends), E, A, cap,
                                              ptr(w13), ptr(w13_sf), w_format, I, K, ctypes.byref(p), ptr(out_fp8),
@@ -222,8 +230,8 @@ def moe_grouped_gemm_act_quant(ctx, a, a_sf, ld_sf, expert_ends, E, A, cap, w13,
 
 
 def moe_act_quant(ctx, gateup, out, out_sf, expert_ends, E, A, M_alloc, I, kind=MOE_ACT_SILU, limit=0.0,
-                  stream=None, situ=(4.0, 25.0)):
-    p = act_params(kind, limit, situ)
+                  stream=None, situ=(4.0, 25.0), group=128):
+    p = act_params(kind, limit, situ, group)
     _check("moe_act_quant",
            load().moe_act_quant(ctx.handle, ptr(gateup), ptr(out), ptr(out_sf), ptr(expert_ends), E, A, M_alloc,
                                 I, ctypes.byref(p), cur_stream(stream)))
@@ -237,10 +245,10 @@ def moe_combine(ctx, down, H, topk_w, src2dst, T, k, rsf, out, stream=None):
 
 def moe_ffn_forward(ctx, *, a_fp8, a_sf, expert_ends, w13, w13_sf, w2, w2_sf, gateup, act_fp8, act_sf, down,
                     topk_w, src2dst, out, T, E, k, H, I, A, cap, w_format=MOE_GEMM_W_E2M1, act_kind=MOE_ACT_SILU,
-                    limit=0.0, rsf=1.0, stream=None, situ=(4.0, 25.0)):
+                    limit=0.0, rsf=1.0, stream=None, situ=(4.0, 25.0), act_group=128):
     a = moe_ffn_args(ptr(a_fp8), ptr(a_sf), ptr(expert_ends), ptr(w13), ptr(w13_sf), ptr(w2), ptr(w2_sf),
                      ptr(gateup), ptr(act_fp8), ptr(act_sf), ptr(down), ptr(topk_w), ptr(src2dst), ptr(out),
-                     T, E, k, H, I, A, cap, w_format, act_params(act_kind, limit, situ), rsf)
+                     T, E, k, H, I, A, cap, w_format, act_params(act_kind, limit, situ, act_group), rsf)
     _check("moe_ffn_forward", load().moe_ffn_forward(ctx.handle, ctypes.byref(a), cur_stream(stream)))
 
 

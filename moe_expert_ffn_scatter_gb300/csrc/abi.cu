@@ -150,7 +150,8 @@ MOE_API size_t moe_route_scatter_workspace_size(int T, int E, int k) {
 MOE_API int moe_route_scatter(moe_ctx* ctx, const moe_route_args* a, moe_stream_t stream) {
   if (!ctx || !a) return MOE_ERR_INVALID_ARG;
   if (a->T < 0 || a->E < 1 || a->E > 4096 || a->k < 1 || a->k > 32 || a->k > a->E || a->H < 128 ||
-      a->H % 128 != 0 || a->A < 1 || a->cap < 0)
+      a->H % 128 != 0 || a->A < 1 || a->cap < 0 ||
+      (a->quant_group != 0 && a->quant_group != 128 && a->quant_group != 32))
     return MOE_ERR_INVALID_ARG;
   if (a->routing_mode != MOE_ROUTE_SOFTMAX_TOPK && a->routing_mode != MOE_ROUTE_SIGMOID_BIAS_TOPK &&
       a->routing_mode != MOE_ROUTE_PRECOMPUTED)
@@ -174,7 +175,8 @@ MOE_API int moe_route_scatter(moe_ctx* ctx, const moe_route_args* a, moe_stream_
 // minus the workspace, plus the size limit of the built-in scratch array.
 static int check_route_noalloc(const moe_route_args* a) {
   if (a->T < 0 || a->E < 1 || a->E > 4096 || a->k < 1 || a->k > 32 || a->k > a->E || a->H < 128 ||
-      a->H % 128 != 0 || a->A < 1 || a->cap < 0)
+      a->H % 128 != 0 || a->A < 1 || a->cap < 0 ||
+      (a->quant_group != 0 && a->quant_group != 128 && a->quant_group != 32))
     return MOE_ERR_INVALID_ARG;
   if (a->routing_mode != MOE_ROUTE_SOFTMAX_TOPK && a->routing_mode != MOE_ROUTE_SIGMOID_BIAS_TOPK &&
       a->routing_mode != MOE_ROUTE_PRECOMPUTED)
@@ -206,9 +208,12 @@ MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t
   if (!ctx || !w_in || !sf_in || !w_out || !sf_out || E < 1 || N < 128 || N % 128 != 0 || K < 128 ||
       K % 128 != 0)
     return MOE_ERR_INVALID_ARG;
-  if ((w_format & ~(MOE_GEMM_W_E4M3 | MOE_GEMM_W_GATEUP_BLOCK128)) != 0) return MOE_ERR_INVALID_ARG;
+  if ((w_format & ~(MOE_GEMM_W_E4M3 | MOE_GEMM_W_GATEUP_BLOCK128 | MOE_GEMM_W_IN_E4M3 | MOE_GEMM_W_SF_BLOCK128)) != 0)
+    return MOE_ERR_INVALID_ARG;
+  if ((w_format & MOE_GEMM_W_IN_E4M3) && !(w_format & MOE_GEMM_W_E4M3)) return MOE_ERR_INVALID_ARG;
   if ((w_format & MOE_GEMM_W_GATEUP_BLOCK128) && N % 256 != 0) return MOE_ERR_INVALID_ARG;
-  if ((w_format & (MOE_GEMM_W_E4M3 | MOE_GEMM_W_GATEUP_BLOCK128)) && w_out == w_in) return MOE_ERR_INVALID_ARG;
+  const bool widen = (w_format & MOE_GEMM_W_E4M3) && !(w_format & MOE_GEMM_W_IN_E4M3);
+  if ((widen || (w_format & MOE_GEMM_W_GATEUP_BLOCK128)) && w_out == w_in) return MOE_ERR_INVALID_ARG;
   if (!al(sf_out, 4) || ((w_format & MOE_GEMM_W_E4M3) && !al(w_out, 2))) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
   return cuda_status(moe::launch_prepare_weights(w_in, sf_in, E, N, K, w_format, w_out, sf_out, S(stream)));
@@ -219,7 +224,8 @@ static int check_gemm(const moe::GemmArgs& g) {
   if (g.E < 1 || g.E > 4096 || g.N < 256 || g.N % 256 != 0 || g.K < 128 || g.K % 128 != 0)
     return MOE_ERR_INVALID_ARG;
   if (g.cap < 0 || g.cap % 128 != 0 || g.ld_sf < g.cap || g.ld_sf % 4 != 0) return MOE_ERR_INVALID_ARG;
-  if ((g.w_format & ~(MOE_GEMM_W_E4M3 | MOE_GEMM_W_GATEUP_BLOCK128)) != 0) return MOE_ERR_INVALID_ARG;
+  if ((g.w_format & ~(MOE_GEMM_W_E4M3 | MOE_GEMM_W_GATEUP_BLOCK128 | MOE_GEMM_A_GROUP32)) != 0)
+    return MOE_ERR_INVALID_ARG;
   if (!al(g.a, 16) || !al(g.w, 32) || !al(g.a_sf, 16) || !al(g.w_sf, 16)) return MOE_ERR_INVALID_ARG;
   if (g.epi == 0 ? (!al(g.out, 16)) : (!g.out_q || !g.out_sf || !al(g.out_q, 16) || g.N % 256 != 0))
     return MOE_ERR_INVALID_ARG;
@@ -242,7 +248,10 @@ MOE_API int moe_grouped_gemm(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf
 
 // Activation parameters: SiLU, SiLU with a clamp limit L > 0, or SiTU with
 // finite positive betas.
+static int act_group(const moe_act_params* act) { return act->quant_group == 32 ? 32 : 128; }
+
 static int check_act(const moe_act_params* act) {
+  if (act->quant_group != 0 && act->quant_group != 128 && act->quant_group != 32) return MOE_ERR_INVALID_ARG;
   if (act->kind == MOE_ACT_SILU) return MOE_OK;
   if (act->kind == MOE_ACT_SILU_CLAMP) return (act->limit > 0.0f) ? MOE_OK : MOE_ERR_INVALID_ARG;
   if (act->kind == MOE_ACT_SITU)
@@ -276,8 +285,10 @@ MOE_API int moe_grouped_gemm_act_quant(moe_ctx* ctx, const uint8_t* a, const int
   if (!ctx || !act || A != 128 || !(w_format & MOE_GEMM_W_GATEUP_BLOCK128)) return MOE_ERR_INVALID_ARG;
   if (check_act(act) != MOE_OK) return MOE_ERR_INVALID_ARG;
   if (I < 128 || I % 128 != 0) return MOE_ERR_INVALID_ARG;
-  moe::GemmArgs g{a, a_sf, ld_sf, expert_ends, E, cap, w13, w13_sf, w_format & MOE_GEMM_W_E4M3, 2 * I, K, nullptr};
+  moe::GemmArgs g{a, a_sf, ld_sf, expert_ends, E, cap, w13, w13_sf,
+                  w_format & (MOE_GEMM_W_E4M3 | MOE_GEMM_A_GROUP32), 2 * I, K, nullptr};
   g.epi = epi_of(act);
+  g.out_group = act_group(act);
   g.silu_tbl = ctx->d_silu;
   g.situ_tbl = ctx->d_situ;
   g.out_q = out_fp8;
@@ -305,8 +316,8 @@ MOE_API int moe_act_quant(moe_ctx* ctx, const uint16_t* gateup, uint8_t* out, in
   const int rc = prepare_act(ctx, act, S(stream));
   if (rc != MOE_OK) return rc;
   return cuda_status(moe::launch_act_quant(gateup, out, out_sf, expert_ends, E, A, M_alloc, I, act->kind,
-                                           act->limit, ctx->d_silu, ctx->d_situ, ctx->num_sms, ctx->d_err,
-                                           S(stream)));
+                                           act->limit, ctx->d_silu, ctx->d_situ, act_group(act), ctx->num_sms,
+                                           ctx->d_err, S(stream)));
 }
 
 MOE_API int moe_combine(moe_ctx* ctx, const uint16_t* down, int H, const float* topk_w,
@@ -329,18 +340,22 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* a, moe_stream_t st
   if (check_act(&a->act) != MOE_OK) return MOE_ERR_INVALID_ARG;
   const int ld = (int)align4l(a->cap);
   const int fmt = a->w_format & MOE_GEMM_W_E4M3;
-  moe::GemmArgs g1{a->a_fp8, a->a_sf, ld, a->expert_ends, a->E, a->cap, a->w13, a->w13_sf, fmt,
-                   2 * a->I, a->H, a->gateup};
+  // GEMM1 reads the scatter's scales (their group: the A_GROUP32 flag of
+  // w_format); GEMM2 reads the act-quant's (their group: act.quant_group)
+  const int fmt2 = fmt | (act_group(&a->act) == 32 ? MOE_GEMM_A_GROUP32 : 0);
+  moe::GemmArgs g1{a->a_fp8, a->a_sf, ld, a->expert_ends, a->E, a->cap, a->w13, a->w13_sf,
+                   fmt | (a->w_format & MOE_GEMM_A_GROUP32), 2 * a->I, a->H, a->gateup};
   if (fused) {
     g1.silu_tbl = ctx->d_silu;
     g1.situ_tbl = ctx->d_situ;
     g1.epi = epi_of(&a->act);
+    g1.out_group = act_group(&a->act);
     g1.out_q = a->act_fp8;
     g1.out_sf = a->act_sf;
     g1.ld_out_sf = ld;
     g1.limit = a->act.limit;
   }
-  moe::GemmArgs g2{a->act_fp8, a->act_sf, ld, a->expert_ends, a->E, a->cap, a->w2, a->w2_sf, fmt,
+  moe::GemmArgs g2{a->act_fp8, a->act_sf, ld, a->expert_ends, a->E, a->cap, a->w2, a->w2_sf, fmt2,
                    a->H, a->I, a->down};
   int rc;
   if ((rc = check_gemm(g1)) != MOE_OK || (rc = check_gemm(g2)) != MOE_OK) return rc;
@@ -354,7 +369,8 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* a, moe_stream_t st
     if (!fused &&
         (rc = cuda_status(moe::launch_act_quant(a->gateup, a->act_fp8, a->act_sf, a->expert_ends, a->E, a->A,
                                                 a->cap, a->I, a->act.kind, a->act.limit, ctx->d_silu,
-                                                ctx->d_situ, ctx->num_sms, ctx->d_err, S(stream)))) != MOE_OK)
+                                                ctx->d_situ, act_group(&a->act), ctx->num_sms, ctx->d_err,
+                                                S(stream)))) != MOE_OK)
       return rc;
     if ((rc = moe::launch_grouped_gemm(g2, ctx->encode, ctx->num_sms, ctx->d_err, S(stream))) != MOE_OK) return rc;
   }

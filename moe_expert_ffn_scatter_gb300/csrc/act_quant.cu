@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
                                                              int A, int M_alloc, int I, int ld_sf,
                                                              float limit, const float* __restrict__ silu_tbl,
                                                              const float* __restrict__ situ_tbl,
-                                                             uint32_t* err) {
+                                                             bool g32, uint32_t* err) {
   constexpr bool kClamp = kAct == 1;
   const float silu_limit = kClamp ? spec_silu(limit) : 0.0f;
   int r0 = 0, r1 = M_alloc;
@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
       }
     }
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    // 8 lanes per 128-column group, or 2 per 32-column group (MXFP8)
+    for (int o = g32 ? 1 : 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
     const uint32_t b = active ? group_scale_byte(amax) : 0u;
     if (active) {
       const float sc = pow2_f32(127 - (int)b);
@@ -107,26 +108,34 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
                 (e4m3x2_satfinite(__fmul_rn(h[4 * i + 2], sc), __fmul_rn(h[4 * i + 3], sc)) << 16);
       *reinterpret_cast<uint4*>(out + (size_t)row * I + col) = q;
     }
-    const uint32_t b0 = __shfl_sync(kFull, b, 0), b1 = __shfl_sync(kFull, b, 8);
-    const uint32_t b2 = __shfl_sync(kFull, b, 16), b3 = __shfl_sync(kFull, b, 24);
-    if (lane == 0) out_sf[(size_t)w * ld_sf + row] = (int32_t)(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24));
+    if (g32) {
+      // one word per 128 columns (8 lanes): the bytes of lanes 8q, 8q+2, 8q+4, 8q+6
+      const int q0 = lane & ~7;
+      const uint32_t word = __shfl_sync(kFull, b, q0) | (__shfl_sync(kFull, b, q0 + 2) << 8) |
+                            (__shfl_sync(kFull, b, q0 + 4) << 16) | (__shfl_sync(kFull, b, q0 + 6) << 24);
+      if ((lane & 7) == 0 && active) out_sf[(size_t)(4 * w + (lane >> 3)) * ld_sf + row] = (int32_t)word;
+    } else {
+      const uint32_t b0 = __shfl_sync(kFull, b, 0), b1 = __shfl_sync(kFull, b, 8);
+      const uint32_t b2 = __shfl_sync(kFull, b, 16), b3 = __shfl_sync(kFull, b, 24);
+      if (lane == 0) out_sf[(size_t)w * ld_sf + row] = (int32_t)(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24));
+    }
   }
 }
 
 template <bool kLive>
 cudaError_t launch_kind(const uint16_t* gateup, uint8_t* out, int32_t* out_sf, const int32_t* ends,
                         int E, int A, int M_alloc, int I, int kind, float limit, const float* silu_tbl,
-                        const float* situ_tbl, dim3 grid, uint32_t* err, cudaStream_t st) {
+                        const float* situ_tbl, bool g32, dim3 grid, uint32_t* err, cudaStream_t st) {
   const int ld = (int)align_up64(M_alloc, 4);
   if (kind == MOE_ACT_SILU_CLAMP)
     act_quant_kernel<kLive, 1><<<grid, kThreads, 0, st>>>(gateup, out, out_sf, ends, E, A, M_alloc, I, ld, limit,
-                                                        silu_tbl, situ_tbl, err);
+                                                        silu_tbl, situ_tbl, g32, err);
   else if (kind == MOE_ACT_SITU)
     act_quant_kernel<kLive, 2><<<grid, kThreads, 0, st>>>(gateup, out, out_sf, ends, E, A, M_alloc, I, ld, limit,
-                                                        silu_tbl, situ_tbl, err);
+                                                        silu_tbl, situ_tbl, g32, err);
   else
     act_quant_kernel<kLive, 0><<<grid, kThreads, 0, st>>>(gateup, out, out_sf, ends, E, A, M_alloc, I, ld, limit,
-                                                        silu_tbl, situ_tbl, err);
+                                                        silu_tbl, situ_tbl, g32, err);
   return cudaGetLastError();
 }
 
@@ -164,19 +173,20 @@ cudaError_t launch_situ_table(float* tbl, float beta_s, float beta_l, cudaStream
 
 cudaError_t launch_act_quant(const uint16_t* gateup, uint8_t* out, int32_t* out_sf,
                              const int32_t* expert_ends, int E, int A, int M_alloc, int I, int kind,
-                             float limit, const float* silu_tbl, const float* situ_tbl, int num_sms, uint32_t* err,
-                             cudaStream_t st) {
+                             float limit, const float* silu_tbl, const float* situ_tbl, int group, int num_sms,
+                             uint32_t* err, cudaStream_t st) {
+  const bool g32 = group == 32;
   if (M_alloc == 0) return cudaSuccess;
   if (expert_ends) {
     if (E == 0) return cudaSuccess;
     const int gy = (int)lmin(lmax(2, (4L * num_sms + E - 1) / E), 65535);
     return launch_kind<true>(gateup, out, out_sf, expert_ends, E, A, M_alloc, I, kind, limit, silu_tbl, situ_tbl,
-                             dim3(1, gy, E), err, st);
+                             g32, dim3(1, gy, E), err, st);
   }
   const long items = (long)M_alloc * (((I / 128) + 3) / 4);
   const int gy = (int)lmin((items + 7) / 8, 8L * num_sms);
   return launch_kind<false>(gateup, out, out_sf, nullptr, 0, A, M_alloc, I, kind, limit, silu_tbl, situ_tbl,
-                            dim3(1, gy, 1), err, st);
+                            g32, dim3(1, gy, 1), err, st);
 }
 
 }  // namespace moe

@@ -72,8 +72,11 @@ __device__ __forceinline__ int src_row(int n, int N, bool blocked) {
   return (w < 128) ? (b << 7) + w : (N >> 1) + (b << 7) + (w - 128);
 }
 
+// sf_block: the input holds one scale per 128 x 128 weight block,
+// [E][ceil(N/128)][K/128] (FP8 block128 recipe); each of the block's
+// 32-K scale slots takes it.
 __global__ void prepare_scales_kernel(const uint8_t* __restrict__ sf_in, int E, int N, int K, bool blocked,
-                                      uint32_t* __restrict__ sf_out) {
+                                      bool sf_block, uint32_t* __restrict__ sf_out) {
   const int KC = K / 128;
   const long total = (long)E * KC * N;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
@@ -83,17 +86,22 @@ __global__ void prepare_scales_kernel(const uint8_t* __restrict__ sf_in, int E, 
     const long ec = i / N;
     const int c = (int)(ec % KC);
     const int e = (int)(ec / KC);
-    const uint8_t* p = sf_in + ((size_t)e * N + src_row(n, N, blocked)) * (K / 32) + 4 * c;
-    sf_out[i] = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+    if (sf_block) {
+      const uint32_t b = sf_in[((size_t)e * ((N + 127) / 128) + src_row(n, N, blocked) / 128) * KC + c];
+      sf_out[i] = b * 0x01010101u;
+    } else {
+      const uint8_t* p = sf_in + ((size_t)e * N + src_row(n, N, blocked)) * (K / 32) + 4 * c;
+      sf_out[i] = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+    }
   }
 }
 
 // Packed e2m1 byte pairs -> e4m3 codes (exact: every e2m1 value is an e4m3
 // value), or a copy; rows remapped by src_row. One thread per output byte
-// pair (e4m3) or byte (e2m1).
+// pair (e4m3) or byte (a copy of e2m1, or of e4m3 input when in8).
 __global__ void weights_kernel(const uint8_t* __restrict__ w_in, int E, int N, int K, bool blocked, bool widen,
-                               uint8_t* __restrict__ w_out) {
-  const long rowb = K / 2;
+                               bool in8, uint8_t* __restrict__ w_out) {
+  const long rowb = in8 ? K : K / 2;
   const long nbytes = (long)E * N * rowb;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nbytes; i += (long)gridDim.x * blockDim.x) {
     const long rowi = i / rowb, col = i % rowb;
@@ -122,20 +130,24 @@ cudaError_t launch_combine(const uint16_t* down, int H, const float* topk_w, con
 cudaError_t launch_prepare_weights(const uint8_t* w_in, const uint8_t* sf_in, int E, int N, int K,
                                    int w_format, uint8_t* w_out, uint32_t* sf_out, cudaStream_t st) {
   const bool blocked = (w_format & MOE_GEMM_W_GATEUP_BLOCK128) != 0;
-  const bool widen = (w_format & MOE_GEMM_W_E4M3) != 0;
+  const bool in8 = (w_format & MOE_GEMM_W_IN_E4M3) != 0;
+  const bool widen = (w_format & MOE_GEMM_W_E4M3) != 0 && !in8;
+  const bool sf_block = (w_format & MOE_GEMM_W_SF_BLOCK128) != 0;
   const long words = (long)E * (K / 128) * N;
   if (words > 0) {
-    prepare_scales_kernel<<<(int)lmin((words + 255) / 256, 65535), 256, 0, st>>>(sf_in, E, N, K, blocked, sf_out);
+    prepare_scales_kernel<<<(int)lmin((words + 255) / 256, 65535), 256, 0, st>>>(sf_in, E, N, K, blocked, sf_block,
+                                                                                 sf_out);
     cudaError_t ce = cudaGetLastError();
     if (ce != cudaSuccess) return ce;
   }
-  const long nbytes = (long)E * N * (K / 2);
+  const long nbytes = (long)E * N * (in8 ? K : K / 2);
   if (nbytes == 0) return cudaSuccess;
   if (!blocked && !widen) {
     if (w_out != w_in) return cudaMemcpyAsync(w_out, w_in, (size_t)nbytes, cudaMemcpyDeviceToDevice, st);
     return cudaSuccess;
   }
-  weights_kernel<<<(int)lmin((nbytes + 255) / 256, 65535), 256, 0, st>>>(w_in, E, N, K, blocked, widen, w_out);
+  weights_kernel<<<(int)lmin((nbytes + 255) / 256, 65535), 256, 0, st>>>(w_in, E, N, K, blocked, widen, in8,
+                                                                          w_out);
   return cudaGetLastError();
 }
 

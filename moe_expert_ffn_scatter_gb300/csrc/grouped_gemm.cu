@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     const int32_t* __restrict__ a_sf, int ld_sf, const int32_t* __restrict__ ends, int E, int cap,
     const uint32_t* __restrict__ w_sf, int N, int K, uint16_t* __restrict__ out, uint8_t* __restrict__ out_q,
     int32_t* __restrict__ out_sf, int ld_out_sf, float limit, const float* __restrict__ silu_tbl,
-    const float* __restrict__ situ_tbl, uint32_t* err) {
+    const float* __restrict__ situ_tbl, bool a_g32, bool out_g32, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -285,8 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
         for (int kc = 0; kc < KC; ++kc) {
           if (!(ok = wait_phase(empty_bar(s), ph ^ 1u, abort_flag, err))) break;
           mbar_arrive_expect_tx(sfa_bar(s), SFA_BYTES);
-          bulk_load(sbase + OFF_SFA_IN + s * SFA_BYTES, a_sf + (size_t)(kc >> 2) * ld_sf + m0, SFA_BYTES,
-                    sfa_bar(s));
+          // group-128 scales: word kc/4 holds the k-block's group in byte kc%4;
+          // group-32 scales (MXFP8): word kc holds its four 32-K groups
+          bulk_load(sbase + OFF_SFA_IN + s * SFA_BYTES, a_sf + (size_t)(a_g32 ? kc : (kc >> 2)) * ld_sf + m0,
+                    SFA_BYTES, sfa_bar(s));
           mbar_arrive_expect_tx(full_bar(s), A_BYTES + (kBfp4 ? B_BYTES / 2 : B_BYTES) + SFB_BYTES);
           tma_load_2d(sbase + OFF_A + s * A_BYTES, &tmA, kc * BK, m0, full_bar(s));
           tma_load_2d(sbase + OFF_B + s * B_BYTES, &tmB, kc * BK, e * N + n0, full_bar(s));
@@ -328,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
           const uint32_t b_addr = sbase + OFF_B + s * B_BYTES;
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
-            const uint32_t idesc = ibase | ((uint32_t)k4 << 4) | ((uint32_t)(kc & 3) << 29);
+            const uint32_t idesc = ibase | ((uint32_t)k4 << 4) | ((uint32_t)(a_g32 ? k4 : (kc & 3)) << 29);
             tc_mma(tmem, desc_sw128(a_addr + 32u * k4), desc_sw128(b_addr + 32u * k4), idesc, tsfa, tsfb,
                    (kc | k4) != 0);
           }
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
         // result is bitwise that of the act-quant kernel on that buffer.
         const int grp = n0 / BN;
         const int I = N / 2;
-        float amax = 0.0f;
+        float amax4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // per 32 columns of h
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           const float ga = bf16_lo(packed[i]), gb = bf16_hi(packed[i]);
@@ -431,14 +433,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
           const float2 hh = mul2(make_float2(sa, sb), make_float2(ua, ub));
           packed[i] = __float_as_uint(hh.x);       // h[2i]
           packed[64 + i] = __float_as_uint(hh.y);  // h[2i + 1]
-          amax = fmaxf(amax, fmaxf(fabsf(hh.x), fabsf(hh.y)));
+          amax4[i >> 4] = fmaxf(amax4[i >> 4], fmaxf(fabsf(hh.x), fabsf(hh.y)));
         }
-        const uint32_t b = group_scale_byte(amax);
+        // one scale for the 128 columns, or one per 32 (MXFP8 recipe)
+        uint32_t bq[4];
+        if (out_g32) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) bq[j] = group_scale_byte(amax4[j]);
+        } else {
+          const uint32_t b = group_scale_byte(fmaxf(fmaxf(amax4[0], amax4[1]), fmaxf(amax4[2], amax4[3])));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) bq[j] = b;
+        }
         if (row < row_end) {
-          const float sc = pow2_f32(127 - (int)b);
           uint4* dst = reinterpret_cast<uint4*>(out_q + (size_t)row * I + (size_t)grp * 128);
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
+            const float sc = pow2_f32(127 - (int)bq[v >> 1]);
             uint32_t wq[4];
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
@@ -450,11 +461,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
             }
             dst[v] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
           }
-          uint8_t* sfb = reinterpret_cast<uint8_t*>(out_sf) + ((size_t)(grp >> 2) * ld_out_sf + row) * 4;
-          sfb[grp & 3] = (uint8_t)b;
-          const int G = I / 128;
-          if (grp == G - 1)
-            for (int t = (grp & 3) + 1; t < 4; ++t) sfb[t] = 0;  // unused bytes of the last word
+          if (out_g32) {
+            out_sf[(size_t)grp * ld_out_sf + row] = (int32_t)(bq[0] | (bq[1] << 8) | (bq[2] << 16) | (bq[3] << 24));
+          } else {
+            uint8_t* sfb = reinterpret_cast<uint8_t*>(out_sf) + ((size_t)(grp >> 2) * ld_out_sf + row) * 4;
+            sfb[grp & 3] = (uint8_t)bq[0];
+            const int G = I / 128;
+            if (grp == G - 1)
+              for (int t = (grp & 3) + 1; t < 4; ++t) sfb[t] = 0;  // unused bytes of the last word
+          }
         }
       }
       acc_ph ^= 1u;
@@ -499,7 +514,7 @@ int launch_impl(const GemmArgs& g, EncodeTiledFn encode, int num_sms, uint32_t* 
   if (grid <= 0) return MOE_OK;
   grouped_gemm_kernel<kBfp4, kEpi><<<grid, kThreads, SMEM_BYTES, st>>>(
       tmA, tmB, g.a_sf, g.ld_sf, g.expert_ends, g.E, g.cap, g.w_sf, g.N, g.K, g.out, g.out_q, g.out_sf,
-      g.ld_out_sf, g.limit, g.silu_tbl, g.situ_tbl, err);
+      g.ld_out_sf, g.limit, g.silu_tbl, g.situ_tbl, (g.w_format & MOE_GEMM_A_GROUP32) != 0, g.out_group == 32, err);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

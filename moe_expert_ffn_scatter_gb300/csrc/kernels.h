@@ -28,8 +28,8 @@ cudaError_t launch_silu_table(float* tbl, cudaStream_t st);
 cudaError_t launch_situ_table(float* tbl, float beta_s, float beta_l, cudaStream_t st);
 cudaError_t launch_act_quant(const uint16_t* gateup, uint8_t* out, int32_t* out_sf,
                              const int32_t* expert_ends, int E, int A, int M_alloc, int I, int kind,
-                             float limit, const float* silu_tbl, const float* situ_tbl, int num_sms, uint32_t* err,
-                             cudaStream_t st);
+                             float limit, const float* silu_tbl, const float* situ_tbl, int group, int num_sms,
+                             uint32_t* err, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* down, int H, const float* topk_w, const int32_t* src2dst,
                            int T, int k, float rsf, uint16_t* out, int num_sms, cudaStream_t st);
 cudaError_t launch_prepare_weights(const uint8_t* w_in, const uint8_t* sf_in, int E, int N, int K,
@@ -62,6 +62,7 @@ struct GemmArgs {
   float limit = 0.0f;
   const float* silu_tbl = nullptr;
   const float* situ_tbl = nullptr;
+  int out_group = 128;  // group of the fused epilogue's e4m3 output: 128, or 32
 };
 // Per-device set-up (shared-memory opt-in); called once per context.
 cudaError_t init_grouped_gemm();

@@ -21,8 +21,9 @@
 //      block scan of the A-aligned counts -> expert_ends.
 //   4. scatter_quant_kernel one warp per token: final src2dst = start[e] +
 //      chunk prefix + rank, then the token row is quantised once (16 lanes per
-//      128-column group, uint4 loads) and its codes and packed scale words are
-//      stored to each destination row.
+//      128-column group, or 4 per 32-column group in the MXFP8 recipe; uint4
+//      loads) and its codes and packed scale words are stored to each
+//      destination row.
 #include <climits>
 #include <mutex>
 
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(const uint16_t* __re
                                                             uint8_t* __restrict__ a_fp8,
                                                             int32_t* __restrict__ a_sf, int T, int E,
                                                             int k, int A, int H, int ld_sf, long cap,
-                                                            uint32_t* err) {
+                                                            bool g32, uint32_t* err) {
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   const int G = H / 128;
@@ -335,8 +336,8 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(const uint16_t* __re
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+        // 16 lanes per 128-column group, or 4 per 32-column group (MXFP8)
+        for (int o = g32 ? 2 : 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
         const uint32_t b = active ? group_scale_byte(amax) : 0u;
         const float sc = pow2_f32(127 - (int)b);
         uint2 codes;
@@ -345,6 +346,20 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(const uint16_t* __re
         for (int j = 0; j < k; ++j) {
           const int d = __shfl_sync(kFull, dst, j);
           if (d >= 0 && active) *reinterpret_cast<uint2*>(a_fp8 + (size_t)d * H + col) = codes;
+        }
+        if (g32) {
+          // each half-warp covers 128 columns: its four group bytes, lanes
+          // 0/4/8/12 (+16), make one word
+          uint32_t w2[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            w2[h] = __shfl_sync(kFull, b, 16 * h) | (__shfl_sync(kFull, b, 16 * h + 4) << 8) |
+                    (__shfl_sync(kFull, b, 16 * h + 8) << 16) | (__shfl_sync(kFull, b, 16 * h + 12) << 24);
+          if (dst >= 0) {
+            a_sf[(size_t)(2 * it) * ld_sf + dst] = (int32_t)w2[0];
+            if (it * 256 + 128 < H) a_sf[(size_t)(2 * it + 1) * ld_sf + dst] = (int32_t)w2[1];
+          }
+          continue;
         }
         const uint32_t b_lo = __shfl_sync(kFull, b, 0);
         const uint32_t b_hi = __shfl_sync(kFull, b, 16);
@@ -414,7 +429,7 @@ cudaError_t launch_route_scatter(const moe_route_args& a, int num_sms, uint32_t*
     const int blocks = (int)lmin((a.T + 7) / 8, (long)num_sms * 16);
     scatter_quant_kernel<<<blocks, 256, 0, st>>>(a.x, a.topk_ids, a.src2dst, (const int32_t*)a.workspace,
                                                  a.expert_ends, a.a_fp8, a.a_sf, a.T, a.E, a.k, a.A, a.H,
-                                                 (int)align_up64(a.cap, 4), a.cap, err);
+                                                 (int)align_up64(a.cap, 4), a.cap, a.quant_group == 32, err);
     ce = cudaGetLastError();
   }
   return ce;

@@ -22,10 +22,15 @@ def ceil_div(a, b):
 class MoEFFNLayer:
     def __init__(self, ctx, *, T, E, k, H, I, A=128, cap=None, routing=B.MOE_ROUTE_SOFTMAX_TOPK,
                  act_kind=B.MOE_ACT_SILU, limit=0.0, rsf=1.0, w_format=B.MOE_GEMM_W_E2M1, fused=True,
-                 situ=(4.0, 25.0), device="cuda"):
+                 situ=(4.0, 25.0), recipe="mxfp4", device="cuda"):
         """fused: run SiLU*mul and the quantisation in GEMM1's epilogue (w13 is
         prepared with gate/up rows interleaved in blocks of 128); otherwise
-        GEMM1 writes the bf16 gate/up buffer and the act-quant kernel follows."""
+        GEMM1 writes the bf16 gate/up buffer and the act-quant kernel follows.
+        recipe: "mxfp4" (e2m1 weights, per-32 scales; group-128 e4m3
+        activations; w_format E4M3 widens the weights), "mxfp8" (e4m3 weights
+        with per-32 scales, group-32 activations) or "fp8_block128" (e4m3
+        weights with one scale per 128 x 128 block, group-128 activations)."""
+        assert recipe in ("mxfp4", "mxfp8", "fp8_block128")
         self.ctx = ctx
         self.T, self.E, self.k, self.H, self.I, self.A = T, E, k, H, I, A
         if cap is None:
@@ -33,9 +38,19 @@ class MoEFFNLayer:
         self.cap = cap
         self.routing = routing
         self.act_kind, self.limit, self.rsf, self.situ = act_kind, limit, rsf, situ
+        self.recipe = recipe
+        self.group = 32 if recipe == "mxfp8" else 128
+        if recipe != "mxfp4":
+            w_format = B.MOE_GEMM_W_E4M3
         self.w_format = w_format
         self.fused = fused
         self.w13_format = w_format | (B.MOE_GEMM_W_GATEUP_BLOCK128 if fused else 0)
+        # the input-side flags moe_prepare_weights needs for this recipe
+        self.prep_flags = {"mxfp4": 0, "mxfp8": B.MOE_GEMM_W_IN_E4M3,
+                           "fp8_block128": B.MOE_GEMM_W_IN_E4M3 | B.MOE_GEMM_W_SF_BLOCK128}[recipe]
+        # GEMM1 reads group-32 input scales in the MXFP8 recipe
+        self.gemm1_format = self.w13_format | (B.MOE_GEMM_A_GROUP32 if self.group == 32 else 0)
+        words = lambda K: ceil_div(K, 4 * self.group)
         dev = torch.device(device)
         u8, i32, f32, bf16 = torch.uint8, torch.int32, torch.float32, torch.bfloat16
         self.topk_ids = torch.empty((T, k), dtype=i32, device=dev)
@@ -43,33 +58,38 @@ class MoEFFNLayer:
         self.src2dst = torch.empty((T, k), dtype=i32, device=dev)
         self.expert_ends = torch.zeros((E,), dtype=i32, device=dev)
         self.a_fp8 = torch.empty((cap, H), dtype=u8, device=dev)
-        self.a_sf = torch.empty((ceil_div(H, 512), align4(cap)), dtype=i32, device=dev)
+        self.a_sf = torch.empty((words(H), align4(cap)), dtype=i32, device=dev)
         self.ws = torch.empty((max(16, B.moe_route_scatter_workspace_size(T, E, k)),), dtype=u8, device=dev)
         self.gateup = None if fused else torch.empty((cap, 2 * I), dtype=bf16, device=dev)
         self.act_fp8 = torch.empty((cap, I), dtype=u8, device=dev)
-        self.act_sf = torch.empty((ceil_div(I, 512), align4(cap)), dtype=i32, device=dev)
+        self.act_sf = torch.empty((words(I), align4(cap)), dtype=i32, device=dev)
         self.down = torch.empty((cap, H), dtype=bf16, device=dev)
         self.out = torch.empty((T, H), dtype=bf16, device=dev)
         self.w13 = self.w13_sf = self.w2 = self.w2_sf = None
 
     # ---------------------------------------------------------------- weights
     def load_weights(self, w13, w13_sf, w2, w2_sf, stream=None):
-        """Upload canonical MXFP4 weights (packed e2m1 [E,N,K/2], UE8M0 [E,N,K/32])
-        and prepare them for the grouped GEMM (scale re-layout, optional e4m3)."""
+        """Upload canonical weights and prepare them for the grouped GEMM (scale
+        re-layout, optional e4m3 widening, gate/up interleave). mxfp4: packed
+        e2m1 [E,N,K/2] + UE8M0 [E,N,K/32]; mxfp8: e4m3 [E,N,K] + UE8M0
+        [E,N,K/32]; fp8_block128: e4m3 [E,N,K] + UE8M0 [E,N/128,K/128]."""
         dev = self.out.device
         E, H, I = self.E, self.H, self.I
 
         def prep(w, sf, N, K, fmt):
             w_in = torch.as_tensor(w).to(dev).contiguous()
             sf_in = torch.as_tensor(sf).to(dev).contiguous()
-            if fmt & B.MOE_GEMM_W_E4M3:
+            if self.recipe != "mxfp4" and not fmt & B.MOE_GEMM_W_GATEUP_BLOCK128:
+                w_out = w_in  # e4m3 input used as is
+            elif fmt & B.MOE_GEMM_W_E4M3:
                 w_out = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
             elif fmt & B.MOE_GEMM_W_GATEUP_BLOCK128:
                 w_out = torch.empty((E, N, K // 2), dtype=torch.uint8, device=dev)
             else:
                 w_out = w_in
             sf_out = torch.empty((E, K // 128, N), dtype=torch.int32, device=dev)
-            B.moe_prepare_weights(self.ctx, w_in, sf_in, E, N, K, fmt, w_out, sf_out, stream=stream)
+            B.moe_prepare_weights(self.ctx, w_in, sf_in, E, N, K, fmt | self.prep_flags, w_out, sf_out,
+                                  stream=stream)
             return w_out, sf_out
 
         self.w13, self.w13_sf = prep(w13, w13_sf, 2 * I, H, self.w13_format)
@@ -103,15 +123,16 @@ class MoEFFNLayer:
         B.moe_route_scatter(self.ctx, routing_mode=self.routing, x=x, logits=logits, corr_bias=bias,
                             topk_ids=self.topk_ids, topk_w=self.topk_w, expert_ends=self.expert_ends,
                             src2dst=self.src2dst, a_fp8=self.a_fp8, a_sf=self.a_sf, workspace=self.ws,
-                            T=self.T, E=self.E, k=self.k, H=self.H, A=self.A, cap=self.cap, stream=stream)
+                            T=self.T, E=self.E, k=self.k, H=self.H, A=self.A, cap=self.cap, stream=stream,
+                            quant_group=self.group)
 
     def ffn(self, stream=None):
         B.moe_ffn_forward(self.ctx, a_fp8=self.a_fp8, a_sf=self.a_sf, expert_ends=self.expert_ends, w13=self.w13,
                           w13_sf=self.w13_sf, w2=self.w2, w2_sf=self.w2_sf, gateup=self.gateup,
                           act_fp8=self.act_fp8, act_sf=self.act_sf, down=self.down, topk_w=self.topk_w,
                           src2dst=self.src2dst, out=self.out, T=self.T, E=self.E, k=self.k, H=self.H, I=self.I,
-                          A=self.A, cap=self.cap, w_format=self.w13_format, act_kind=self.act_kind,
-                          limit=self.limit, rsf=self.rsf, stream=stream, situ=self.situ)
+                          A=self.A, cap=self.cap, w_format=self.gemm1_format, act_kind=self.act_kind,
+                          limit=self.limit, rsf=self.rsf, stream=stream, situ=self.situ, act_group=self.group)
 
     def forward(self, x, logits=None, bias=None, stream=None):
         """x [T,H] bf16, logits [T,E] fp32 (device) -> self.out [T,H] bf16."""

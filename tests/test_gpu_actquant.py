@@ -27,17 +27,18 @@ def nan_padding(orc, gateup, counts, A=128):
     return g, live
 
 
-def run_gpu(ctx, gateup_u16, counts, I, A=128, dense=False, kind=B.MOE_ACT_SILU, limit=0.0, situ=(4.0, 25.0)):
+def run_gpu(ctx, gateup_u16, counts, I, A=128, dense=False, kind=B.MOE_ACT_SILU, limit=0.0, situ=(4.0, 25.0),
+            group=128):
     M = gateup_u16.shape[0]
     E = len(counts)
     g = dev_bf16(gateup_u16)
     out = filled((M, I), 0xAB)
-    out_sf = filled((((I // 128) + 3) // 4, synth.align4(M)), 0xAB, torch.int32)
+    out_sf = filled((((I // group) + 3) // 4, synth.align4(M)), 0xAB, torch.int32)
     ends = None
     if not dense:
         ends = torch.full((E,), -7, dtype=torch.int32, device="cuda")
         B.moe_expert_ends_from_counts(ctx, dev(np.asarray(counts, np.int32)), A, ends)
-    B.moe_act_quant(ctx, g, out, out_sf, ends, E, A, M, I, kind, limit, situ=situ)
+    B.moe_act_quant(ctx, g, out, out_sf, ends, E, A, M, I, kind, limit, situ=situ, group=group)
     torch.cuda.synchronize()
     assert B.moe_get_device_error(ctx) == 0
     return out, out_sf, ends
@@ -161,6 +162,27 @@ def test_situ_every_bit_pattern(ctx, orc, half):
     bad = np.argwhere(got != ref)
     assert bad.size == 0, [(int(r), int(c), int(got[r, c]), int(ref[r, c])) for r, c in bad[:8]]
     assert np.array_equal(host(out_sf), ref_sf)
+
+
+@pytest.mark.parametrize("kind,I", [(B.MOE_ACT_SILU, 2048), (B.MOE_ACT_SILU_CLAMP, 384), (B.MOE_ACT_SITU, 640)],
+                         ids=["silu", "clamp_I384", "situ_I640"])
+def test_group32_mxfp8_recipe_bit_exact(ctx, orc, kind, I):
+    """Group-32 e4m3 output (MXFP8 recipe, next row f4): one scale per 32
+    columns, four per word; live rows only, padding untouched."""
+    g = np.random.default_rng(I)
+    counts = np.array([100, 0, 37, 260], np.int32)
+    _, end = orc.endpoints(counts, 128)
+    M = int(synth.align_up(end[-1], 128))
+    gateup = synth.bf16_normal(g, (M, 2 * I))
+    gateup[5, :20] = 0x7FC0
+    gateup, live = nan_padding(orc, gateup, counts)
+    limit = 1.5 if kind == B.MOE_ACT_SILU_CLAMP else 0.0
+    out, out_sf, _ = run_gpu(ctx, gateup, counts, I, kind=kind, limit=limit, group=32)
+    ref, ref_sf = orc.act_quant(gateup, end, 128, clamp=kind == B.MOE_ACT_SILU_CLAMP, limit=limit,
+                                situ=(4.0, 25.0) if kind == B.MOE_ACT_SITU else None, group=32)
+    assert np.array_equal(host(out), ref)
+    assert np.array_equal(host(out_sf), ref_sf)
+    assert np.all(host(out)[~live] == 0xAB)
 
 
 def test_graph_replay_with_reversed_counts(ctx, orc):

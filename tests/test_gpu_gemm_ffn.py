@@ -8,7 +8,7 @@ from moe_expert_ffn_scatter_gb300 import binding as B
 from moe_expert_ffn_scatter_gb300 import synth
 from moe_expert_ffn_scatter_gb300.layer import MoEFFNLayer
 from tests.gpu_util import check_ffn_tolerance, dev, dev_bf16, filled, host, host_u16
-from tests.refs import bf16_bits_to_f64, bf16_ulp, e2m1_decode, e4m3_decode_torch
+from tests.refs import bf16_bits_to_f64, bf16_ulp, e2m1_decode, e4m3_decode_torch, e4m3_encode_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -114,6 +114,51 @@ def test_gemm_no_live_rows(ctx, orc):
     assert np.all(got == 0xABAB)
 
 
+@pytest.mark.parametrize("recipe", ["mxfp8", "fp8_block128"])
+def test_gemm_fp8_weight_recipes(ctx, orc, recipe):
+    """FP8 weights (next row f4): e4m3 with per-32 scales and group-32 A
+    scales (MXFP8), or with 128 x 128 block scales (FP8 block128), prepared
+    from their canonical layouts; against the oracle within the fp32
+    accumulation bound, padding rows untouched."""
+    g = np.random.default_rng(21)
+    E, N, K = 3, 512, 512
+    counts = np.array([150, 0, 77], np.int32)
+    _, ends = orc.endpoints(counts, 128)
+    cap = synth.align_up(int(ends[-1]), 128)
+    group = 32 if recipe == "mxfp8" else 128
+    ld = synth.align4(cap)
+    a = synth.e4m3_codes(g, (cap, K), exp_lo=1, exp_hi=14)
+    sfb = synth.ue8m0_bytes(g, (cap, K // group), -3, 3)
+    a_sf = synth.pack_scale_words(sfb, ld)
+    w = synth.e4m3_codes(g, (E, N, K))
+    if recipe == "mxfp8":
+        w_sf_in = synth.ue8m0_bytes(g, (E, N, K // 32))
+        w_sf = w_sf_in
+        flags = B.MOE_GEMM_W_IN_E4M3
+    else:
+        w_sf_in = synth.ue8m0_bytes(g, (E, N // 128, K // 128))
+        w_sf = orc.expand_block_scales(w_sf_in, N, K)
+        flags = B.MOE_GEMM_W_IN_E4M3 | B.MOE_GEMM_W_SF_BLOCK128
+    wd = dev(w)
+    sf_out = torch.empty((E, K // 128, N), dtype=torch.int32, device="cuda")
+    B.moe_prepare_weights(ctx, wd, dev(w_sf_in), E, N, K, B.MOE_GEMM_W_E4M3 | flags, wd, sf_out)
+    out = filled((cap, N), 0xAB, torch.int16)
+    fmt = B.MOE_GEMM_W_E4M3 | (B.MOE_GEMM_A_GROUP32 if group == 32 else 0)
+    B.moe_grouped_gemm(ctx, dev(a), dev(a_sf), ld, dev(ends), E, 128, cap, wd, sf_out, fmt, N, K, out)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_error(ctx) == 0
+    got = host_u16(out)
+    ref = orc.grouped_gemm(a, a_sf, ends, 128, w, w_sf, out=np.full((cap, N), 0xABAB, np.uint16), a_group=group,
+                           wfmt=1)
+    ad = np.abs(e4m3_decode_torch(a)) * np.repeat(np.ldexp(1.0, sfb.astype(int) - 127), group, axis=1)
+    wabs = np.abs(e4m3_decode_torch(w)) * np.repeat(np.ldexp(1.0, w_sf.astype(int) - 127), 32, axis=2)
+    start = np.concatenate([[0], (ends[:-1] + 127) // 128 * 128])
+    abssum = np.zeros((cap, N))
+    for e in range(E):
+        abssum[start[e]:ends[e]] = ad[start[e]:ends[e]] @ wabs[e].T
+    assert_gemm_close(got, ref, ends, abssum)
+
+
 def test_combine_bit_exact(ctx, orc):
     g = np.random.default_rng(6)
     T, k, H, rows = 333, 6, 4096, 2500
@@ -129,13 +174,18 @@ def test_combine_bit_exact(ctx, orc):
 
 
 # ------------------------------------------------------------ whole layer
-def make_layer(ctx, cfg, inp, fmt=B.MOE_GEMM_W_E2M1, fused=True, act_kind=None):
+def make_layer(ctx, cfg, inp, fmt=B.MOE_GEMM_W_E2M1, fused=True, act_kind=None, recipe="mxfp4"):
     routing = B.MOE_ROUTE_SIGMOID_BIAS_TOPK if cfg.routing == "sigmoid_bias" else B.MOE_ROUTE_SOFTMAX_TOPK
     if act_kind is None:
         act_kind = B.MOE_ACT_SILU_CLAMP if cfg.clamp else B.MOE_ACT_SILU
     layer = MoEFFNLayer(ctx, T=cfg.T, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I, A=cfg.A, cap=cfg.cap, routing=routing,
-                        act_kind=act_kind, limit=cfg.limit, rsf=cfg.rsf, w_format=fmt, fused=fused)
-    layer.load_weights(inp.w13, inp.w13_sf, inp.w2, inp.w2_sf)
+                        act_kind=act_kind, limit=cfg.limit, rsf=cfg.rsf, w_format=fmt, fused=fused, recipe=recipe)
+    if recipe == "mxfp8":  # the same values as e4m3 codes with their per-32 scales
+        w13 = e4m3_encode_torch(e2m1_decode(inp.w13, cfg.H).astype(np.float32))
+        w2 = e4m3_encode_torch(e2m1_decode(inp.w2, cfg.I).astype(np.float32))
+        layer.load_weights(w13, inp.w13_sf, w2, inp.w2_sf)
+    else:
+        layer.load_weights(inp.w13, inp.w13_sf, inp.w2, inp.w2_sf)
     return layer
 
 
@@ -174,7 +224,7 @@ def test_tiny_layer_vs_oracle(ctx, orc, fused):
     check_ffn_tolerance(host_u16(out), ref)
 
 
-@pytest.mark.parametrize("act", ["silu", "silu_clamp", "situ"])
+@pytest.mark.parametrize("act", ["silu", "silu_clamp", "situ", "silu_group32"])
 @pytest.mark.parametrize("fmt", [B.MOE_GEMM_W_E2M1, B.MOE_GEMM_W_E4M3], ids=["e2m1", "e4m3"])
 def test_fused_act_quant_equals_separate_kernel(ctx, act, fmt):
     """GEMM1 with SiLU*mul + quant in its epilogue gives bit for bit what
@@ -182,13 +232,15 @@ def test_fused_act_quant_equals_separate_kernel(ctx, act, fmt):
     the zero bytes of the last word when I/128 is not a multiple of 4) and the
     layer output. I = 384: three groups of 128."""
     clamp = act == "silu_clamp"
-    kind = {"silu": B.MOE_ACT_SILU, "silu_clamp": B.MOE_ACT_SILU_CLAMP, "situ": B.MOE_ACT_SITU}[act]
+    kind = {"silu": B.MOE_ACT_SILU, "silu_clamp": B.MOE_ACT_SILU_CLAMP, "situ": B.MOE_ACT_SITU,
+            "silu_group32": B.MOE_ACT_SILU}[act]
+    recipe = "mxfp8" if act == "silu_group32" else "mxfp4"
     cfg = synth.FFNConfig("fused", T=700, E=6, k=3, H=512, I=384, seed=14, clamp=clamp,
                           limit=2.5 if clamp else 0.0)
     inp = synth.ffn_inputs(cfg)
     res = []
     for fused in (False, True):
-        layer = make_layer(ctx, cfg, inp, fmt=fmt, fused=fused, act_kind=kind)
+        layer = make_layer(ctx, cfg, inp, fmt=fmt, fused=fused, act_kind=kind, recipe=recipe)
         layer.act_fp8.fill_(0xAB)
         layer.act_sf.view(torch.uint8).fill_(0xAB)
         layer.forward(dev_bf16(inp.x), dev(inp.logits))
@@ -203,6 +255,37 @@ def test_fused_act_quant_equals_separate_kernel(ctx, act, fmt):
     assert np.array_equal(o0, o1)
     live = live_rows(e0, cfg.cap)
     assert np.all(a1[~live] == 0xAB)
+
+
+@pytest.mark.parametrize("recipe", ["mxfp8", "fp8_block128"])
+@pytest.mark.parametrize("fused", [False, True], ids=["unfused", "fused"])
+def test_tiny_layer_fp8_recipes_vs_oracle(ctx, orc, recipe, fused):
+    """The whole layer under the FP8 recipes of next row f4."""
+    cfg = synth.FFNConfig("tiny fp8", T=96, E=4, k=2, H=256, I=256, seed=18)
+    inp = synth.ffn_inputs(cfg, weights=False)
+    g = np.random.default_rng(19)
+    w13 = synth.e4m3_codes(g, (cfg.E, 2 * cfg.I, cfg.H))
+    w2 = synth.e4m3_codes(g, (cfg.E, cfg.H, cfg.I))
+    if recipe == "mxfp8":
+        w13_sf = synth.ue8m0_bytes(g, (cfg.E, 2 * cfg.I, cfg.H // 32))
+        w2_sf = synth.ue8m0_bytes(g, (cfg.E, cfg.H, cfg.I // 32))
+        w13_sf32, w2_sf32 = w13_sf, w2_sf
+    else:
+        w13_sf = synth.ue8m0_bytes(g, (cfg.E, 2 * cfg.I // 128, cfg.H // 128))
+        w2_sf = synth.ue8m0_bytes(g, (cfg.E, cfg.H // 128, cfg.I // 128))
+        w13_sf32 = orc.expand_block_scales(w13_sf, 2 * cfg.I, cfg.H)
+        w2_sf32 = orc.expand_block_scales(w2_sf, cfg.H, cfg.I)
+    layer = MoEFFNLayer(ctx, T=cfg.T, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I, A=cfg.A, cap=cfg.cap, recipe=recipe,
+                        fused=fused)
+    layer.load_weights(w13, w13_sf, w2, w2_sf)
+    out = layer.forward(dev_bf16(inp.x), dev(inp.logits))
+    torch.cuda.synchronize()
+    assert B.moe_get_device_error(ctx) == 0
+    ids, w = orc.route_softmax_topk(inp.logits, cfg.k)
+    group = 32 if recipe == "mxfp8" else 128
+    ref = orc.ffn_tokens(inp.x, ids, w, w13, w13_sf32, w2, w2_sf32, np.arange(cfg.T, dtype=np.int32), wfmt=1,
+                         group=group)
+    check_ffn_tolerance(host_u16(out), ref)
 
 
 def test_tiny_layer_situ_vs_oracle(ctx, orc):

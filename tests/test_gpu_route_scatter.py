@@ -17,30 +17,30 @@ def ctx(cuda_lib):
     return B.Context(0)
 
 
-def gpu_route_scatter(ctx, x, E, k, A, cap, mode, logits=None, bias=None, ids=None):
+def gpu_route_scatter(ctx, x, E, k, A, cap, mode, logits=None, bias=None, ids=None, group=128):
     T, H = x.shape
     ids_d = dev(ids) if ids is not None else torch.full((T, k), -9, dtype=torch.int32, device="cuda")
     w_d = torch.full((T, k), -1.0, dtype=torch.float32, device="cuda")
     ends = torch.full((E,), -9, dtype=torch.int32, device="cuda")
     s2d = torch.full((T, k), -9, dtype=torch.int32, device="cuda")
     a = filled((cap, H), 0xAB)
-    a_sf = filled(((H // 128 + 3) // 4, synth.align4(cap)), 0xAB, torch.int32)
+    a_sf = filled(((H // group + 3) // 4, synth.align4(cap)), 0xAB, torch.int32)
     ws = torch.empty((B.moe_route_scatter_workspace_size(T, E, k),), dtype=torch.uint8, device="cuda")
     B.moe_route_scatter(ctx, routing_mode=mode, x=dev_bf16(x), logits=None if logits is None else dev(logits),
                         corr_bias=None if bias is None else dev(bias), topk_ids=ids_d,
                         topk_w=w_d if mode != B.MOE_ROUTE_PRECOMPUTED else None, expert_ends=ends, src2dst=s2d,
-                        a_fp8=a, a_sf=a_sf, workspace=ws, T=T, E=E, k=k, H=H, A=A, cap=cap)
+                        a_fp8=a, a_sf=a_sf, workspace=ws, T=T, E=E, k=k, H=H, A=A, cap=cap, quant_group=group)
     torch.cuda.synchronize()
     assert B.moe_get_device_error(ctx) == 0
     return host(ids_d), host(w_d), host(ends), host(s2d), host(a), host(a_sf)
 
 
-def check_against_oracle(orc, res, ids_ref, x, E, A, cap, w_ref=None):
+def check_against_oracle(orc, res, ids_ref, x, E, A, cap, w_ref=None, group=128):
     ids, w, ends, s2d, a, a_sf = res
     assert np.array_equal(ids, ids_ref)
     if w_ref is not None:
         assert np.array_equal(w.view(np.uint32), w_ref.view(np.uint32))  # bit-exact weights
-    r_ends, r_s2d, r_a, r_sf = orc.scatter(ids_ref, x, E, A, cap)
+    r_ends, r_s2d, r_a, r_sf = orc.scatter(ids_ref, x, E, A, cap, group=group)
     assert np.array_equal(ends, r_ends)
     assert np.array_equal(s2d, r_s2d)
     assert np.array_equal(a, r_a)
@@ -134,6 +134,23 @@ def test_topk_selection_edge_cases(ctx, orc, name, logits, k, bias):
     check_against_oracle(orc, res, ids_ref, x, E, 128, cap)
     finite = np.all(np.isfinite(np.take_along_axis(logits, ids_ref, axis=1)), axis=1)
     assert np.array_equal(res[1][finite].view(np.uint32), w_ref[finite].view(np.uint32))
+
+
+@pytest.mark.parametrize("H", [256, 384, 4096])
+def test_scatter_group32_mxfp8_recipe(ctx, orc, H):
+    """Input quantisation with group 32 (MXFP8 recipe, next row f4): codes and
+    the four-bytes-a-word scale array bit-exact, padding untouched; H = 384
+    leaves half a 256-column pass."""
+    g = np.random.default_rng(H)
+    T, E, k = 300, 8, 3
+    logits = synth.fp32_normal(g, (T, E))
+    x = synth.bf16_normal(g, (T, H))
+    x[5, :40] = 0x7FC0  # NaN values in one group
+    x[6] = 0            # an all-zero row
+    cap = synth.align_up(T * k + E * 127, 128)
+    ids_ref, w_ref = orc.route_softmax_topk(logits, k)
+    res = gpu_route_scatter(ctx, x, E, k, 128, cap, B.MOE_ROUTE_SOFTMAX_TOPK, logits=logits, group=32)
+    check_against_oracle(orc, res, ids_ref, x, E, 128, cap, w_ref, group=32)
 
 
 def test_skewed_routing_one_hot_expert(ctx, orc):
