@@ -69,7 +69,7 @@ def peaks():
 def kernel_source_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("grouped_gemm.cu", "common.cuh"):
+    for f in ("grouped_gemm.cu", "tcgen05.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "moe_expert_ffn_scatter_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -378,12 +378,27 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* args, moe_stream_t
  *   MXFP4_G32:      w_gu [n_local][2I][H/2], w_gu_sf [n_local][2I][H/32],
  *                   w_d [n_local][H][I/2], w_d_sf [n_local][H][I/32]
  *   b_gu [n_local][2I] bf16, b_d [n_local][H] bf16.
- * Requires H % 32 == 0, I % 32 == 0, T <= 64, k <= 32; w_gu, w_d, the MXFP4
- * scale arrays and the biases 16-byte aligned, x and act 8-byte aligned.
- * T <= 8 with H % 64 == 0 and I % 64 == 0 runs on the tensor cores: each
- * selected expert's weights are read once for all tokens (m16n8k16 f16 MMA
- * on exactly converted weights against token columns scaled per token by a
- * power of two). y1 / y2 of non-local slots are never written. */
+ * Requires H % 32 == 0, I % 32 == 0, k <= 32, and T <= 64 -- or T <= 128
+ * with a workspace; w_gu, w_d, the MXFP4 scale arrays and the biases 16-byte
+ * aligned, x and act 8-byte aligned. y1 / y2 / act of non-local slots are
+ * never written.
+ * Paths, each reading every selected local expert's weights once for all the
+ * slots that chose it ([SD] §4 crossover removed):
+ *   - workspace given (at least moe_decode_workspace_size() bytes, 256-byte
+ *     aligned, owned by the caller, contents need not be initialised; not
+ *     shared by calls in flight at the same time), T * k <= 4096,
+ *     num_local_experts <= 1024, H, I >= 128, and for MXFP4 H, I <= 4096,
+ *     H % 64 == I % 64 == 0 and w_gu, w_d 32-byte aligned: the tcgen05
+ *     block-scaled path. The slots are grouped by expert into 16-row
+ *     aligned segments; each bf16 activation row (x, then act) is fed to the
+ *     MMA as two e4m3 terms with group-32 UE8M0 scales (hi = e4m3(v / s_hi),
+ *     lo = e4m3((v - hi s_hi) / s_lo)), which reproduce every value within
+ *     2^13 of its group's maximum exactly and the others to 2^-21 of that
+ *     maximum; the weights enter the tensor cores in their stored format.
+ *   - otherwise T <= 8 with H % 64 == 0 and I % 64 == 0: m16n8k16 f16 MMA on
+ *     exactly converted weights against token columns scaled per token by a
+ *     power of two;
+ *   - otherwise one GEMV block per (token, slot, 32 rows). */
 typedef struct moe_decode_args {
     const uint16_t* x;
     const int32_t* topk_ids;
@@ -404,8 +419,13 @@ typedef struct moe_decode_args {
     uint16_t* y2;
     uint16_t* out;
     int32_t T, H, I, k;
+    void* workspace;        /* device scratch of the tcgen05 path, or NULL */
+    size_t workspace_bytes;
 } moe_decode_args;
 
+/* Bytes of the tcgen05 decode path's workspace for these sizes (0 when the
+ * sizes are out of range). */
+MOE_API size_t moe_decode_workspace_size(int32_t T, int32_t k, int32_t H, int32_t I, int32_t num_local_experts);
 MOE_API int moe_sparse_gemv_decode(moe_ctx* ctx, const moe_decode_args* args, moe_stream_t stream);
 
 #ifdef __cplusplus

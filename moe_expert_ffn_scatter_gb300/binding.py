@@ -80,7 +80,8 @@ class moe_decode_args(ctypes.Structure):
                 ("w_d", _P), ("w_d_scale", _P), ("w_d_sf", _P), ("b_d", _P),
                 ("glu_layout", _I32), ("glu_alpha", _F), ("glu_beta", _F), ("glu_limit", _F),
                 ("y1", _P), ("act", _P), ("y2", _P), ("out", _P),
-                ("T", _I32), ("H", _I32), ("I", _I32), ("k", _I32)]
+                ("T", _I32), ("H", _I32), ("I", _I32), ("k", _I32),
+                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t)]
 
 
 _SIGS = {
@@ -100,6 +101,7 @@ _SIGS = {
     "moe_act_quant": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.POINTER(moe_act_params), _P]),
     "moe_combine": (_I, [_P, _P, _I, _P, _P, _I, _I, _F, _P, _P]),
     "moe_ffn_forward": (_I, [_P, ctypes.POINTER(moe_ffn_args), _P]),
+    "moe_decode_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32, _I32, _I32]),
     "moe_sparse_gemv_decode": (_I, [_P, ctypes.POINTER(moe_decode_args), _P]),
 }
 
@@ -255,9 +257,25 @@ def moe_ffn_forward(ctx, *, a_fp8, a_sf, expert_ends, w13, w13_sf, w2, w2_sf, ga
 def moe_sparse_gemv_decode(ctx, *, x, topk_ids, topk_w, expert_start, num_local_experts, wfmt, w_gu, b_gu, w_d,
                            b_d, y1, act, y2, out, T, H, I, k, w_gu_scale=None, w_gu_sf=None, w_d_scale=None,
                            w_d_sf=None, glu_layout=MOE_GLU_INTERLEAVED, glu_alpha=1.702, glu_beta=1.0,
-                           glu_limit=7.0, stream=None):
+                           glu_limit=7.0, workspace=None, stream=None):
+    """workspace: a uint8 device tensor of at least moe_decode_workspace_size()
+    bytes selects the tcgen05 path (T <= 128); None keeps the mma.sync / GEMV
+    paths (T <= 64)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     a = moe_decode_args(ptr(x), ptr(topk_ids), ptr(topk_w), expert_start, num_local_experts, wfmt,
                         ptr(w_gu), ptr(w_gu_scale), ptr(w_gu_sf), ptr(b_gu), ptr(w_d), ptr(w_d_scale), ptr(w_d_sf),
                         ptr(b_d), glu_layout, glu_alpha, glu_beta, glu_limit, ptr(y1), ptr(act), ptr(y2), ptr(out),
-                        T, H, I, k)
+                        T, H, I, k, ptr(workspace), ws_bytes)
     _check("moe_sparse_gemv_decode", load().moe_sparse_gemv_decode(ctx.handle, ctypes.byref(a), cur_stream(stream)))
+
+
+def moe_decode_workspace_size(T, k, H, I, num_local_experts):
+    return int(load().moe_decode_workspace_size(T, k, H, I, num_local_experts))
+
+
+def decode_workspace(T, k, H, I, num_local_experts, device="cuda"):
+    """Device workspace of the tcgen05 decode path (uint8 tensor)."""
+    n = moe_decode_workspace_size(T, k, H, I, num_local_experts)
+    if n == 0:
+        raise ValueError("decode sizes out of range")
+    return torch.empty(n, dtype=torch.uint8, device=device)

@@ -14,7 +14,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
-SOURCES = ["abi.cu", "route_scatter.cu", "act_quant.cu", "combine.cu", "decode.cu", "grouped_gemm.cu"]
+SOURCES = ["abi.cu", "route_scatter.cu", "act_quant.cu", "combine.cu", "decode.cu", "decode_gemm.cu",
+           "grouped_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-I" + os.path.join(ROOT, "include")]

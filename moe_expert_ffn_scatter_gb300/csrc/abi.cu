@@ -99,6 +99,7 @@ MOE_API int moe_ctx_create(moe_ctx** out, int device) {
   c->situ_bs = 4.0f;  // Kimi's SiTU pair, filled now so that ordinary use never refills
   c->situ_bl = 25.0f;
   if (moe::init_grouped_gemm() != cudaSuccess || moe::init_decode() != cudaSuccess ||
+      moe::init_decode_gemm() != cudaSuccess ||
       cudaMemset(c->d_err, 0, sizeof(uint32_t)) != cudaSuccess ||
       moe::launch_silu_table(c->d_silu, 0) != cudaSuccess ||
       moe::launch_situ_table(c->d_situ, c->situ_bs, c->situ_bl, 0) != cudaSuccess ||
@@ -378,9 +379,15 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* a, moe_stream_t st
                                          ctx->num_sms, S(stream)));
 }
 
+MOE_API size_t moe_decode_workspace_size(int32_t T, int32_t k, int32_t H, int32_t I, int32_t num_local_experts) {
+  if (T < 1 || k < 1 || k > 32 || H < 32 || I < 32 || num_local_experts < 1) return 0;
+  return moe::decode_ws_layout(T, k, H, I, num_local_experts).total;
+}
+
 MOE_API int moe_sparse_gemv_decode(moe_ctx* ctx, const moe_decode_args* a, moe_stream_t stream) {
   if (!ctx || !a) return MOE_ERR_INVALID_ARG;
-  if (a->T < 0 || a->T > 64 || a->k < 1 || a->k > 32 || a->H < 32 || a->H % 32 != 0 || a->I < 32 ||
+  const bool ws = a->workspace != nullptr;
+  if (a->T < 0 || a->T > (ws ? 128 : 64) || a->k < 1 || a->k > 32 || a->H < 32 || a->H % 32 != 0 || a->I < 32 ||
       a->I % 32 != 0 || a->num_local_experts < 0)
     return MOE_ERR_INVALID_ARG;
   if (a->wfmt != MOE_WFMT_FP8_PER_EXPERT && a->wfmt != MOE_WFMT_MXFP4_G32) return MOE_ERR_INVALID_ARG;
@@ -396,7 +403,18 @@ MOE_API int moe_sparse_gemv_decode(moe_ctx* ctx, const moe_decode_args* a, moe_s
         !al(a->act, 8))
       return MOE_ERR_INVALID_ARG;
   }
+  bool tc5 = false;
+  if (ws && a->T > 0) {
+    if (!al(a->workspace, 256)) return MOE_ERR_INVALID_ARG;
+    // e2m1 tensor maps want a 32-byte aligned base
+    tc5 = moe::decode_gemm_ok(a->T, a->k, a->H, a->I, a->num_local_experts, a->wfmt) &&
+          (a->wfmt != MOE_WFMT_MXFP4_G32 || (al(a->w_gu, 32) && al(a->w_d, 32)));
+    if (tc5 && a->workspace_bytes < moe::decode_ws_layout(a->T, a->k, a->H, a->I, a->num_local_experts).total)
+      return MOE_ERR_INVALID_ARG;
+    if (!tc5 && a->T > 64) return MOE_ERR_INVALID_ARG;
+  }
   DeviceGuard g(ctx->device);
+  if (tc5) return moe::launch_decode_gemm(*a, ctx->encode, ctx->num_sms, ctx->d_err, S(stream));
   return cuda_status(moe::launch_decode(*a, ctx->num_sms, ctx->d_err, S(stream)));
 }
 

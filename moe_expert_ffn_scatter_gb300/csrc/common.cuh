@@ -134,6 +134,17 @@ __device__ __forceinline__ float spec_sigmoid(float x) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, spec_exp(-x)));
 }
 
+// gpt-oss GLU of the decode path ([SD] §3): g = min(g, L), u = clamp(u, -L, L)
+// when L > 0; act = (g * sigmoid(alpha g)) * (u + beta).
+__device__ __forceinline__ float glu_value(float g, float u, float alpha, float beta, float limit) {
+  if (limit > 0.0f) {
+    g = fminf(g, limit);
+    u = fminf(fmaxf(u, -limit), limit);
+  }
+  const float s = spec_sigmoid(__fmul_rn(alpha, g));
+  return __fmul_rn(__fmul_rn(g, s), __fadd_rn(u, beta));
+}
+
 // tanh specification (the pages use tanh in SiTU without defining it; the
 // oracle implements the same definition independently):
 //   |y| < 2^-12  -> y

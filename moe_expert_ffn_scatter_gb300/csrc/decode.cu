@@ -173,15 +173,6 @@ __global__ void weighted_sum_kernel(const uint16_t* __restrict__ y2, const int32
   }
 }
 
-__device__ __forceinline__ float glu_value(float g, float u, float alpha, float beta, float limit) {
-  if (limit > 0.0f) {
-    g = fminf(g, limit);
-    u = fminf(fmaxf(u, -limit), limit);
-  }
-  const float s = spec_sigmoid(__fmul_rn(alpha, g));
-  return __fmul_rn(__fmul_rn(g, s), __fadd_rn(u, beta));
-}
-
 // ------------------------------------------------------ tensor-core path
 // For T <= 8 tokens the two GEMVs are skinny GEMMs: [16 weight rows] x [K] x
 // [8 token columns]. One CTA per SM walks a contiguous range of tiles; a tile
@@ -566,6 +557,13 @@ cudaError_t gemv(const uint16_t* x, int x_per_slot, const moe_decode_args& a, co
 
 }  // namespace
 
+cudaError_t launch_weighted_sum(const moe_decode_args& a, bool pdl, cudaStream_t st) {
+  const long total = (long)a.T * a.H;
+  return launch_maybe_pdl(weighted_sum_kernel, dim3((int)lmin((total + 255) / 256, 4096)), dim3(256), 0, st, pdl,
+                          (const uint16_t*)a.y2, a.topk_ids, a.topk_w, a.T, a.k, a.expert_start,
+                          a.num_local_experts, a.H, a.out);
+}
+
 // Shared-memory geometry of the tensor-core path. Row strides are padded so
 // that the warp's 16-byte (FP8) or 4-byte (MXFP4) weight loads and its
 // 16-byte token-column loads hit distinct banks.
@@ -607,24 +605,6 @@ TcGeom tc_geom(int K) {
 template <int WFMT>
 bool tc_ok(int T, int k, int N, int K) {
   return T <= kTcTok && T * k <= kTcMaxSlots && N % kTcRows == 0 && K % 64 == 0 && tc_geom<WFMT>(K).nst >= 2;
-}
-
-// Launch, optionally with programmatic stream serialization (the kernel may
-// start before the previous kernel of the stream has finished).
-template <typename... KArgs, typename... Args>
-cudaError_t launch_maybe_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
-                             Args... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 template <int WFMT>
@@ -686,10 +666,7 @@ cudaError_t launch_decode_tc(const moe_decode_args& a, const float* gu_scale, co
   s.y = a.y2;
   s.act = nullptr;
   if ((ce = launch_tc<WFMT>(s, num_sms, st, true)) != cudaSuccess) return ce;
-  const long total = (long)a.T * a.H;
-  return launch_maybe_pdl(weighted_sum_kernel, dim3((int)lmin((total + 255) / 256, 4096)), dim3(256), 0, st, true,
-                          (const uint16_t*)a.y2, a.topk_ids, a.topk_w, a.T, a.k, a.expert_start,
-                          a.num_local_experts, a.H, a.out);
+  return launch_weighted_sum(a, true, st);
 }
 
 cudaError_t init_decode() {
@@ -725,10 +702,7 @@ cudaError_t launch_decode(const moe_decode_args& a, int num_sms, uint32_t* err, 
   ce = fp8 ? gemv<MOE_WFMT_FP8_PER_EXPERT>(a.act, 1, a, a.w_d, a.w_d_scale, nullptr, a.b_d, a.H, a.I, a.y2, st)
            : gemv<MOE_WFMT_MXFP4_G32>(a.act, 1, a, a.w_d, nullptr, a.w_d_sf, a.b_d, a.H, a.I, a.y2, st);
   if (ce != cudaSuccess) return ce;
-  const long total = (long)a.T * a.H;
-  weighted_sum_kernel<<<(int)lmin((total + 255) / 256, 4096), 256, 0, st>>>(
-      a.y2, a.topk_ids, a.topk_w, a.T, a.k, a.expert_start, a.num_local_experts, a.H, a.out);
-  return cudaGetLastError();
+  return launch_weighted_sum(a, false, st);
 }
 
 }  // namespace moe

@@ -72,5 +72,20 @@ int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, ui
 
 cudaError_t init_decode();
 cudaError_t launch_decode(const moe_decode_args& a, int num_sms, uint32_t* err, cudaStream_t st);
+// out = slot-ordered weighted sum of y2 over local slots (last launch of both
+// decode paths); pdl: may start before the previous kernel has finished.
+cudaError_t launch_weighted_sum(const moe_decode_args& a, bool pdl, cudaStream_t st);
+
+// Workspace of the tcgen05 decode path: byte offsets of its regions (each
+// 1024-byte aligned) and the segment-row capacity R.
+struct DecodeWs {
+  size_t cnt, seg, row_slot, xs, xsf, as, asf, total;
+  int R;
+};
+DecodeWs decode_ws_layout(int T, int k, int H, int I, int n_local);
+bool decode_gemm_ok(int T, int k, int H, int I, int n_local, int wfmt);
+cudaError_t init_decode_gemm();
+// Returns MOE_OK or a MOE_ERR_* code; a.workspace holds decode_ws_layout().total bytes.
+int launch_decode_gemm(const moe_decode_args& a, EncodeTiledFn enc, int num_sms, uint32_t* err, cudaStream_t st);
 
 }  // namespace moe

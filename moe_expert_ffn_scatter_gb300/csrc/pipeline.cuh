@@ -43,7 +43,7 @@ __device__ __forceinline__ uint64_t pipe_globaltimer() {
 // Bounded wait for the phase of `bar` with parity `parity`. Returns false
 // when the wait ran out (error bit and abort flag set) or, with
 // honour_abort, when another role has aborted.
-__device__ __noinline__ bool pipe_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* err,
+static __device__ __noinline__ bool pipe_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* err,
                                        bool honour_abort = true) {
   if (pipe_mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = pipe_globaltimer();
@@ -80,6 +80,24 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // Barrier over the first `threads` threads of the block (named barrier id).
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Launch, optionally with programmatic stream serialization (the kernel may
+// start before the previous kernel of the stream has finished).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_maybe_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                             Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 }  // namespace moe

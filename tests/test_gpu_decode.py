@@ -1,5 +1,7 @@
-"""Sparse decode GEMV path on the GPU against the oracle: FP8-per-expert and
-MXFP4 weights, T in {1, 2, 4, 8}, non-local slots never written and skipped."""
+"""Sparse decode path on the GPU against the oracle: FP8-per-expert and MXFP4
+weights; the mma.sync path (T in {1, 2, 4, 8}, no workspace) and the tcgen05
+path (workspace given, T up to 128); non-local slots never written and
+skipped."""
 import numpy as np
 import pytest
 import torch
@@ -28,7 +30,18 @@ def inputs(T, seed=synth.DECODE_SEED):
     return synth.DecodeInputs(d.x[:T], d.logits[:T], d.fp8, d.mxfp4)
 
 
-def run_decode(ctx, d, ids, w, wfmt, H, I, es, nl, fill=0x7FC0):
+_CACHE_BIG = {}
+
+
+def inputs_big(T, seed=synth.DECODE_SEED + 100):
+    """A 128-token draw (its own weights); smaller T use its first rows."""
+    if seed not in _CACHE_BIG:
+        _CACHE_BIG[seed] = synth.decode_inputs(128, seed=seed)
+    d = _CACHE_BIG[seed]
+    return synth.DecodeInputs(d.x[:T], d.logits[:T], d.fp8, d.mxfp4)
+
+
+def run_decode(ctx, d, ids, w, wfmt, H, I, es, nl, fill=0x7FC0, ws=False, glu_layout=B.MOE_GLU_INTERLEAVED):
     T, k = ids.shape
     W = d.fp8 if wfmt == B.MOE_WFMT_FP8_PER_EXPERT else d.mxfp4
     loc = {kk: v[es:es + nl] for kk, v in W.items()}
@@ -40,18 +53,23 @@ def run_decode(ctx, d, ids, w, wfmt, H, I, es, nl, fill=0x7FC0):
     B.moe_sparse_gemv_decode(ctx, x=dev_bf16(d.x), topk_ids=dev(ids), topk_w=dev(w), expert_start=es,
                              num_local_experts=nl, wfmt=wfmt, w_gu=dev(loc["w_gu"]), b_gu=dev_bf16(loc["b_gu"]),
                              w_d=dev(loc["w_d"]), b_d=dev_bf16(loc["b_d"]), y1=y1, act=act, y2=y2, out=out,
-                             T=T, H=H, I=I, k=k, **kw)
+                             T=T, H=H, I=I, k=k, glu_layout=glu_layout,
+                             workspace=B.decode_workspace(T, k, H, I, nl) if ws else None, **kw)
     torch.cuda.synchronize()
     return host_u16(y1), host_u16(act), host_u16(y2), host_u16(out), loc
 
 
-@pytest.mark.parametrize("wfmt", [B.MOE_WFMT_FP8_PER_EXPERT, B.MOE_WFMT_MXFP4_G32], ids=["fp8", "mxfp4"])
+WFMTS = pytest.mark.parametrize("wfmt", [B.MOE_WFMT_FP8_PER_EXPERT, B.MOE_WFMT_MXFP4_G32], ids=["fp8", "mxfp4"])
+
+
+@WFMTS
+@pytest.mark.parametrize("ws", [False, True], ids=["mma_sync", "tcgen05"])
 @pytest.mark.parametrize("T", [1, 2, 4, 8])
-def test_decode_gpt_oss_shape(ctx, orc, wfmt, T):
+def test_decode_gpt_oss_shape(ctx, orc, wfmt, T, ws):
     d = inputs(T)
     ids, w = orc.route_softmax_topk(d.logits, synth.DECODE_K)
     H = I = synth.DECODE_H
-    y1, act, y2, out, loc = run_decode(ctx, d, ids, w, wfmt, H, I, 0, synth.DECODE_E)
+    y1, act, y2, out, loc = run_decode(ctx, d, ids, w, wfmt, H, I, 0, synth.DECODE_E, ws=ws)
     ry1, ract, ry2, rout = orc.decode(d.x, ids, w, loc, wfmt, I)
     # first GEMV: fp32 accumulation against one fp64 sum
     a, b = bf16_bits_to_f64(y1), bf16_bits_to_f64(ry1)
@@ -59,8 +77,9 @@ def test_decode_gpt_oss_shape(ctx, orc, wfmt, T):
     check_decode_tolerance(out, rout)
 
 
-@pytest.mark.parametrize("wfmt", [B.MOE_WFMT_FP8_PER_EXPERT, B.MOE_WFMT_MXFP4_G32], ids=["fp8", "mxfp4"])
-def test_decode_expert_parallel_slice_skips_nonlocal(ctx, orc, wfmt):
+@WFMTS
+@pytest.mark.parametrize("ws", [False, True], ids=["mma_sync", "tcgen05"])
+def test_decode_expert_parallel_slice_skips_nonlocal(ctx, orc, wfmt, ws):
     """This call owns experts 8..23 only: slots routed elsewhere stay NaN in
     y1/act/y2 and do not reach the output."""
     T = 8
@@ -68,7 +87,7 @@ def test_decode_expert_parallel_slice_skips_nonlocal(ctx, orc, wfmt):
     ids, w = orc.route_softmax_topk(d.logits, synth.DECODE_K)
     H = I = synth.DECODE_H
     es, nl = 8, 16
-    y1, act, y2, out, loc = run_decode(ctx, d, ids, w, wfmt, H, I, es, nl)
+    y1, act, y2, out, loc = run_decode(ctx, d, ids, w, wfmt, H, I, es, nl, ws=ws)
     nonlocal_ = (ids < es) | (ids >= es + nl)
     assert np.all(y1[nonlocal_] == 0x7FC0) and np.all(y2[nonlocal_] == 0x7FC0)
     assert np.all(act.reshape(T, -1, I)[nonlocal_] == 0x7FC0)
@@ -76,3 +95,126 @@ def test_decode_expert_parallel_slice_skips_nonlocal(ctx, orc, wfmt):
     _, _, _, rout = orc.decode(d.x, ids, w, loc, wfmt, I, expert_start=es, n_local=nl)
     local_any = ~nonlocal_.all(axis=1)
     check_decode_tolerance(out[local_any], rout[local_any])
+
+
+def check_first_gemv(y1, ry1, mask=None):
+    """y1 against the oracle: fp32 accumulation of the two-term products
+    against one fp64 sum; 99% of the values within one bf16 step."""
+    a, b = bf16_bits_to_f64(y1), bf16_bits_to_f64(ry1)
+    if mask is not None:
+        a, b = a[mask], b[mask]
+    assert np.mean(np.abs(a - b) <= bf16_ulp(b) * 1.0001) > 0.99
+
+
+@WFMTS
+@pytest.mark.parametrize("T", [16, 37, 64, 128])
+def test_decode_tcgen05_batches(ctx, orc, wfmt, T):
+    """Batches past the mma.sync path's 8 tokens: every expert read once for
+    all slots that chose it (T = 37 leaves ragged segments)."""
+    d = inputs_big(T)
+    ids, w = orc.route_softmax_topk(d.logits, synth.DECODE_K)
+    H = I = synth.DECODE_H
+    y1, act, y2, out, loc = run_decode(ctx, d, ids, w, wfmt, H, I, 0, synth.DECODE_E, ws=True)
+    ry1, ract, ry2, rout = orc.decode(d.x, ids, w, loc, wfmt, I)
+    check_first_gemv(y1, ry1)
+    check_decode_tolerance(out, rout)
+
+
+@WFMTS
+def test_decode_tcgen05_halves_layout(ctx, orc, wfmt):
+    """GLU halves layout: gate rows [0, I), up rows [I, 2I) of w_gu."""
+    T = 24
+    d = inputs_big(T)
+    ids, w = orc.route_softmax_topk(d.logits, synth.DECODE_K)
+    H = I = synth.DECODE_H
+    y1, act, y2, out, loc = run_decode(ctx, d, ids, w, wfmt, H, I, 0, synth.DECODE_E, ws=True,
+                                       glu_layout=B.MOE_GLU_HALVES)
+    ry1, ract, ry2, rout = orc.decode(d.x, ids, w, loc, wfmt, I, interleaved=False)
+    check_first_gemv(y1, ry1)
+    check_decode_tolerance(out, rout)
+
+
+@WFMTS
+def test_decode_tcgen05_hot_expert_two_chunks(ctx, orc, wfmt):
+    """Every one of 100 tokens picks expert 5 (100 slots: two 64-column chunks
+    of one weight block) and three others; expert-parallel slice 0..23."""
+    T, k = 100, synth.DECODE_K
+    d = inputs_big(T)
+    g = np.random.default_rng(7)
+    ids = np.empty((T, k), np.int32)
+    for t in range(T):
+        others = g.choice([e for e in range(synth.DECODE_E) if e != 5], size=k - 1, replace=False)
+        ids[t] = np.concatenate([[5], others])
+        g.shuffle(ids[t])
+    w = g.random((T, k)).astype(np.float32)
+    w /= w.sum(axis=1, keepdims=True)
+    H = I = synth.DECODE_H
+    es, nl = 0, 24
+    y1, act, y2, out, loc = run_decode(ctx, d, ids, w, wfmt, H, I, es, nl, ws=True)
+    ry1, ract, ry2, rout = orc.decode(d.x, ids, w, loc, wfmt, I, expert_start=es, n_local=nl)
+    local = ids < es + nl
+    assert np.all(y1[~local] == 0x7FC0) and np.all(y2[~local] == 0x7FC0)
+    check_first_gemv(y1, ry1, local)
+    local_any = local.any(axis=1)
+    check_decode_tolerance(out[local_any], rout[local_any])
+
+
+def test_decode_tcgen05_graph_replay_new_routing(ctx, orc):
+    """Captured once, replayed with other routing written into the same id and
+    weight buffers: equal to an eager call on that routing."""
+    wfmt = B.MOE_WFMT_MXFP4_G32
+    T, k = 48, synth.DECODE_K
+    H = I = synth.DECODE_H
+    d = inputs_big(T)
+    ids_a, w_a = orc.route_softmax_topk(d.logits, k)
+    ids_b, w_b = orc.route_softmax_topk(d.logits[::-1].copy(), k)
+    W = d.mxfp4
+    x, ids_t, w_t = dev_bf16(d.x), dev(ids_a), dev(w_a)
+    args = dict(expert_start=0, num_local_experts=synth.DECODE_E, wfmt=wfmt, w_gu=dev(W["w_gu"]),
+                w_gu_sf=dev(W["gu_sf"]), b_gu=dev_bf16(W["b_gu"]), w_d=dev(W["w_d"]), w_d_sf=dev(W["d_sf"]),
+                b_d=dev_bf16(W["b_d"]), T=T, H=H, I=I, k=k)
+    bufs = dict(y1=torch.empty((T, k, 2 * I), dtype=torch.bfloat16, device="cuda"),
+                act=torch.empty((T * k, I), dtype=torch.bfloat16, device="cuda"),
+                y2=torch.empty((T, k, H), dtype=torch.bfloat16, device="cuda"),
+                out=torch.empty((T, H), dtype=torch.bfloat16, device="cuda"))
+    ws = B.decode_workspace(T, k, H, I, synth.DECODE_E)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        B.moe_sparse_gemv_decode(ctx, x=x, topk_ids=ids_t, topk_w=w_t, workspace=ws, **args, **bufs)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        B.moe_sparse_gemv_decode(ctx, x=x, topk_ids=ids_t, topk_w=w_t, workspace=ws, **args, **bufs)
+    ids_t.copy_(dev(ids_b))
+    w_t.copy_(dev(w_b))
+    graph.replay()
+    torch.cuda.synchronize()
+    got = host_u16(bufs["out"])
+    eager = {kk: torch.empty_like(v) for kk, v in bufs.items()}
+    B.moe_sparse_gemv_decode(ctx, x=x, topk_ids=dev(ids_b), topk_w=dev(w_b), workspace=ws, **args, **eager)
+    torch.cuda.synchronize()
+    assert np.array_equal(got, host_u16(eager["out"]))
+    _, _, _, rout = orc.decode(d.x, ids_b, w_b, W, wfmt, I)
+    check_decode_tolerance(got, rout)
+
+
+def test_decode_tcgen05_workspace_checks(ctx):
+    """A workspace smaller than moe_decode_workspace_size or misaligned is an
+    invalid argument; T > 128 with a workspace too."""
+    T, k, H, I, nl = 16, 4, 256, 128, 8
+    need = B.moe_decode_workspace_size(T, k, H, I, nl)
+    assert need > 0 and B.moe_decode_workspace_size(0, k, H, I, nl) == 0
+    z = lambda *shape: torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+    u8 = lambda n: torch.zeros(n, dtype=torch.uint8, device="cuda")
+    args = dict(x=z(T, H), topk_ids=torch.zeros((T, k), dtype=torch.int32, device="cuda"),
+                topk_w=torch.zeros((T, k), dtype=torch.float32, device="cuda"), expert_start=0,
+                num_local_experts=nl, wfmt=B.MOE_WFMT_FP8_PER_EXPERT, w_gu=u8(nl * 2 * I * H),
+                w_gu_scale=torch.ones(nl, device="cuda"), b_gu=z(nl, 2 * I), w_d=u8(nl * H * I),
+                w_d_scale=torch.ones(nl, device="cuda"), b_d=z(nl, H), y1=z(T, k, 2 * I), act=z(T * k, I),
+                y2=z(T, k, H), out=z(T, H), T=T, H=H, I=I, k=k)
+    with pytest.raises(B.MoeError):
+        B.moe_sparse_gemv_decode(ctx, workspace=u8(need - 1024), **args)
+    with pytest.raises(B.MoeError):
+        B.moe_sparse_gemv_decode(ctx, workspace=u8(need + 1024)[16:], **args)
+    B.moe_sparse_gemv_decode(ctx, workspace=u8(need), **args)
+    torch.cuda.synchronize()
