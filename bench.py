@@ -42,14 +42,16 @@ def parse():
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--profile-kernel", choices=["route_scatter", "gemm1_act", "gemm2", "combine", "act_quant",
                                                   "kimi_layer", "kimi_route_scatter", "decode_fp8",
-                                                  "decode_mxfp4"],
+                                                  "decode_mxfp4", "decode_fp8_tc5", "decode_mxfp4_tc5"],
                    help="set up the layer, run one full step, then launch only this step's kernel "
                         "warmup + steps times and exit (for ncu captures); prints no JSON line. "
                         "act_quant launches the standalone live-row act-quant kernel at the "
                         "microbench shape (3,072 live of 28,672 rows, I = 2,048); kimi_layer runs "
                         "the Kimi-shaped layer warmup + steps times and prints its timings; "
                         "kimi_route_scatter launches only its routing + scatter (no weights); "
-                        "decode_fp8 / decode_mxfp4 run the T=1 sparse decode over 2 layers")
+                        "decode_fp8 / decode_mxfp4 run the sparse decode over 2 layers on the mma.sync "
+                        "path, the _tc5 forms on the tcgen05 path (T from --decode-tokens)")
+    p.add_argument("--decode-tokens", type=int, default=1)
     return p.parse_args()
 
 
@@ -238,11 +240,13 @@ def run_ours(args):
     if args.profile_kernel == "act_quant":
         profile_act_quant(args, B, synth, torch, np, local)
         return
-    if args.profile_kernel in ("decode_fp8", "decode_mxfp4"):
+    if args.profile_kernel and args.profile_kernel.startswith("decode_"):
         ctx = B.Context(local)
-        wfmt = B.MOE_WFMT_FP8_PER_EXPERT if args.profile_kernel == "decode_fp8" else B.MOE_WFMT_MXFP4_G32
+        wfmt = B.MOE_WFMT_FP8_PER_EXPERT if "fp8" in args.profile_kernel else B.MOE_WFMT_MXFP4_G32
+        tc5 = args.profile_kernel.endswith("_tc5")
         decode_microbench(ctx, B, synth, torch, np, peaks()[0]["hbm_gbs"], n_layers=2,
-                          reps=args.warmup + args.steps, fmts=(wfmt,), tokens=(1,), use_graph=False)
+                          reps=args.warmup + args.steps, fmts=(wfmt,), tokens=() if tc5 else (args.decode_tokens,),
+                          tc5_tokens=(args.decode_tokens,) if tc5 else (), use_graph=False)
         return
     if args.profile_kernel == "kimi_route_scatter":
         from moe_expert_ffn_scatter_gb300.layer import MoEFFNLayer
@@ -538,12 +542,16 @@ def actq_microbench(ctx, B, synth, torch, np, hbm, reps=50):
     return res
 
 
-def decode_microbench(ctx, B, synth, torch, np, hbm, n_layers=24, reps=5, fmts=None, tokens=(1, 8), use_graph=True):
+def decode_microbench(ctx, B, synth, torch, np, hbm, n_layers=24, reps=5, fmts=None, tokens=(1, 8),
+                      tc5_tokens=(1, 8, 32, 128), use_graph=True):
     """gpt-oss-shaped sparse decode (E=32, top-4, H=I=2,880), FP8-per-expert and
-    MXFP4 weights, T in {1, 8}: 24 layers with their own weight copies run in
-    sequence, so L2 (126 MB) cannot serve the 0.4-0.8 GB of weights per layer.
-    Bytes counted: weights (+ scales, bias) of the distinct experts selected."""
+    MXFP4 weights: the mma.sync path (no workspace) at `tokens`, the tcgen05
+    path (workspace) at `tc5_tokens` (keys *_tc5). 24 layers with their own
+    weight copies run in sequence, so L2 (126 MB) cannot serve the 0.4-0.8 GB
+    of weights per layer. Bytes counted: weights (+ scales, bias) of the
+    distinct experts selected."""
     d = synth.decode_inputs(8)
+    x_all = synth.decode_inputs(128, fp8=False, mxfp4=False)  # token rows and logits for T > 8
     E, k, H, I = synth.DECODE_E, synth.DECODE_K, synth.DECODE_H, synth.DECODE_I
     res = {}
     for fmt_name, wfmt, W in (("fp8", B.MOE_WFMT_FP8_PER_EXPERT, d.fp8), ("mxfp4", B.MOE_WFMT_MXFP4_G32, d.mxfp4)):
@@ -555,11 +563,13 @@ def decode_microbench(ctx, B, synth, torch, np, hbm, n_layers=24, reps=5, fmts=N
             layers.append({kk: v.clone() for kk, v in base.items()})
         del base
         per_expert = sum(v[0].numel() * v.element_size() for kk, v in layers[0].items() if kk not in ("gu_scale", "d_scale"))
-        for T in tokens:
-            x = torch.from_numpy(d.x[:T].view(np.int16)).view(torch.bfloat16).cuda()
+        for T, tc5 in [(t, False) for t in tokens] + [(t, True) for t in tc5_tokens]:
+            src = d if T <= 8 else x_all
+            x = torch.from_numpy(src.x[:T].view(np.int16)).view(torch.bfloat16).cuda()
+            ws = B.decode_workspace(T, k, H, I, E) if tc5 else None
             # routing is an input of this call: the 4 largest generator logits per token,
             # slot weights 1/4 each (the decode GEMVs' cost does not depend on them)
-            ids_np = np.argsort(-d.logits[:T], axis=1, kind="stable")[:, :k].astype(np.int32)
+            ids_np = np.argsort(-src.logits[:T], axis=1, kind="stable")[:, :k].astype(np.int32)
             ids = torch.from_numpy(ids_np).cuda()
             w = torch.full((T, k), 0.25, dtype=torch.float32, device="cuda")
             uniq = len(set(ids_np.ravel().tolist()))
@@ -572,7 +582,8 @@ def decode_microbench(ctx, B, synth, torch, np, hbm, n_layers=24, reps=5, fmts=N
                           dict(w_gu_sf=L["gu_sf"], w_d_sf=L["d_sf"]))
                     B.moe_sparse_gemv_decode(ctx, x=x, topk_ids=ids, topk_w=w, expert_start=0, num_local_experts=E,
                                              wfmt=wfmt, w_gu=L["w_gu"], b_gu=L["b_gu"], w_d=L["w_d"], b_d=L["b_d"],
-                                             y1=y1, act=act, y2=y2, out=out, T=T, H=H, I=I, k=k, **kw)
+                                             y1=y1, act=act, y2=y2, out=out, T=T, H=H, I=I, k=k, workspace=ws,
+                                             **kw)
             # decode steps are launch-bound on the host: capture the 24 layers once
             # in a CUDA graph (the layer calls only enqueue fixed grids) and replay
             run_layers()
@@ -598,7 +609,7 @@ def decode_microbench(ctx, B, synth, torch, np, hbm, n_layers=24, reps=5, fmts=N
             del graph
             us_layer = 1e3 * e0.elapsed_time(e1) / (reps * n_layers)
             nbytes = uniq * per_expert
-            res["%s_T%d" % (fmt_name, T)] = {"us_per_layer": us_layer, "us_per_24_layers": us_layer * n_layers,
+            res["%s_T%d%s" % (fmt_name, T, "_tc5" if tc5 else "")] = {"us_per_layer": us_layer, "us_per_24_layers": us_layer * n_layers,
                                              "unique_experts": uniq, "bytes_per_layer": nbytes,
                                              "gbs": nbytes / (us_layer * 1e-6) / 1e9,
                                              "frac_of_hbm": nbytes / (us_layer * 1e-6) / 1e9 / hbm}

@@ -387,8 +387,9 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* args, moe_stream_t
  *   - workspace given (at least moe_decode_workspace_size() bytes, 256-byte
  *     aligned, owned by the caller, contents need not be initialised; not
  *     shared by calls in flight at the same time), T * k <= 4096,
- *     num_local_experts <= 1024, H, I >= 128, and for MXFP4 H, I <= 4096,
- *     H % 64 == I % 64 == 0 and w_gu, w_d 32-byte aligned: the tcgen05
+ *     num_local_experts <= 1024, H, I >= 128, and for MXFP4 H, I <= 3072,
+ *     H % 64 == I % 64 == 0 and w_gu, w_d 32-byte aligned, y1, act, y2
+ *     16-byte aligned: the tcgen05
  *     block-scaled path. The slots are grouped by expert into 16-row
  *     aligned segments; each bf16 activation row (x, then act) is fed to the
  *     MMA as two e4m3 terms with group-32 UE8M0 scales (hi = e4m3(v / s_hi),

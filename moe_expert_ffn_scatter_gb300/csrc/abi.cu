@@ -408,7 +408,8 @@ MOE_API int moe_sparse_gemv_decode(moe_ctx* ctx, const moe_decode_args* a, moe_s
     if (!al(a->workspace, 256)) return MOE_ERR_INVALID_ARG;
     // e2m1 tensor maps want a 32-byte aligned base
     tc5 = moe::decode_gemm_ok(a->T, a->k, a->H, a->I, a->num_local_experts, a->wfmt) &&
-          (a->wfmt != MOE_WFMT_MXFP4_G32 || (al(a->w_gu, 32) && al(a->w_d, 32)));
+          (a->wfmt != MOE_WFMT_MXFP4_G32 || (al(a->w_gu, 32) && al(a->w_d, 32))) && al(a->y1, 16) &&
+          al(a->act, 16) && al(a->y2, 16);
     if (tc5 && a->workspace_bytes < moe::decode_ws_layout(a->T, a->k, a->H, a->I, a->num_local_experts).total)
       return MOE_ERR_INVALID_ARG;
     if (!tc5 && a->T > 64) return MOE_ERR_INVALID_ARG;

@@ -67,16 +67,18 @@ constexpr int kDgChunk = 64;  // slot columns per tile
 constexpr int kDgAlign = 16;  // segment starts and the MMA's N granularity
 constexpr int kDgMaxLocal = 1024;
 constexpr int kDgMaxSlots = 4096;
-constexpr int kDgMaxKs = 128;  // MXFP4 scale bytes per weight row (K <= 4096)
+constexpr int kDgMaxKs = 96;  // MXFP4 scale bytes per weight row (K <= 3072)
+constexpr int kEpiStride = 257;  // floats per staged slot row: 128 gate + 128 up + 1 (bank spread)
 constexpr int kDgBK = 128;
 
-// Stage layout (bytes): two 128 x 128 A blocks (gate, up), two 64 x 128 B
-// terms (hi, lo), the tcgen05.cp sources of the A and B scales, and the B
-// scale words as copied (row-major, 64 per term).
-constexpr uint32_t kStA0 = 0, kStA1 = 16384, kStB0 = 32768, kStB1 = 40960;
-constexpr uint32_t kStSfa = 49152;   // + 512 * block
-constexpr uint32_t kStSfb = 50176;   // + 512 * term
-constexpr uint32_t kStSfin = 51200;  // + 256 * term
+// Stage layout (bytes): the 128 x 128 A tile (activation terms of up to 64
+// slots), the 256 x 128 B tile (two 128-row weight blocks), the tcgen05.cp
+// sources of the A and B scales, and the A scale words as copied (128, in
+// split-row order).
+constexpr uint32_t kStA = 0, kStB = 16384;
+constexpr uint32_t kStSfa = 49152;
+constexpr uint32_t kStSfb = 49664;   // + 512 * block
+constexpr uint32_t kStSfin = 50688;
 constexpr uint32_t kStBytes = 52224;  // 51 KB, keeps every stage 1024-byte aligned
 
 template <bool kFp4>
@@ -84,9 +86,10 @@ struct DgSmem {
   static constexpr int kStages = kFp4 ? 3 : 4;
   static constexpr uint32_t kTsf = kStages * kStBytes;                        // 2 x 256 rows x Ks (MXFP4)
   static constexpr uint32_t kTsfBytes = kFp4 ? 256u * kDgMaxKs : 0u;
-  static constexpr uint32_t kPrefix = kTsf + 2 * kTsfBytes;                   // tile prefix [n_local + 1]
+  static constexpr uint32_t kEpi = kTsf + 2 * kTsfBytes;                      // GLU staging [16][257] fp32
+  static constexpr uint32_t kPrefix = kEpi + 16 * kEpiStride * 4 + 16;         // tile prefix [n_local + 1]
   static constexpr uint32_t kBar = kPrefix + (kDgMaxLocal + 1) * 4 + 4;       // 8-byte aligned
-  static constexpr uint32_t kNumBars = 3 * kStages + 9;
+  static constexpr uint32_t kNumBars = 3 * kStages + 7;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kScan = kAbort + 4;                               // [32] scan scratch
@@ -97,6 +100,11 @@ struct DgSmem {
 };
 
 __host__ __device__ constexpr int align16i(int v) { return (v + kDgAlign - 1) / kDgAlign * kDgAlign; }
+
+// Split row of term h (0 hi, 1 lo) of segment row r: blocks of 16 segment rows
+// become 16 hi rows followed by 16 lo rows, so that in the MMA's accumulator
+// the two terms of a slot sit in lanes j and j + 16 of one warp.
+__host__ __device__ __forceinline__ int split_row(int r, int h) { return 32 * (r >> 4) + 16 * h + (r & 15); }
 
 // Exclusive prefix over v(0..n-1) by the whole block (n <= 4 * blockDim.x):
 // out[e] = v(0) + ... + v(e-1), out[n] = the total. Ends with a barrier.
@@ -125,17 +133,33 @@ __device__ void block_exclusive_scan(int n, F v, int32_t* out, int32_t* tmp) {
   __syncthreads();
 }
 
-// Two-term split of one group of 32 values, one per lane (warp-collective):
-// codes of the hi and lo terms of this lane's value and the group's two scale
-// bytes.
-__device__ __forceinline__ void split_group(float v, uint32_t& ch, uint32_t& cl, uint32_t& sh, uint32_t& sl) {
-  const float a = __uint_as_float(__reduce_max_sync(kAll, __float_as_uint(fabsf(v))));
-  sh = group_scale_byte(a);
-  ch = e4m3x2_satfinite(__fmul_rn(v, pow2_f32(127 - (int)sh)), 0.0f) & 0xFFu;
-  const float r = __fsub_rn(v, __fmul_rn(e4m3x2_to_f32x2(ch).x, pow2_f32((int)sh - 127)));
-  const float ar = __uint_as_float(__reduce_max_sync(kAll, __float_as_uint(fabsf(r))));
-  sl = group_scale_byte(ar);
-  cl = e4m3x2_satfinite(__fmul_rn(r, pow2_f32(127 - (int)sl)), 0.0f) & 0xFFu;
+// Two-term split of four values of one group held by a lane, the group's 32
+// values spread over 8 consecutive lanes (collective over the warp; each
+// 8-lane group reduces its own maximum): the four hi and lo codes packed as
+// bytes, and the group's scale bytes.
+__device__ __forceinline__ void split_quad(const float (&v)[4], uint32_t& hq, uint32_t& lq, uint32_t& sh,
+                                           uint32_t& sl) {
+  float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kAll, m, o));
+  sh = group_scale_byte(m);
+  const float up_h = pow2_f32(127 - (int)sh), down_h = pow2_f32((int)sh - 127);
+  const uint32_t h01 = e4m3x2_satfinite(__fmul_rn(v[0], up_h), __fmul_rn(v[1], up_h));
+  const uint32_t h23 = e4m3x2_satfinite(__fmul_rn(v[2], up_h), __fmul_rn(v[3], up_h));
+  const float2 d01 = e4m3x2_to_f32x2(h01), d23 = e4m3x2_to_f32x2(h23);
+  float r[4];
+  r[0] = __fsub_rn(v[0], __fmul_rn(d01.x, down_h));
+  r[1] = __fsub_rn(v[1], __fmul_rn(d01.y, down_h));
+  r[2] = __fsub_rn(v[2], __fmul_rn(d23.x, down_h));
+  r[3] = __fsub_rn(v[3], __fmul_rn(d23.y, down_h));
+  float mr = fmaxf(fmaxf(fabsf(r[0]), fabsf(r[1])), fmaxf(fabsf(r[2]), fabsf(r[3])));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) mr = fmaxf(mr, __shfl_xor_sync(kAll, mr, o));
+  sl = group_scale_byte(mr);
+  const float up_l = pow2_f32(127 - (int)sl);
+  hq = (h01 & 0xFFFFu) | (h23 << 16);
+  lq = (e4m3x2_satfinite(__fmul_rn(r[0], up_l), __fmul_rn(r[1], up_l)) & 0xFFFFu) |
+       (e4m3x2_satfinite(__fmul_rn(r[2], up_l), __fmul_rn(r[3], up_l)) << 16);
 }
 
 struct DsArgs {
@@ -146,16 +170,18 @@ struct DsArgs {
   int32_t* cnt;       // [n_local]
   int32_t* seg;       // [n_local]
   int32_t* row_slot;  // [R]
-  uint8_t* xs;        // [2][R][H]
-  uint32_t* xsf;      // [2][ceil(H/128)][R]
+  uint8_t* xs;        // [2R][H] split rows
+  uint32_t* xsf;      // [ceil(H/128)][2R]
   int R;
 };
 
 // Segments and the split of x. Every CTA derives the same counts, segment
 // starts and per-slot ranks from topk_ids (the rank of a slot is the number
 // of earlier slots with the same expert, so the order is deterministic); CTA
-// 0 writes the counts, the starts and the padding entries of row_slot; each
-// warp then takes whole slots: their row_slot entry and the split x row.
+// 0 writes the counts, the starts and the padding entries of row_slot. Work
+// items are (slot, 128-element block): a warp loads the block (8 bytes per
+// lane; lanes 8b..8b+7 hold group b), splits it and writes 128 hi and 128 lo
+// codes and the block's two scale words.
 __global__ void __launch_bounds__(256) decode_split_kernel(const __grid_constant__ DsArgs a) {
   __shared__ int32_t cnt_s[kDgMaxLocal];
   __shared__ int32_t seg_s[kDgMaxLocal + 1];
@@ -181,34 +207,40 @@ __global__ void __launch_bounds__(256) decode_split_kernel(const __grid_constant
     }
     for (int r = seg_s[a.n_local] + (int)threadIdx.x; r < a.R; r += blockDim.x) a.row_slot[r] = -1;
   }
-  const int H = a.H, G = H / 32, W = (H + kDgBK - 1) / kDgBK;
-  for (int s = blockIdx.x * 8 + warp; s < S; s += gridDim.x * 8) {
+  const int H = a.H, W = (H + kDgBK - 1) / kDgBK;
+  const long items = (long)S * W;
+  for (long it = (long)blockIdx.x * 8 + warp; it < items; it += (long)gridDim.x * 8) {
+    const int s = (int)(it / W), w = (int)(it % W);
     const int lid = lid_s[s];
     if (lid < 0) continue;  // warp-uniform
+    const int col = kDgBK * w + 4 * lane;  // first of this lane's four elements
+    const bool in = col < H;               // H % 32 == 0: whole groups in or out
+    uint2 p = make_uint2(0u, 0u);
+    if (in) p = __ldg(reinterpret_cast<const uint2*>(a.x + (size_t)(s / a.k) * H + col));
     int c = 0;
     for (int s2 = lane; s2 < s; s2 += 32) c += (lid_s[s2] == lid);
-    c = __reduce_add_sync(kAll, c);
-    const int row = seg_s[lid] + c;
-    if (lane == 0) a.row_slot[row] = s;
-    const uint16_t* src = a.x + (size_t)(s / a.k) * H;
-    uint8_t* hrow = a.xs + (size_t)row * H;
-    uint8_t* lrow = a.xs + ((size_t)a.R + row) * H;
-    for (int w = 0; w < W; ++w) {
-      uint32_t wh = 0x7F7F7F7Fu, wl = 0x7F7F7F7Fu;  // groups past H keep unit scales
-      for (int b = 0; b < 4; ++b) {
-        const int g = 4 * w + b;
-        if (g >= G) break;
-        uint32_t ch, cl, sh, sl;
-        split_group(bf16_to_f32(src[32 * g + lane]), ch, cl, sh, sl);
-        hrow[32 * g + lane] = (uint8_t)ch;
-        lrow[32 * g + lane] = (uint8_t)cl;
-        wh = (wh & ~(0xFFu << (8 * b))) | (sh << (8 * b));
-        wl = (wl & ~(0xFFu << (8 * b))) | (sl << (8 * b));
-      }
-      if (lane == 0) {
-        a.xsf[(size_t)w * a.R + row] = wh;
-        a.xsf[((size_t)W + w) * a.R + row] = wl;
-      }
+    const int row = seg_s[lid] + __reduce_add_sync(kAll, c);
+    if (w == 0 && lane == 0) a.row_slot[row] = s;
+    const float v[4] = {bf16_lo(p.x), bf16_hi(p.x), bf16_lo(p.y), bf16_hi(p.y)};
+    uint32_t hq, lq, sh, sl;
+    split_quad(v, hq, lq, sh, sl);
+    const int rh = split_row(row, 0), rl = split_row(row, 1);
+    if (in) {
+      *reinterpret_cast<uint32_t*>(a.xs + (size_t)rh * H + col) = hq;
+      *reinterpret_cast<uint32_t*>(a.xs + (size_t)rl * H + col) = lq;
+    }
+    // scale words: byte b from lane 8b; groups past H keep unit scales
+    uint32_t wh = 0, wl = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t bh = __shfl_sync(kAll, in ? sh : 0x7Fu, 8 * b);
+      const uint32_t bl = __shfl_sync(kAll, in ? sl : 0x7Fu, 8 * b);
+      wh |= bh << (8 * b);
+      wl |= bl << (8 * b);
+    }
+    if (lane == 0) {
+      a.xsf[(size_t)w * 2 * a.R + rh] = wh;
+      a.xsf[(size_t)w * 2 * a.R + rl] = wl;
     }
   }
 }
@@ -218,7 +250,7 @@ struct DgArgs {
   const int32_t* seg;       // [n_local] first segment row of the expert
   const int32_t* row_slot;  // [R] slot t*k+j of each segment row, -1 for padding
   int n_local, R;
-  const uint32_t* bsf;  // [2][KC][R] scale words of the B terms
+  const uint32_t* asf;  // [KC][2R] scale words of the activation terms (split rows)
   const uint8_t* wsf;   // MXFP4: [n_local][rows][K/32]
   const float* wscale;  // FP8: [n_local]
   const uint16_t* bias;  // [n_local][rows]
@@ -227,25 +259,27 @@ struct DgArgs {
   float alpha, beta, limit;
   uint16_t* y;        // [T*k][rows]
   uint16_t* act;      // GLU: [T*k][M]
-  uint8_t* a_split;   // GLU: [2][R][M] e4m3 terms of act
-  uint32_t* a_sf;     // GLU: [2][ceil(M/128)][R]
+  uint8_t* a_split;   // GLU: [2R][M] e4m3 terms of act (split rows)
+  uint32_t* a_sf;     // GLU: [ceil(M/128)][2R]
   uint32_t* err;
 };
 
-// Instruction descriptor: A format e2m1 (5) or e4m3 (0), B e4m3, K-major, N
-// >> 3 at bit 17, UE8M0 scales (bit 23), M = 128 (M >> 4 at bit 24); the
-// scale-factor ids (B at bit 4, A at bit 29) are or-ed in per K32 step.
-__device__ __forceinline__ uint32_t dg_idesc(bool a_fp4, int n) {
-  return ((a_fp4 ? 5u : 0u) << 7) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24);
+// Instruction descriptor: A (activation terms) e4m3, B (weights) e2m1 (5) or
+// e4m3 (0), both K-major, N = 256 (N >> 3 at bit 17), UE8M0 scales (bit 23),
+// M = 128 (M >> 4 at bit 24); the scale-factor ids (B at bit 4, A at bit 29)
+// are or-ed in per K32 step.
+__host__ __device__ constexpr uint32_t dg_idesc(bool b_fp4) {
+  return ((b_fp4 ? 5u : 0u) << 10) | ((uint32_t)(256 >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24);
 }
 
 template <bool kFp4, bool kGlu>
 __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                                                                     const __grid_constant__ CUtensorMap tmWt,
-                                                                    const __grid_constant__ CUtensorMap tmB,
+                                                                    const __grid_constant__ CUtensorMap tmA,
                                                                     const __grid_constant__ DgArgs a) {
   using L = DgSmem<kFp4>;
   constexpr int S = L::kStages;
+  constexpr int RT = kGlu ? 128 : 256;  // output rows per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -259,9 +293,9 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
   auto sfin_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
   auto tsf_full = [&](int b) { return bar0 + 8u * (3 * S + b); };
   auto tsf_empty = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
-  auto acc_full = [&](int b) { return bar0 + 8u * (3 * S + 4 + b); };
-  auto acc_empty = [&](int b) { return bar0 + 8u * (3 * S + 6 + b); };
-  const uint32_t done_bar = bar0 + 8u * (3 * S + 8);
+  const uint32_t acc_full = bar0 + 8u * (3 * S + 4);
+  const uint32_t acc_empty = bar0 + 8u * (3 * S + 5);
+  const uint32_t done_bar = bar0 + 8u * (3 * S + 6);
   auto stage = [&](int s) { return smem + (size_t)s * kStBytes; };
 
   pdl_launch_dependents();
@@ -269,14 +303,14 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 2);   // producer's expect_tx arrive + transposer's arrive
       mbar_init(empty_bar(s), 1);  // tcgen05.commit
-      mbar_init(sfin_bar(s), 1);   // producer's expect_tx arrive for the B scale words
+      mbar_init(sfin_bar(s), 1);   // producer's expect_tx arrive for the activation scale words
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tsf_full(b), 1);
       mbar_init(tsf_empty(b), 1);
-      mbar_init(acc_full(b), 1);
-      mbar_init(acc_empty(b), 4);  // one arrive per epilogue warp
     }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kGlu ? 1 : 4);  // GLU: the warp that reads last; else one arrive per epilogue warp
     mbar_init(done_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -288,10 +322,10 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // The segments, the B terms and (second GEMM) the act terms come from the
+  // The segments, the activation terms and their scales come from the
   // preceding kernels of the stream.
   pdl_wait();
-  const int nmb = (a.M + 127) / 128;
+  const int nmb = (a.M + RT - 1) / RT;
   block_exclusive_scan(a.n_local, [&](int e) { return (a.cnt[e] + kDgChunk - 1) / kDgChunk * nmb; }, P,
                        reinterpret_cast<int32_t*>(smem + L::kScan));
   tc_fence_before();
@@ -301,11 +335,13 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
   const int total = P[a.n_local];
   const int KC = (a.K + kDgBK - 1) / kDgBK;
   const int Ks = a.K / 32;
+  const int R2 = 2 * a.R;
   // A K that is not a multiple of 128 ends with a block over [K - 128, K)
   // (e2m1 tensor maps take inner extents in multiples of 128 only; the block
   // stays inside each row), of which the MMA takes the K32 steps past the
-  // previous block: k4 >= skip. Its scale bytes: A word built from groups
-  // K/32 - 4 + k4 (id k4); B word kc holds groups 4kc.. (id k4 - skip).
+  // previous block: k4 >= skip. Its scale bytes: weight word built from
+  // groups K/32 - 4 + k4 (id k4); activation word kc holds groups 4kc..
+  // (id k4 - skip).
   const int skip = (a.K % kDgBK) ? (kDgBK - a.K % kDgBK) / 32 : 0;
   auto kx = [&](int kc) { return (skip && kc == KC - 1) ? a.K - kDgBK : kc * kDgBK; };
   // Tile t: expert e (the last with P[e] <= t), row block mb, first segment
@@ -331,7 +367,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
       // -------------------------------------------------------- producer
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
       if (kFp4 && skip) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmWt)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
       int s = 0;
       uint32_t ph = 0;
       int issued[S];
@@ -342,19 +378,19 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
         int e, mb, r0, live;
         tile_info(tile, e, mb, r0, live);
         const int n = align16i(live);
-        const int m0 = mb * 128;
+        const int m0 = mb * RT;
         if (kFp4) {
           const int tb = ti & 1;
           if (!(ok = wait_phase(tsf_empty(tb), ((ti >> 1) & 1) ^ 1u, abort_flag, a.err))) break;
           const uint32_t dst = sbase + L::kTsf + tb * L::kTsfBytes;
-          const uint32_t vg = (uint32_t)min(128, a.M - m0);
           const uint8_t* wexp = a.wsf + (size_t)e * a.rows * Ks;
           if (kGlu && !a.interleaved) {
+            const uint32_t vg = (uint32_t)min(128, a.M - m0);
             mbar_arrive_expect_tx(tsf_full(tb), 2u * vg * Ks);
             bulk_load(dst, wexp + (size_t)m0 * Ks, vg * Ks, tsf_full(tb));
             bulk_load(dst + 128u * Ks, wexp + (size_t)(a.M + m0) * Ks, vg * Ks, tsf_full(tb));
           } else {
-            const uint32_t rows = kGlu ? 2u * vg : vg;
+            const uint32_t rows = kGlu ? 2u * (uint32_t)min(128, a.M - m0) : (uint32_t)min(256, a.M - m0);
             mbar_arrive_expect_tx(tsf_full(tb), rows * Ks);
             bulk_load(dst, wexp + (size_t)(kGlu ? 2 * m0 : m0) * Ks, rows * Ks, tsf_full(tb));
           }
@@ -363,24 +399,24 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
           if (!(ok = wait_phase(empty_bar(s), ph ^ 1u, abort_flag, a.err))) break;
           const uint32_t st = sbase + (uint32_t)s * kStBytes;
           mbar_arrive_expect_tx(sfin_bar(s), 2u * n * 4u);
-          bulk_load(st + kStSfin, a.bsf + (size_t)kc * a.R + r0, n * 4u, sfin_bar(s));
-          bulk_load(st + kStSfin + 256u, a.bsf + ((size_t)KC + kc) * a.R + r0, n * 4u, sfin_bar(s));
+          bulk_load(st + kStSfin, a.asf + (size_t)kc * R2 + 2 * r0, 2u * n * 4u, sfin_bar(s));
           constexpr uint32_t kWBox = kFp4 ? 8192u : 16384u;  // packed global bytes of a 128 x 128 box
-          mbar_arrive_expect_tx(full_bar(s), (kGlu ? 2u : 1u) * kWBox + 2u * n * 128u);
+          mbar_arrive_expect_tx(full_bar(s), 2u * kWBox + 2u * n * 128u);
+          for (int j = 0; j < n / 16; ++j)
+            tma_load_2d(st + kStA + 4096u * j, &tmA, kx(kc), 2 * r0 + 32 * j, full_bar(s));
           // e2m1 tail block: its own map based at element K - 128
           const bool tail = kFp4 && skip && kc == KC - 1;
           const CUtensorMap* wm = tail ? &tmWt : &tmW;
-          const int xa = tail ? 0 : kx(kc);
+          const int xw = tail ? 0 : kx(kc);
           if (kGlu && a.interleaved) {
-            tma_load_4d(st + kStA0, wm, xa, 0, m0, e, full_bar(s));
-            tma_load_4d(st + kStA1, wm, xa, 1, m0, e, full_bar(s));
+            tma_load_4d(st + kStB, wm, xw, 0, m0, e, full_bar(s));
+            tma_load_4d(st + kStB + 16384u, wm, xw, 1, m0, e, full_bar(s));
+          } else if (kGlu) {
+            tma_load_4d(st + kStB, wm, xw, m0, 0, e, full_bar(s));
+            tma_load_4d(st + kStB + 16384u, wm, xw, m0, 1, e, full_bar(s));
           } else {
-            tma_load_4d(st + kStA0, wm, xa, m0, 0, e, full_bar(s));
-            if (kGlu) tma_load_4d(st + kStA1, wm, xa, m0, 1, e, full_bar(s));
-          }
-          for (int j = 0; j < n / 16; ++j) {
-            tma_load_2d(st + kStB0 + 2048u * j, &tmB, kx(kc), r0 + 16 * j, full_bar(s));
-            tma_load_2d(st + kStB1 + 2048u * j, &tmB, kx(kc), a.R + r0 + 16 * j, full_bar(s));
+            tma_load_4d(st + kStB, wm, xw, m0, 0, e, full_bar(s));
+            tma_load_4d(st + kStB + 16384u, wm, xw, m0 + 128, 0, e, full_bar(s));
           }
           issued[s] = (int)ph;
           if (++s == S) { s = 0; ph ^= 1u; }
@@ -403,41 +439,29 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
       bool ok = true;
       int ti = 0;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++ti) {
-        int e, mb, r0, live;
-        tile_info(tile, e, mb, r0, live);
-        const int n = align16i(live);
-        const int b = ti & 1;
-        if (!(ok = wait_phase(acc_empty(b), ((ti >> 1) & 1) ^ 1u, abort_flag, a.err))) break;
+        if (!(ok = wait_phase(acc_empty, (ti & 1) ^ 1u, abort_flag, a.err))) break;
         tc_fence_after();
-        const uint32_t dg = tmem + 128u * b, du = dg + 64u;
-        const uint32_t ibase = dg_idesc(kFp4, n);
         for (int kc = 0; kc < KC; ++kc) {
           if (!(ok = wait_phase(full_bar(s), ph, abort_flag, a.err))) break;
           tc_fence_after();
           const uint32_t st = sbase + (uint32_t)s * kStBytes;
-          const uint32_t tsf = tmem + 256u + 32u * s;  // A gate, A up, B hi, B lo: 4 columns each
+          const uint32_t tsf = tmem + 256u + 16u * s;  // A: 4 columns, B: 8 columns
           tc_cp_sf(tsf, desc_sf(st + kStSfa));
-          if (kGlu) tc_cp_sf(tsf + 4u, desc_sf(st + kStSfa + 512u));
-          tc_cp_sf(tsf + 8u, desc_sf(st + kStSfb));
-          tc_cp_sf(tsf + 12u, desc_sf(st + kStSfb + 512u));
+          tc_cp_sf(tsf + 4u, desc_sf(st + kStSfb));
+          tc_cp_sf(tsf + 8u, desc_sf(st + kStSfb + 512u));
           const int k4_0 = (kc == KC - 1) ? skip : 0;
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
             if (k4 < k4_0) continue;
-            const uint32_t idesc = ibase | ((uint32_t)(k4 - k4_0) << 4) | ((uint32_t)k4 << 29);
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-              const uint64_t db = desc_sw128(st + (p ? kStB1 : kStB0) + 32u * k4);
-              const uint32_t acc = (kc | (k4 - k4_0) | p) != 0;
-              tc_mma(dg, desc_sw128(st + kStA0 + 32u * k4), db, idesc, tsf, tsf + 8u + 4u * p, acc);
-              if (kGlu) tc_mma(du, desc_sw128(st + kStA1 + 32u * k4), db, idesc, tsf + 4u, tsf + 8u + 4u * p, acc);
-            }
+            const uint32_t idesc = dg_idesc(kFp4) | ((uint32_t)k4 << 4) | ((uint32_t)(k4 - k4_0) << 29);
+            tc_mma(tmem, desc_sw128(st + kStA + 32u * k4), desc_sw128(st + kStB + 32u * k4), idesc, tsf, tsf + 4u,
+                   (kc | (k4 - k4_0)) != 0);
           }
           tc_commit(empty_bar(s));
           if (++s == S) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(acc_full(b));
+        tc_commit(acc_full);
       }
       tc_commit(done_bar);
       wait_phase(done_bar, 0, abort_flag, a.err, false);
@@ -454,42 +478,42 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++ti) {
       int e, mb, r0, live;
       tile_info(tile, e, mb, r0, live);
-      const int n = align16i(live);
-      const int m0 = mb * 128;
+      const int n2 = 2 * align16i(live);  // activation rows of the tile
+      const int m0 = mb * RT;
       const int tb = ti & 1;
       if (kFp4 && !(ok = wait_phase(tsf_full(tb), (ti >> 1) & 1, abort_flag, a.err))) break;
       const uint8_t* tsf = smem + L::kTsf + tb * L::kTsfBytes;
       for (int kc = 0; kc < KC; ++kc) {
         if (!(ok = wait_phase(sfin_bar(s), ph, abort_flag, a.err))) break;
         uint8_t* st = stage(s);
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-          const uint32_t* in = reinterpret_cast<const uint32_t*>(st + kStSfin + 256 * p);
+        {
+          const uint32_t* in = reinterpret_cast<const uint32_t*>(st + kStSfin);
           uint4 v;
-          v.x = (lane < n) ? in[lane] : 0x7F7F7F7Fu;
-          v.y = (32 + lane < n) ? in[32 + lane] : 0x7F7F7F7Fu;
-          v.z = 0x7F7F7F7Fu;
-          v.w = 0x7F7F7F7Fu;
-          *reinterpret_cast<uint4*>(st + kStSfb + 512 * p + 16 * lane) = v;
+          v.x = (lane < n2) ? in[lane] : 0x7F7F7F7Fu;
+          v.y = (32 + lane < n2) ? in[32 + lane] : 0x7F7F7F7Fu;
+          v.z = (64 + lane < n2) ? in[64 + lane] : 0x7F7F7F7Fu;
+          v.w = (96 + lane < n2) ? in[96 + lane] : 0x7F7F7F7Fu;
+          *reinterpret_cast<uint4*>(st + kStSfa + 16 * lane) = v;
         }
 #pragma unroll
-        for (int blk = 0; blk < (kGlu ? 2 : 1); ++blk) {
+        for (int blk = 0; blk < 2; ++blk) {
           uint32_t w[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             w[j] = 0x7F7F7F7Fu;
-            const int r = 32 * j + lane;
-            if (kFp4 && m0 + r < a.M) {
-              const int raw = kGlu ? (a.interleaved ? 2 * r + blk : 128 * blk + r) : r;
-              const uint8_t* src = tsf + (size_t)raw * Ks;
-              uint32_t word = 0;
-              const int g0 = kx(kc) / 32;
-#pragma unroll
-              for (int bb = 0; bb < 4; ++bb) word |= (uint32_t)src[g0 + bb] << (8 * bb);
-              w[j] = word;
+            const int r = 32 * j + lane;  // row within the 128-row block
+            if (kFp4) {
+              // output row of this weight row, and its row in the tile's scale copy
+              const int orow = kGlu ? m0 + r : m0 + 128 * blk + r;
+              const int raw = kGlu ? (a.interleaved ? 2 * r + blk : 128 * blk + r) : 128 * blk + r;
+              if (orow < a.M) {
+                const uint8_t* src = tsf + (size_t)raw * Ks + kx(kc) / 32;
+                w[j] = (uint32_t)src[0] | ((uint32_t)src[1] << 8) | ((uint32_t)src[2] << 16) |
+                       ((uint32_t)src[3] << 24);
+              }
             }
           }
-          *reinterpret_cast<uint4*>(st + kStSfa + 512 * blk + 16 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(st + kStSfb + 512 * blk + 16 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -502,74 +526,129 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------- epilogue
+    // Warp q holds accumulator lanes 32q..32q+31: lanes j < 16 the hi term
+    // and lanes j + 16 the lo term of chunk column 16q + j; shfl_xor 16 sums
+    // them.
     const int q = warp & 3;
-    const int KC2 = (a.M + kDgBK - 1) / kDgBK;  // scale words per act row (GLU)
     int ti = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ti) {
       int e, mb, r0, live;
       tile_info(tile, e, mb, r0, live);
-      const int b = ti & 1;
-      const int i = mb * 128 + 32 * q + lane;  // output row of this thread
-      const bool valid = i < a.M;
-      const int slot_lo = a.row_slot[r0 + lane];
-      const int slot_hi = (live > 32) ? a.row_slot[r0 + 32 + lane] : -1;
+      const int m0 = mb * RT;
       const float ws = kFp4 ? 1.0f : __ldg(a.wscale + e);
       const uint16_t* bexp = a.bias + (size_t)e * a.rows;
-      const int grow = kGlu ? (a.interleaved ? 2 * i : i) : i;
-      const int urow = a.interleaved ? 2 * i + 1 : a.M + i;
-      const float bg = valid ? bf16_to_f32(bexp[grow]) : 0.0f;
-      const float bu = (kGlu && valid) ? bf16_to_f32(bexp[urow]) : 0.0f;
-      if (!wait_phase(acc_full(b), (ti >> 1) & 1, abort_flag, a.err)) break;
+      const int nchunk = min(RT, a.M - m0) / 32;  // 32-row chunks with output rows (M % 32 == 0)
+      if (!wait_phase(acc_full, ti & 1, abort_flag, a.err)) break;
       tc_fence_after();
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        if (32 * h >= live) break;
-        uint32_t g[32], u[32];
-        const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + 128u * b + 32u * h;
-        tmem_ld_32cols(tbase, g);
-        if (kGlu) tmem_ld_32cols(tbase + 64u, u);
-        tmem_ld_wait();
-        if (h == 1 || live <= 32) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty(b));
-        }
-        const int slot_src = h ? slot_hi : slot_lo;
+      if (!kGlu) {
+        // y2 rows: each low lane finishes its slot's row, 32 outputs per chunk
+        const int c = 16 * q + (lane & 15);
+        const bool mine = lane < 16 && c < live;
+        const int slot = mine ? a.row_slot[r0 + c] : -1;
+        const bool any = 16 * q < live;
+        for (int ch = 0; any && ch < nchunk; ++ch) {
+          uint32_t g[32];
+          tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + 32u * ch, g);
+          tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if (32 * h + c >= live) break;  // warp-uniform
-          const int slot = __shfl_sync(kAll, slot_src, c);
-          const size_t yrow = (size_t)slot * a.rows;
-          if (kGlu) {
-            const uint32_t yg = f32_to_bf16_bits(fmaf(__uint_as_float(g[c]), ws, bg));
-            const uint32_t yu = f32_to_bf16_bits(fmaf(__uint_as_float(u[c]), ws, bu));
-            const uint32_t av =
-                f32_to_bf16_bits(glu_value(bf16_to_f32((uint16_t)yg), bf16_to_f32((uint16_t)yu), a.alpha, a.beta,
-                                           a.limit));
-            if (valid) {
-              if (a.interleaved) {
-                *reinterpret_cast<uint32_t*>(a.y + yrow + grow) = yg | (yu << 16);
-              } else {
-                a.y[yrow + grow] = (uint16_t)yg;
-                a.y[yrow + urow] = (uint16_t)yu;
-              }
-              a.act[(size_t)slot * a.M + i] = (uint16_t)av;
+          for (int j = 0; j < 32; ++j)
+            g[j] = __float_as_uint(__uint_as_float(g[j]) + __shfl_xor_sync(kAll, __uint_as_float(g[j]), 16));
+          if (!mine) continue;
+          const int r_out = m0 + 32 * ch;
+          const uint4* b4 = reinterpret_cast<const uint4*>(bexp + r_out);
+          uint4* d = reinterpret_cast<uint4*>(a.y + (size_t)slot * a.rows + r_out);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 bv = __ldg(b4 + v);
+            const uint32_t* bw = &bv.x;
+            uint32_t o[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int j = 8 * v + 2 * t;
+              o[t] = pack_bf16x2(fmaf(__uint_as_float(g[j]), ws, bf16_lo(bw[t])),
+                                 fmaf(__uint_as_float(g[j + 1]), ws, bf16_hi(bw[t])));
             }
-            uint32_t ch, cl, sh, sl;
-            split_group(valid ? bf16_to_f32((uint16_t)av) : 0.0f, ch, cl, sh, sl);
-            const int row = r0 + 32 * h + c;
-            if (valid) {
-              a.a_split[(size_t)row * a.M + i] = (uint8_t)ch;
-              a.a_split[((size_t)a.R + row) * a.M + i] = (uint8_t)cl;
-            }
-            if (lane == 0) {
-              reinterpret_cast<uint8_t*>(a.a_sf + (size_t)mb * a.R + row)[q] = (uint8_t)sh;
-              reinterpret_cast<uint8_t*>(a.a_sf + ((size_t)KC2 + mb) * a.R + row)[q] = (uint8_t)sl;
-            }
-          } else if (valid) {
-            a.y[yrow + i] = (uint16_t)f32_to_bf16_bits(fmaf(__uint_as_float(g[c]), ws, bg));
+            d[v] = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+        continue;
+      }
+      // GLU: per pass, the warp holding 16 slots stages their summed gate/up
+      // rows in shared memory; then all four warps finish them, lanes over 32
+      // consecutive rows (coalesced stores; one warp reduction per group of
+      // 32 for the split of act). The accumulator is released after the last
+      // pass's reads.
+      float* buf = reinterpret_cast<float*>(smem + L::kEpi);
+      const int npass = (live + 15) / 16;
+      for (int p = 0; p < npass; ++p) {
+        if (q == p) {
+          for (int ch = 0; ch < nchunk; ++ch) {
+            uint32_t g[32], u[32];
+            const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + 32u * ch;
+            tmem_ld_32cols(tq, g);
+            tmem_ld_32cols(tq + 128u, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float gs = __uint_as_float(g[j]) + __shfl_xor_sync(kAll, __uint_as_float(g[j]), 16);
+              const float us = __uint_as_float(u[j]) + __shfl_xor_sync(kAll, __uint_as_float(u[j]), 16);
+              if (lane < 16) {
+                buf[lane * kEpiStride + 32 * ch + j] = gs;
+                buf[lane * kEpiStride + 128 + 32 * ch + j] = us;
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (p == npass - 1 && lane == 0) mbar_arrive(acc_empty);
+        }
+        named_barrier(1, 128);
+        const int np = min(16, live - 16 * p);
+        for (int sl = q; sl < np; sl += 4) {
+          const int col = 16 * p + sl;  // chunk column
+          const int slot = a.row_slot[r0 + col];
+          const int srow = r0 + col;
+          uint16_t* yrow = a.y + (size_t)slot * a.rows;
+          uint32_t wh = 0x7F7F7F7Fu, wl = 0x7F7F7F7Fu;
+          for (int ch = 0; ch < nchunk; ++ch) {
+            const int i = m0 + 32 * ch + lane;
+            const float gsum = buf[sl * kEpiStride + 32 * ch + lane];
+            const float usum = buf[sl * kEpiStride + 128 + 32 * ch + lane];
+            const int grow = a.interleaved ? 2 * i : i, urow = a.interleaved ? 2 * i + 1 : a.M + i;
+            const uint32_t yG = f32_to_bf16_bits(fmaf(gsum, ws, bf16_to_f32(bexp[grow])));
+            const uint32_t yU = f32_to_bf16_bits(fmaf(usum, ws, bf16_to_f32(bexp[urow])));
+            const uint32_t A = f32_to_bf16_bits(
+                glu_value(bf16_to_f32((uint16_t)yG), bf16_to_f32((uint16_t)yU), a.alpha, a.beta, a.limit));
+            if (a.interleaved) {
+              reinterpret_cast<uint32_t*>(yrow)[i] = yG | (yU << 16);
+            } else {
+              yrow[grow] = (uint16_t)yG;
+              yrow[urow] = (uint16_t)yU;
+            }
+            a.act[(size_t)slot * a.M + i] = (uint16_t)A;
+            // two-term split of the group of 32 act values held by the warp
+            const float v = bf16_to_f32((uint16_t)A);
+            const float am = __uint_as_float(__reduce_max_sync(kAll, __float_as_uint(fabsf(v))));
+            const uint32_t sh = group_scale_byte(am);
+            const uint32_t hc = e4m3x2_satfinite(__fmul_rn(v, pow2_f32(127 - (int)sh)), 0.0f) & 0xFFu;
+            const float r = __fsub_rn(v, __fmul_rn(e4m3x2_to_f32x2(hc).x, pow2_f32((int)sh - 127)));
+            const float ar = __uint_as_float(__reduce_max_sync(kAll, __float_as_uint(fabsf(r))));
+            const uint32_t sl2 = group_scale_byte(ar);
+            const uint32_t lc = e4m3x2_satfinite(__fmul_rn(r, pow2_f32(127 - (int)sl2)), 0.0f) & 0xFFu;
+            a.a_split[(size_t)split_row(srow, 0) * a.M + i] = (uint8_t)hc;
+            a.a_split[(size_t)split_row(srow, 1) * a.M + i] = (uint8_t)lc;
+            wh = (wh & ~(0xFFu << (8 * ch))) | (sh << (8 * ch));
+            wl = (wl & ~(0xFFu << (8 * ch))) | (sl2 << (8 * ch));
+          }
+          if (lane == 0) {
+            a.a_sf[(size_t)mb * R2 + split_row(srow, 0)] = wh;
+            a.a_sf[(size_t)mb * R2 + split_row(srow, 1)] = wl;
+          }
+        }
+        named_barrier(1, 128);  // the staging buffer is free for the next pass
       }
     }
   }
@@ -676,9 +755,9 @@ int launch_decode_gemm(const moe_decode_args& a, EncodeTiledFn enc, int num_sms,
       !encode_weights(enc, &mW2t, a.w_d, fp4, n_local, H, I, H, false, false, fp4 && I % kDgBK ? I - kDgBK : 0,
                       fp4 && I % kDgBK ? kDgBK : ext2) ||
       !encode_2d(enc, &mB1, CU_TENSOR_MAP_DATA_TYPE_UINT8, xs, (uint64_t)a.H, 2 * (uint64_t)L.R, (uint64_t)a.H,
-                 kDgBK, 16) ||
+                 kDgBK, 32) ||
       !encode_2d(enc, &mB2, CU_TENSOR_MAP_DATA_TYPE_UINT8, as, (uint64_t)a.I, 2 * (uint64_t)L.R, (uint64_t)a.I,
-                 kDgBK, 16))
+                 kDgBK, 32))
     return MOE_ERR_INVALID_ARG;
 
   DsArgs ds{};
@@ -696,7 +775,8 @@ int launch_decode_gemm(const moe_decode_args& a, EncodeTiledFn enc, int num_sms,
   ds.xsf = xsf;
   ds.R = L.R;
   const int S = a.T * a.k;
-  const int gsplit = (int)lmax(1, lmin((S + 7) / 8, num_sms));
+  const long items = (long)S * ((a.H + kDgBK - 1) / kDgBK);  // one warp each
+  const int gsplit = (int)lmax(1, lmin((items + 7) / 8, 8L * num_sms));
   decode_split_kernel<<<gsplit, 256, 0, st>>>(ds);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -711,7 +791,7 @@ int launch_decode_gemm(const moe_decode_args& a, EncodeTiledFn enc, int num_sms,
   g.beta = a.glu_beta;
   g.limit = a.glu_limit;
   // GEMM 1 + GLU + split of act
-  g.bsf = xsf;
+  g.asf = xsf;
   g.wsf = a.w_gu_sf;
   g.wscale = a.w_gu_scale;
   g.bias = a.b_gu;
@@ -729,7 +809,7 @@ int launch_decode_gemm(const moe_decode_args& a, EncodeTiledFn enc, int num_sms,
                                           DgSmem<false>::kBytes, st, true, mW1, mW1t, mB1, g);
   if (ce != cudaSuccess) return MOE_ERR_CUDA;
   // GEMM 2
-  g.bsf = asf;
+  g.asf = asf;
   g.wsf = a.w_d_sf;
   g.wscale = a.w_d_scale;
   g.bias = a.b_d;
