@@ -583,7 +583,7 @@ def decode_microbench(ctx, B, synth, torch, np, hbm, n_layers=24, reps=5, fmts=N
                     B.moe_sparse_gemv_decode(ctx, x=x, topk_ids=ids, topk_w=w, expert_start=0, num_local_experts=E,
                                              wfmt=wfmt, w_gu=L["w_gu"], b_gu=L["b_gu"], w_d=L["w_d"], b_d=L["b_d"],
                                              y1=y1, act=act, y2=y2, out=out, T=T, H=H, I=I, k=k, workspace=ws,
-                                             **kw)
+                                             path=B.MOE_DECODE_TCGEN05 if tc5 else B.MOE_DECODE_AUTO, **kw)
             # decode steps are launch-bound on the host: capture the 24 layers once
             # in a CUDA graph (the layer calls only enqueue fixed grids) and replay
             run_layers()

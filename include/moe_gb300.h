@@ -93,6 +93,12 @@ typedef void* moe_stream_t; /* cudaStream_t */
 #define MOE_GLU_HALVES 0               /* [gate_0..gate_{I-1}, up_0..up_{I-1}] */
 #define MOE_GLU_INTERLEAVED 1          /* [gate_0, up_0, gate_1, up_1, ...] */
 
+/* decode paths (moe_decode_args.path) */
+#define MOE_DECODE_AUTO 0              /* by size and workspace, see moe_sparse_gemv_decode */
+#define MOE_DECODE_TCGEN05 1           /* block-scaled tcgen05 path (workspace required) */
+#define MOE_DECODE_MMA_SYNC 2          /* m16n8k16 path (T <= 8) */
+#define MOE_DECODE_GEMV 3              /* one GEMV block per (token, slot, 32 rows) */
+
 /* ------------------------------------------------------------- context
  * moe_ctx_create: binds `device`, reads its SM count, allocates the 4-byte
  *   device error word and the SiLU table (entry i = silu of the bf16 value
@@ -382,12 +388,16 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* args, moe_stream_t
  * with a workspace; w_gu, w_d, the MXFP4 scale arrays and the biases 16-byte
  * aligned, x and act 8-byte aligned. y1 / y2 / act of non-local slots are
  * never written.
- * Paths, each reading every selected local expert's weights once for all the
- * slots that chose it ([SD] §4 crossover removed):
- *   - workspace given (at least moe_decode_workspace_size() bytes, 256-byte
+ * Paths (args.path; AUTO takes the tcgen05 path when it applies and T >= 8
+ * for FP8 or T >= 4 for MXFP4 -- below that the mma.sync path is faster,
+ * when it applies --, else the mma.sync path, else the GEMV path; a forced
+ * path that does not apply is an invalid argument). The first two read every
+ * selected local expert's weights once for all the slots that chose it
+ * ([SD] §4 crossover removed):
+ *   - TCGEN05: workspace given (at least moe_decode_workspace_size() bytes, 256-byte
  *     aligned, owned by the caller, contents need not be initialised; not
  *     shared by calls in flight at the same time), T * k <= 4096,
- *     num_local_experts <= 1024, H, I >= 128, and for MXFP4 H, I <= 3072,
+ *     num_local_experts <= 1024, H, I >= 128, and for MXFP4 H, I <= 4096,
  *     H % 64 == I % 64 == 0 and w_gu, w_d 32-byte aligned, y1, act, y2
  *     16-byte aligned: the tcgen05
  *     block-scaled path. The slots are grouped by expert into 16-row
@@ -396,10 +406,10 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* args, moe_stream_t
  *     lo = e4m3((v - hi s_hi) / s_lo)), which reproduce every value within
  *     2^13 of its group's maximum exactly and the others to 2^-21 of that
  *     maximum; the weights enter the tensor cores in their stored format.
- *   - otherwise T <= 8 with H % 64 == 0 and I % 64 == 0: m16n8k16 f16 MMA on
- *     exactly converted weights against token columns scaled per token by a
- *     power of two;
- *   - otherwise one GEMV block per (token, slot, 32 rows). */
+ *   - MMA_SYNC: T <= 8 with H % 64 == 0 and I % 64 == 0: m16n8k16 f16 MMA
+ *     on exactly converted weights against token columns scaled per token by
+ *     a power of two;
+ *   - GEMV: one GEMV block per (token, slot, 32 rows), T <= 64. */
 typedef struct moe_decode_args {
     const uint16_t* x;
     const int32_t* topk_ids;
@@ -422,6 +432,7 @@ typedef struct moe_decode_args {
     int32_t T, H, I, k;
     void* workspace;        /* device scratch of the tcgen05 path, or NULL */
     size_t workspace_bytes;
+    int32_t path;           /* MOE_DECODE_* */
 } moe_decode_args;
 
 /* Bytes of the tcgen05 decode path's workspace for these sizes (0 when the

@@ -24,6 +24,10 @@ MOE_WFMT_FP8_PER_EXPERT = 0
 MOE_WFMT_MXFP4_G32 = 1
 MOE_GLU_HALVES = 0
 MOE_GLU_INTERLEAVED = 1
+MOE_DECODE_AUTO = 0
+MOE_DECODE_TCGEN05 = 1
+MOE_DECODE_MMA_SYNC = 2
+MOE_DECODE_GEMV = 3
 MOE_GEMM_W_E2M1 = 0
 MOE_GEMM_W_E4M3 = 1
 MOE_GEMM_W_GATEUP_BLOCK128 = 2
@@ -81,7 +85,7 @@ class moe_decode_args(ctypes.Structure):
                 ("glu_layout", _I32), ("glu_alpha", _F), ("glu_beta", _F), ("glu_limit", _F),
                 ("y1", _P), ("act", _P), ("y2", _P), ("out", _P),
                 ("T", _I32), ("H", _I32), ("I", _I32), ("k", _I32),
-                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("path", _I32)]
 
 
 _SIGS = {
@@ -257,15 +261,16 @@ def moe_ffn_forward(ctx, *, a_fp8, a_sf, expert_ends, w13, w13_sf, w2, w2_sf, ga
 def moe_sparse_gemv_decode(ctx, *, x, topk_ids, topk_w, expert_start, num_local_experts, wfmt, w_gu, b_gu, w_d,
                            b_d, y1, act, y2, out, T, H, I, k, w_gu_scale=None, w_gu_sf=None, w_d_scale=None,
                            w_d_sf=None, glu_layout=MOE_GLU_INTERLEAVED, glu_alpha=1.702, glu_beta=1.0,
-                           glu_limit=7.0, workspace=None, stream=None):
+                           glu_limit=7.0, workspace=None, path=None, stream=None):
     """workspace: a uint8 device tensor of at least moe_decode_workspace_size()
-    bytes selects the tcgen05 path (T <= 128); None keeps the mma.sync / GEMV
-    paths (T <= 64)."""
+    bytes enables the tcgen05 path (T <= 128); path: MOE_DECODE_* (default
+    AUTO: tcgen05 from T >= 8 (FP8) / T >= 4 (MXFP4) when it applies, else
+    mma.sync, else GEMV)."""
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     a = moe_decode_args(ptr(x), ptr(topk_ids), ptr(topk_w), expert_start, num_local_experts, wfmt,
                         ptr(w_gu), ptr(w_gu_scale), ptr(w_gu_sf), ptr(b_gu), ptr(w_d), ptr(w_d_scale), ptr(w_d_sf),
                         ptr(b_d), glu_layout, glu_alpha, glu_beta, glu_limit, ptr(y1), ptr(act), ptr(y2), ptr(out),
-                        T, H, I, k, ptr(workspace), ws_bytes)
+                        T, H, I, k, ptr(workspace), ws_bytes, MOE_DECODE_AUTO if path is None else path)
     _check("moe_sparse_gemv_decode", load().moe_sparse_gemv_decode(ctx.handle, ctypes.byref(a), cur_stream(stream)))
 
 

@@ -403,20 +403,28 @@ MOE_API int moe_sparse_gemv_decode(moe_ctx* ctx, const moe_decode_args* a, moe_s
         !al(a->act, 8))
       return MOE_ERR_INVALID_ARG;
   }
-  bool tc5 = false;
-  if (ws && a->T > 0) {
-    if (!al(a->workspace, 256)) return MOE_ERR_INVALID_ARG;
-    // e2m1 tensor maps want a 32-byte aligned base
-    tc5 = moe::decode_gemm_ok(a->T, a->k, a->H, a->I, a->num_local_experts, a->wfmt) &&
-          (a->wfmt != MOE_WFMT_MXFP4_G32 || (al(a->w_gu, 32) && al(a->w_d, 32))) && al(a->y1, 16) &&
-          al(a->act, 16) && al(a->y2, 16);
-    if (tc5 && a->workspace_bytes < moe::decode_ws_layout(a->T, a->k, a->H, a->I, a->num_local_experts).total)
-      return MOE_ERR_INVALID_ARG;
-    if (!tc5 && a->T > 64) return MOE_ERR_INVALID_ARG;
+  if (a->path < MOE_DECODE_AUTO || a->path > MOE_DECODE_GEMV) return MOE_ERR_INVALID_ARG;
+  if (ws && !al(a->workspace, 256)) return MOE_ERR_INVALID_ARG;
+  // tcgen05 path: sizes in range, e2m1 tensor maps want a 32-byte aligned base,
+  // 16-byte vector stores of y1 / act / y2, and a large enough workspace
+  const bool tc5 = ws && a->T > 0 &&
+                   moe::decode_gemm_ok(a->T, a->k, a->H, a->I, a->num_local_experts, a->wfmt) &&
+                   (a->wfmt != MOE_WFMT_MXFP4_G32 || (al(a->w_gu, 32) && al(a->w_d, 32))) && al(a->y1, 16) &&
+                   al(a->act, 16) && al(a->y2, 16) &&
+                   a->workspace_bytes >= moe::decode_ws_layout(a->T, a->k, a->H, a->I, a->num_local_experts).total;
+  const bool mma = a->T > 0 && moe::decode_mma_sync_ok(*a);
+  int path = a->path;
+  if (path == MOE_DECODE_AUTO) {
+    const int t_min = a->wfmt == MOE_WFMT_FP8_PER_EXPERT ? 8 : 4;  // measured crossover with the mma.sync path
+    path = (tc5 && (a->T >= t_min || !mma)) ? MOE_DECODE_TCGEN05 : mma ? MOE_DECODE_MMA_SYNC : MOE_DECODE_GEMV;
   }
+  if (a->T > 0 && ((path == MOE_DECODE_TCGEN05 && !tc5) || (path == MOE_DECODE_MMA_SYNC && !mma) ||
+                   (path == MOE_DECODE_GEMV && a->T > 64)))
+    return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
-  if (tc5) return moe::launch_decode_gemm(*a, ctx->encode, ctx->num_sms, ctx->d_err, S(stream));
-  return cuda_status(moe::launch_decode(*a, ctx->num_sms, ctx->d_err, S(stream)));
+  if (path == MOE_DECODE_TCGEN05 && a->T > 0)
+    return moe::launch_decode_gemm(*a, ctx->encode, ctx->num_sms, ctx->d_err, S(stream));
+  return cuda_status(moe::launch_decode(*a, path == MOE_DECODE_MMA_SYNC, ctx->num_sms, ctx->d_err, S(stream)));
 }
 
 }  // extern "C"

@@ -678,16 +678,21 @@ cudaError_t init_decode() {
                               (int)kTcSmemMax);
 }
 
-cudaError_t launch_decode(const moe_decode_args& a, int num_sms, uint32_t* err, cudaStream_t st) {
+bool decode_mma_sync_ok(const moe_decode_args& a) {
+  if (a.wfmt == MOE_WFMT_FP8_PER_EXPERT)
+    return tc_ok<MOE_WFMT_FP8_PER_EXPERT>(a.T, a.k, 2 * a.I, a.H) && tc_ok<MOE_WFMT_FP8_PER_EXPERT>(a.T, a.k, a.H, a.I);
+  return tc_ok<MOE_WFMT_MXFP4_G32>(a.T, a.k, 2 * a.I, a.H) && tc_ok<MOE_WFMT_MXFP4_G32>(a.T, a.k, a.H, a.I);
+}
+
+cudaError_t launch_decode(const moe_decode_args& a, bool allow_mma_sync, int num_sms, uint32_t* err,
+                          cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
   cudaError_t ce;
   const bool fp8 = a.wfmt == MOE_WFMT_FP8_PER_EXPERT;
-  if (fp8 && tc_ok<MOE_WFMT_FP8_PER_EXPERT>(a.T, a.k, 2 * a.I, a.H) &&
-      tc_ok<MOE_WFMT_FP8_PER_EXPERT>(a.T, a.k, a.H, a.I))
-    return launch_decode_tc<MOE_WFMT_FP8_PER_EXPERT>(a, a.w_gu_scale, nullptr, a.w_d_scale, nullptr, num_sms, err,
-                                                     st);
-  if (!fp8 && tc_ok<MOE_WFMT_MXFP4_G32>(a.T, a.k, 2 * a.I, a.H) && tc_ok<MOE_WFMT_MXFP4_G32>(a.T, a.k, a.H, a.I))
-    return launch_decode_tc<MOE_WFMT_MXFP4_G32>(a, nullptr, a.w_gu_sf, nullptr, a.w_d_sf, num_sms, err, st);
+  if (allow_mma_sync && decode_mma_sync_ok(a))
+    return fp8 ? launch_decode_tc<MOE_WFMT_FP8_PER_EXPERT>(a, a.w_gu_scale, nullptr, a.w_d_scale, nullptr, num_sms, err,
+                                                           st)
+               : launch_decode_tc<MOE_WFMT_MXFP4_G32>(a, nullptr, a.w_gu_sf, nullptr, a.w_d_sf, num_sms, err, st);
   // Otherwise four launches: GEMV, GLU, GEMV, weighted sum.
   ce = fp8 ? gemv<MOE_WFMT_FP8_PER_EXPERT>(a.x, 0, a, a.w_gu, a.w_gu_scale, nullptr, a.b_gu, 2 * a.I, a.H, a.y1, st)
            : gemv<MOE_WFMT_MXFP4_G32>(a.x, 0, a, a.w_gu, nullptr, a.w_gu_sf, a.b_gu, 2 * a.I, a.H, a.y1, st);

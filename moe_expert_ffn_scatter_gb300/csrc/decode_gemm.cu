@@ -63,41 +63,56 @@ namespace {
 
 constexpr unsigned kAll = 0xFFFFFFFFu;
 constexpr int kDgThreads = 256;
-constexpr int kDgChunk = 64;  // slot columns per tile
+constexpr int kDgChunk = 32;  // slots per tile (A tile: 64 rows of activation terms)
 constexpr int kDgAlign = 16;  // segment starts and the MMA's N granularity
 constexpr int kDgMaxLocal = 1024;
 constexpr int kDgMaxSlots = 4096;
-constexpr int kDgMaxKs = 96;  // MXFP4 scale bytes per weight row (K <= 3072)
+constexpr int kDgMaxKs = 128;  // MXFP4 scale bytes per weight row (K <= 4096)
 constexpr int kEpiStride = 257;  // floats per staged slot row: 128 gate + 128 up + 1 (bank spread)
+constexpr int kEpiSlots = 8;     // slots staged per GLU epilogue pass
+constexpr int kMaxStages = 6;
 constexpr int kDgBK = 128;
 
-// Stage layout (bytes): the 128 x 128 A tile (activation terms of up to 64
-// slots), the 256 x 128 B tile (two 128-row weight blocks), the tcgen05.cp
-// sources of the A and B scales, and the A scale words as copied (128, in
-// split-row order).
-constexpr uint32_t kStA = 0, kStB = 16384;
-constexpr uint32_t kStSfa = 49152;
-constexpr uint32_t kStSfb = 49664;   // + 512 * block
-constexpr uint32_t kStSfin = 50688;
-constexpr uint32_t kStBytes = 52224;  // 51 KB, keeps every stage 1024-byte aligned
+// Stage layout (bytes): the 64 x 128 A tile (activation terms of up to 32
+// slots; the MMA's M = 128 also reads the next 64 rows, whose accumulator
+// lanes are never used), the 256 x 128 B tile (two 128-row weight blocks), the
+// tcgen05.cp sources of the A and B scales, and the A scale words as copied
+// (64, in split-row order).
+constexpr uint32_t kStA = 0, kStB = 8192;
+constexpr uint32_t kStSfa = 40960;
+constexpr uint32_t kStSfb = 41472;   // + 512 * block
+constexpr uint32_t kStSfin = 42496;
+constexpr uint32_t kStBytes = 43008;  // 42 KB, keeps every stage 1024-byte aligned
+constexpr uint32_t kSmemMax = 232448;
 
-template <bool kFp4>
-struct DgSmem {
-  static constexpr int kStages = kFp4 ? 3 : 4;
-  static constexpr uint32_t kTsf = kStages * kStBytes;                        // 2 x 256 rows x Ks (MXFP4)
-  static constexpr uint32_t kTsfBytes = kFp4 ? 256u * kDgMaxKs : 0u;
-  static constexpr uint32_t kEpi = kTsf + 2 * kTsfBytes;                      // GLU staging [16][257] fp32
-  static constexpr uint32_t kPrefix = kEpi + 16 * kEpiStride * 4 + 16;         // tile prefix [n_local + 1]
-  static constexpr uint32_t kBar = kPrefix + (kDgMaxLocal + 1) * 4 + 4;       // 8-byte aligned
-  static constexpr uint32_t kNumBars = 3 * kStages + 7;
-  static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
-  static constexpr uint32_t kAbort = kTmemSlot + 4;
-  static constexpr uint32_t kScan = kAbort + 4;                               // [32] scan scratch
-  static constexpr uint32_t kUsed = kScan + 32 * 4;
-  static constexpr uint32_t kBytes = kUsed + 1024;
-  static_assert(kBytes <= 232448, "shared memory budget");
-  static_assert(kBar % 8 == 0, "mbarrier alignment");
+// Shared-memory layout, computed on the host from the weight format and K: as
+// many stages as fit (the bytes in flight per SM set the streaming rate), the
+// MXFP4 tile scale rows (two buffers of 256 rows x K/32 bytes), the GLU
+// staging rows, the tile prefix, the barriers.
+struct DgLayout {
+  int stages;
+  uint32_t tsf, tsf_bytes, epi, prefix, bar, tmem_slot, abort_flag, scan, bytes;
 };
+
+DgLayout dg_layout(bool fp4, int Ks) {
+  DgLayout L{};
+  L.tsf_bytes = fp4 ? (uint32_t)(256 * Ks + 15) / 16 * 16 : 0u;
+  const uint32_t epi_bytes = kEpiSlots * kEpiStride * 4 + 16;
+  const uint32_t prefix_bytes = (kDgMaxLocal + 1) * 4 + 4;
+  const uint32_t tail = epi_bytes + prefix_bytes + (3 * kMaxStages + 7) * 8 + 4 + 4 + 32 * 4;
+  const uint32_t fixed = 2 * L.tsf_bytes + tail + 1024;  // + slack for the 1024-byte alignment
+  L.stages = (int)((kSmemMax - fixed) / kStBytes);
+  if (L.stages > kMaxStages) L.stages = kMaxStages;
+  L.tsf = (uint32_t)L.stages * kStBytes;
+  L.epi = L.tsf + 2 * L.tsf_bytes;
+  L.prefix = L.epi + epi_bytes;
+  L.bar = L.prefix + prefix_bytes;  // 8-byte aligned: every term above is a multiple of 8
+  L.tmem_slot = L.bar + (3 * L.stages + 7) * 8;
+  L.abort_flag = L.tmem_slot + 4;
+  L.scan = L.abort_flag + 4;
+  L.bytes = L.scan + 32 * 4 + 1024;
+  return L;
+}
 
 __host__ __device__ constexpr int align16i(int v) { return (v + kDgAlign - 1) / kDgAlign * kDgAlign; }
 
@@ -262,6 +277,7 @@ struct DgArgs {
   uint8_t* a_split;   // GLU: [2R][M] e4m3 terms of act (split rows)
   uint32_t* a_sf;     // GLU: [ceil(M/128)][2R]
   uint32_t* err;
+  DgLayout lay;
 };
 
 // Instruction descriptor: A (activation terms) e4m3, B (weights) e2m1 (5) or
@@ -277,17 +293,17 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
                                                                     const __grid_constant__ CUtensorMap tmWt,
                                                                     const __grid_constant__ CUtensorMap tmA,
                                                                     const __grid_constant__ DgArgs a) {
-  using L = DgSmem<kFp4>;
-  constexpr int S = L::kStages;
+  const DgLayout& L = a.lay;
+  const int S = L.stages;
   constexpr int RT = kGlu ? 128 : 256;  // output rows per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
-  int32_t* P = reinterpret_cast<int32_t*>(smem + L::kPrefix);
-  const uint32_t bar0 = sbase + L::kBar;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem_slot);
+  int32_t* P = reinterpret_cast<int32_t*>(smem + L.prefix);
+  const uint32_t bar0 = sbase + L.bar;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
   auto sfin_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
@@ -327,7 +343,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
   pdl_wait();
   const int nmb = (a.M + RT - 1) / RT;
   block_exclusive_scan(a.n_local, [&](int e) { return (a.cnt[e] + kDgChunk - 1) / kDgChunk * nmb; }, P,
-                       reinterpret_cast<int32_t*>(smem + L::kScan));
+                       reinterpret_cast<int32_t*>(smem + L.scan));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -370,7 +386,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
       int s = 0;
       uint32_t ph = 0;
-      int issued[S];
+      int issued[kMaxStages];
       for (int i = 0; i < S; ++i) issued[i] = -1;
       bool ok = true;
       int ti = 0;
@@ -382,7 +398,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
         if (kFp4) {
           const int tb = ti & 1;
           if (!(ok = wait_phase(tsf_empty(tb), ((ti >> 1) & 1) ^ 1u, abort_flag, a.err))) break;
-          const uint32_t dst = sbase + L::kTsf + tb * L::kTsfBytes;
+          const uint32_t dst = sbase + L.tsf + tb * L.tsf_bytes;
           const uint8_t* wexp = a.wsf + (size_t)e * a.rows * Ks;
           if (kGlu && !a.interleaved) {
             const uint32_t vg = (uint32_t)min(128, a.M - m0);
@@ -482,7 +498,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
       const int m0 = mb * RT;
       const int tb = ti & 1;
       if (kFp4 && !(ok = wait_phase(tsf_full(tb), (ti >> 1) & 1, abort_flag, a.err))) break;
-      const uint8_t* tsf = smem + L::kTsf + tb * L::kTsfBytes;
+      const uint8_t* tsf = smem + L.tsf + tb * L.tsf_bytes;
       for (int kc = 0; kc < KC; ++kc) {
         if (!(ok = wait_phase(sfin_bar(s), ph, abort_flag, a.err))) break;
         uint8_t* st = stage(s);
@@ -581,10 +597,12 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
       // consecutive rows (coalesced stores; one warp reduction per group of
       // 32 for the split of act). The accumulator is released after the last
       // pass's reads.
-      float* buf = reinterpret_cast<float*>(smem + L::kEpi);
-      const int npass = (live + 15) / 16;
+      float* buf = reinterpret_cast<float*>(smem + L.epi);
+      const int npass = (live + kEpiSlots - 1) / kEpiSlots;
       for (int p = 0; p < npass; ++p) {
-        if (q == p) {
+        // slots 8p..8p+7: lanes 8(p % 2) + j (hi) and + 16 (lo) of warp p / 2
+        const int lane0 = kEpiSlots * (p & 1);
+        if (q == (p >> 1)) {
           for (int ch = 0; ch < nchunk; ++ch) {
             uint32_t g[32], u[32];
             const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + 32u * ch;
@@ -595,9 +613,9 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
             for (int j = 0; j < 32; ++j) {
               const float gs = __uint_as_float(g[j]) + __shfl_xor_sync(kAll, __uint_as_float(g[j]), 16);
               const float us = __uint_as_float(u[j]) + __shfl_xor_sync(kAll, __uint_as_float(u[j]), 16);
-              if (lane < 16) {
-                buf[lane * kEpiStride + 32 * ch + j] = gs;
-                buf[lane * kEpiStride + 128 + 32 * ch + j] = us;
+              if (lane >= lane0 && lane < lane0 + kEpiSlots) {
+                buf[(lane - lane0) * kEpiStride + 32 * ch + j] = gs;
+                buf[(lane - lane0) * kEpiStride + 128 + 32 * ch + j] = us;
               }
             }
           }
@@ -606,9 +624,9 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
           if (p == npass - 1 && lane == 0) mbar_arrive(acc_empty);
         }
         named_barrier(1, 128);
-        const int np = min(16, live - 16 * p);
+        const int np = min(kEpiSlots, live - kEpiSlots * p);
         for (int sl = q; sl < np; sl += 4) {
-          const int col = 16 * p + sl;  // chunk column
+          const int col = kEpiSlots * p + sl;  // chunk column
           const int slot = a.row_slot[r0 + col];
           const int srow = r0 + col;
           uint16_t* yrow = a.y + (size_t)slot * a.rows;
@@ -665,7 +683,7 @@ __global__ void __launch_bounds__(kDgThreads, 1) decode_gemm_kernel(const __grid
 template <bool kFp4, bool kGlu>
 cudaError_t set_smem() {
   return cudaFuncSetAttribute(decode_gemm_kernel<kFp4, kGlu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)DgSmem<kFp4>::kBytes);
+                              (int)kSmemMax);
 }
 
 // Weight tensor map over [n_local][rows][K] (FP8 bytes, or e2m1 nibbles):
@@ -720,6 +738,8 @@ bool decode_gemm_ok(int T, int k, int H, int I, int n_local, int wfmt) {
   if (H % 32 != 0 || I % 32 != 0 || H < kDgBK || I < kDgBK) return false;
   // MXFP4: the ragged-K map starts at byte (K - 128) / 2, 32-byte aligned
   if (wfmt == MOE_WFMT_MXFP4_G32 && (H / 32 > kDgMaxKs || I / 32 > kDgMaxKs || H % 64 || I % 64)) return false;
+  const bool fp4 = wfmt == MOE_WFMT_MXFP4_G32;
+  if (dg_layout(fp4, H / 32).stages < 2 || dg_layout(fp4, I / 32).stages < 2) return false;
   return true;
 }
 
@@ -803,10 +823,11 @@ int launch_decode_gemm(const moe_decode_args& a, EncodeTiledFn enc, int num_sms,
   g.act = a.act;
   g.a_split = as;
   g.a_sf = asf;
+  g.lay = dg_layout(fp4, a.H / 32);
   cudaError_t ce = fp4 ? launch_maybe_pdl(decode_gemm_kernel<true, true>, dim3(num_sms), dim3(kDgThreads),
-                                          DgSmem<true>::kBytes, st, true, mW1, mW1t, mB1, g)
+                                          (size_t)g.lay.bytes, st, true, mW1, mW1t, mB1, g)
                        : launch_maybe_pdl(decode_gemm_kernel<false, true>, dim3(num_sms), dim3(kDgThreads),
-                                          DgSmem<false>::kBytes, st, true, mW1, mW1t, mB1, g);
+                                          (size_t)g.lay.bytes, st, true, mW1, mW1t, mB1, g);
   if (ce != cudaSuccess) return MOE_ERR_CUDA;
   // GEMM 2
   g.asf = asf;
@@ -821,10 +842,11 @@ int launch_decode_gemm(const moe_decode_args& a, EncodeTiledFn enc, int num_sms,
   g.act = nullptr;
   g.a_split = nullptr;
   g.a_sf = nullptr;
-  ce = fp4 ? launch_maybe_pdl(decode_gemm_kernel<true, false>, dim3(num_sms), dim3(kDgThreads), DgSmem<true>::kBytes,
+  g.lay = dg_layout(fp4, a.I / 32);
+  ce = fp4 ? launch_maybe_pdl(decode_gemm_kernel<true, false>, dim3(num_sms), dim3(kDgThreads), (size_t)g.lay.bytes,
                               st, true, mW2, mW2t, mB2, g)
-           : launch_maybe_pdl(decode_gemm_kernel<false, false>, dim3(num_sms), dim3(kDgThreads),
-                              DgSmem<false>::kBytes, st, true, mW2, mW2t, mB2, g);
+           : launch_maybe_pdl(decode_gemm_kernel<false, false>, dim3(num_sms), dim3(kDgThreads), (size_t)g.lay.bytes,
+                              st, true, mW2, mW2t, mB2, g);
   if (ce != cudaSuccess) return MOE_ERR_CUDA;
   return launch_weighted_sum(a, true, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

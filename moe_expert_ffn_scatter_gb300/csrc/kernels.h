@@ -71,7 +71,11 @@ int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, ui
                         cudaStream_t st);
 
 cudaError_t init_decode();
-cudaError_t launch_decode(const moe_decode_args& a, int num_sms, uint32_t* err, cudaStream_t st);
+// mma.sync path when allowed and applicable (decode_mma_sync_ok), else the
+// per-(token, slot) GEMV launches.
+bool decode_mma_sync_ok(const moe_decode_args& a);
+cudaError_t launch_decode(const moe_decode_args& a, bool allow_mma_sync, int num_sms, uint32_t* err,
+                          cudaStream_t st);
 // out = slot-ordered weighted sum of y2 over local slots (last launch of both
 // decode paths); pdl: may start before the previous kernel has finished.
 cudaError_t launch_weighted_sum(const moe_decode_args& a, bool pdl, cudaStream_t st);

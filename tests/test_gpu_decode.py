@@ -41,7 +41,12 @@ def inputs_big(T, seed=synth.DECODE_SEED + 100):
     return synth.DecodeInputs(d.x[:T], d.logits[:T], d.fp8, d.mxfp4)
 
 
-def run_decode(ctx, d, ids, w, wfmt, H, I, es, nl, fill=0x7FC0, ws=False, glu_layout=B.MOE_GLU_INTERLEAVED):
+def run_decode(ctx, d, ids, w, wfmt, H, I, es, nl, fill=0x7FC0, ws=False, glu_layout=B.MOE_GLU_INTERLEAVED,
+               path=None):
+    """ws=True forces the tcgen05 path (with a workspace), ws=False the
+    mma.sync path where it applies; path overrides."""
+    if path is None:
+        path = B.MOE_DECODE_TCGEN05 if ws else B.MOE_DECODE_AUTO
     T, k = ids.shape
     W = d.fp8 if wfmt == B.MOE_WFMT_FP8_PER_EXPERT else d.mxfp4
     loc = {kk: v[es:es + nl] for kk, v in W.items()}
@@ -53,7 +58,7 @@ def run_decode(ctx, d, ids, w, wfmt, H, I, es, nl, fill=0x7FC0, ws=False, glu_la
     B.moe_sparse_gemv_decode(ctx, x=dev_bf16(d.x), topk_ids=dev(ids), topk_w=dev(w), expert_start=es,
                              num_local_experts=nl, wfmt=wfmt, w_gu=dev(loc["w_gu"]), b_gu=dev_bf16(loc["b_gu"]),
                              w_d=dev(loc["w_d"]), b_d=dev_bf16(loc["b_d"]), y1=y1, act=act, y2=y2, out=out,
-                             T=T, H=H, I=I, k=k, glu_layout=glu_layout,
+                             T=T, H=H, I=I, k=k, glu_layout=glu_layout, path=path,
                              workspace=B.decode_workspace(T, k, H, I, nl) if ws else None, **kw)
     torch.cuda.synchronize()
     return host_u16(y1), host_u16(act), host_u16(y2), host_u16(out), loc
@@ -200,7 +205,7 @@ def test_decode_tcgen05_graph_replay_new_routing(ctx, orc):
 
 def test_decode_tcgen05_workspace_checks(ctx):
     """A workspace smaller than moe_decode_workspace_size or misaligned is an
-    invalid argument; T > 128 with a workspace too."""
+    invalid argument for the tcgen05 path."""
     T, k, H, I, nl = 16, 4, 256, 128, 8
     need = B.moe_decode_workspace_size(T, k, H, I, nl)
     assert need > 0 and B.moe_decode_workspace_size(0, k, H, I, nl) == 0
@@ -212,9 +217,46 @@ def test_decode_tcgen05_workspace_checks(ctx):
                 w_gu_scale=torch.ones(nl, device="cuda"), b_gu=z(nl, 2 * I), w_d=u8(nl * H * I),
                 w_d_scale=torch.ones(nl, device="cuda"), b_d=z(nl, H), y1=z(T, k, 2 * I), act=z(T * k, I),
                 y2=z(T, k, H), out=z(T, H), T=T, H=H, I=I, k=k)
+    tc5 = B.MOE_DECODE_TCGEN05
     with pytest.raises(B.MoeError):
-        B.moe_sparse_gemv_decode(ctx, workspace=u8(need - 1024), **args)
+        B.moe_sparse_gemv_decode(ctx, workspace=u8(need - 1024), path=tc5, **args)
     with pytest.raises(B.MoeError):
-        B.moe_sparse_gemv_decode(ctx, workspace=u8(need + 1024)[16:], **args)
-    B.moe_sparse_gemv_decode(ctx, workspace=u8(need), **args)
+        B.moe_sparse_gemv_decode(ctx, workspace=u8(need + 1024)[16:], path=tc5, **args)
+    B.moe_sparse_gemv_decode(ctx, workspace=u8(need), path=tc5, **args)
+    torch.cuda.synchronize()
+
+
+@WFMTS
+@pytest.mark.parametrize("T", [1, 16])
+def test_decode_auto_path_matches_forced(ctx, orc, wfmt, T):
+    """AUTO with a workspace: T = 1 takes the mma.sync path, T = 16 the tcgen05
+    path, bit for bit the forced results."""
+    d = inputs_big(T)
+    ids, w = orc.route_softmax_topk(d.logits, synth.DECODE_K)
+    H = I = synth.DECODE_H
+    forced = B.MOE_DECODE_MMA_SYNC if T <= 8 else B.MOE_DECODE_TCGEN05
+    auto = run_decode(ctx, d, ids, w, wfmt, H, I, 0, synth.DECODE_E, ws=True, path=B.MOE_DECODE_AUTO)
+    ref = run_decode(ctx, d, ids, w, wfmt, H, I, 0, synth.DECODE_E, ws=True, path=forced)
+    for a_, b_ in zip(auto[:4], ref[:4]):
+        assert np.array_equal(a_, b_)
+
+
+def test_decode_forced_path_checks(ctx):
+    """A forced path that does not apply is an invalid argument."""
+    T, k, H, I, nl = 16, 4, 256, 128, 8
+    z = lambda *shape: torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+    u8 = lambda n: torch.zeros(n, dtype=torch.uint8, device="cuda")
+    args = dict(x=z(T, H), topk_ids=torch.zeros((T, k), dtype=torch.int32, device="cuda"),
+                topk_w=torch.zeros((T, k), dtype=torch.float32, device="cuda"), expert_start=0,
+                num_local_experts=nl, wfmt=B.MOE_WFMT_FP8_PER_EXPERT, w_gu=u8(nl * 2 * I * H),
+                w_gu_scale=torch.ones(nl, device="cuda"), b_gu=z(nl, 2 * I), w_d=u8(nl * H * I),
+                w_d_scale=torch.ones(nl, device="cuda"), b_d=z(nl, H), y1=z(T, k, 2 * I), act=z(T * k, I),
+                y2=z(T, k, H), out=z(T, H), T=T, H=H, I=I, k=k)
+    with pytest.raises(B.MoeError):  # tcgen05 without a workspace
+        B.moe_sparse_gemv_decode(ctx, path=B.MOE_DECODE_TCGEN05, **args)
+    with pytest.raises(B.MoeError):  # mma.sync takes T <= 8
+        B.moe_sparse_gemv_decode(ctx, path=B.MOE_DECODE_MMA_SYNC, **args)
+    with pytest.raises(B.MoeError):
+        B.moe_sparse_gemv_decode(ctx, path=7, **args)
+    B.moe_sparse_gemv_decode(ctx, path=B.MOE_DECODE_GEMV, **args)
     torch.cuda.synchronize()
