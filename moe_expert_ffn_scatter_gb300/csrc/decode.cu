@@ -509,6 +509,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
         if (a.glu) bias1 = bf16_to_f32(bst[tc_blk_row(a, gl + 8)]);
       }
     }
+    // The bias values above are read from the stage (generic proxy) but used
+    // only after its release; the next bulk copy (async proxy) may refill the
+    // stage as soon as the empty barrier completes, so fence the reads first.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     named_barrier(1, kCT);
     if (threadIdx.x == 0 && ok) pipe_mbar_arrive(smem_addr(bars + nst + s));
     if (ok && threadIdx.x < nout) {

@@ -17,12 +17,16 @@
 //   decode_gemm_kernel        y2 = W_d act (* scale) + b
 //   weighted_sum_kernel       (decode.cu) out = slot-ordered sum of topk_w y2
 //
-// Operands of tcgen05.mma.kind::mxf8f6f4.block_scale (M128, N = the expert's
-// slots rounded up to 16, at most 64 per tile, K32): the weights are the A
-// operand, 128 rows per tile, moved by TMA in their stored format (e4m3, or
-// e2m1 expanded to a byte per element by the 16U4_ALIGN16B tensor-map type)
-// with their UE8M0 group-32 scales -- FP8-per-expert weights take unit scales
-// and their fp32 scale in the epilogue; the slots are the B operand.
+// Operands of tcgen05.mma.kind::mxf8f6f4.block_scale (M128, N256, K32): the
+// weights are the B operand, 256 rows per tile (with the GLU the gate and the
+// up 128-row blocks of the same output rows), moved by TMA in their stored
+// format (e4m3, or e2m1 expanded to a byte per element by the 16U4_ALIGN16B
+// tensor-map type) with their UE8M0 group-32 scales -- FP8-per-expert weights
+// take unit scales and their fp32 scale in the epilogue; the A operand holds
+// the two activation terms of up to 32 slots (64 rows; the accumulator lanes
+// of the other 64 rows are never read). A small-N MMA costs about as much as
+// a wide one, so the wide side goes to the weights: 4 MMAs per 128-wide K
+// block.
 //
 // Two-term activation split. For a group of 32 bf16 values v with absolute
 // maximum a:
@@ -37,10 +41,11 @@
 // GEMM kernel structure (one persistent CTA per SM, 256 threads), as in the
 // grouped GEMM of the layer path:
 //   warp 0    producer: the tile's weight scale rows (MXFP4, one bulk copy per
-//             tile), then per 128-wide K block the B terms' scale words (bulk)
-//             and the A (gate and up blocks with GLU) and B tiles (TMA)
-//   warp 1    TMEM owner and MMA issuer (two accumulators of 64 columns per
-//             buffer, double-buffered)
+//             tile), then per 128-wide K block the activation terms' scale
+//             words (bulk), the A tile (activation terms) and the B tile
+//             (weights; the gate and up blocks with GLU) by TMA
+//   warp 1    TMEM owner and MMA issuer: one 128 x 256 fp32 accumulator,
+//             released by the epilogue once it has read it
 //   warp 2    scale transposer: A and B scale words into the 32-row x 16-byte
 //             source layout of tcgen05.cp 32x128b.warpx4
 //   warps 4-7 epilogue: tcgen05.ld, bias, GLU and the split of act, or bias
