@@ -2,9 +2,13 @@
 //
 // Combine ([DG] §2.6.1, post_reorder): out[t] = bf16(rsf * sum_j w[t,j] *
 // down[src2dst[t,j]]) over the slots with src2dst >= 0, fp32 accumulation,
-// one fused multiply-add per slot in slot order. One thread per (token, 8
-// columns): uint4 gathers from the k grouped rows, a uint4 store; the token's
-// src2dst / weights are warp-broadcast loads.
+// one fused multiply-add per slot in slot order. A warp per work item (token,
+// 256 columns), 8 columns per lane: lanes j < k hold the token's slot j
+// (src2dst, weight), broadcast by shuffles; uint4 gathers from the k grouped
+// rows, a uint4 store. The slot data of the warp's next item is loaded while
+// the current item's gathers are in flight, so an item costs one memory
+// round trip instead of two dependent ones. k > 32 takes
+// combine_kernel_wide, a thread per (token, 8 columns).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -12,7 +16,80 @@ namespace moe {
 
 namespace {
 
-__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ down, int H,
+#ifndef MOE_COMBINE_BPS
+#define MOE_COMBINE_BPS 3
+#endif
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
+constexpr int kCombineBlocksPerSm = MOE_COMBINE_BPS;  // grid: one wave of resident blocks
+
+__global__ void __launch_bounds__(256, kCombineBlocksPerSm) combine_kernel(const uint16_t* __restrict__ down, int H,
+                                                      const float* __restrict__ topk_w,
+                                                      const int32_t* __restrict__ s2d, int T, int k,
+                                                      float rsf, uint16_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int cb = (H + 255) / 256;  // 256-column blocks per token
+  const long n_items = (long)T * cb;
+  const long wstride = (long)gridDim.x * (blockDim.x / 32);
+  long item = (long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  int nxt_dst = -1;
+  float nxt_w = 0.0f;
+  auto load_slots = [&](long it) {
+    nxt_dst = -1;
+    nxt_w = 0.0f;
+    if (it < n_items && lane < k) {
+      const size_t o = (size_t)(it / cb) * k + lane;
+      nxt_dst = s2d[o];
+      nxt_w = topk_w[o];
+    }
+  };
+  load_slots(item);
+  for (; item < n_items; item += wstride) {
+    const int my_dst = nxt_dst;
+    const float my_w = nxt_w;
+    load_slots(item + wstride);
+    const int t = (int)(item / cb);
+    const int c = (int)(item % cb) * 256 + lane * 8;
+    const bool in = c < H;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      int dst[8];
+      float wt[8];
+      uint4 v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        dst[q] = __shfl_sync(kFullMask, my_dst, (j0 + q) & 31);
+        wt[q] = __shfl_sync(kFullMask, my_w, (j0 + q) & 31);
+        if (j0 + q >= k) dst[q] = -1;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        v[q] = (dst[q] >= 0 && in) ? __ldg(reinterpret_cast<const uint4*>(down + (size_t)dst[q] * H + c))
+                                   : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (dst[q] < 0) continue;
+        const uint32_t* pv = &v[q].x;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = __fmaf_rn(wt[q], bf16_lo(pv[i]), acc[2 * i]);
+          acc[2 * i + 1] = __fmaf_rn(wt[q], bf16_hi(pv[i]), acc[2 * i + 1]);
+        }
+      }
+    }
+    if (in) {
+      uint4 o;
+      uint32_t* po = &o.x;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        po[i] = pack_bf16x2(__fmul_rn(acc[2 * i], rsf), __fmul_rn(acc[2 * i + 1], rsf));
+      *reinterpret_cast<uint4*>(out + (size_t)t * H + c) = o;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) combine_kernel_wide(const uint16_t* __restrict__ down, int H,
                                                       const float* __restrict__ topk_w,
                                                       const int32_t* __restrict__ s2d, int T, int k,
                                                       float rsf, uint16_t* __restrict__ out) {
@@ -122,7 +199,13 @@ cudaError_t launch_combine(const uint16_t* down, int H, const float* topk_w, con
                            int T, int k, float rsf, uint16_t* out, int num_sms, cudaStream_t st) {
   const long total = (long)T * (H / 8);
   if (total == 0) return cudaSuccess;
-  const int blocks = (int)lmin((total + 255) / 256, (long)num_sms * 8);
+  if (k > 32) {
+    const int blocks = (int)lmin((total + 255) / 256, (long)num_sms * 8);
+    combine_kernel_wide<<<blocks, 256, 0, st>>>(down, H, topk_w, src2dst, T, k, rsf, out);
+    return cudaGetLastError();
+  }
+  const long items = (long)T * ((H + 255) / 256);
+  const int blocks = (int)lmin((items + 7) / 8, (long)num_sms * kCombineBlocksPerSm);
   combine_kernel<<<blocks, 256, 0, st>>>(down, H, topk_w, src2dst, T, k, rsf, out);
   return cudaGetLastError();
 }
