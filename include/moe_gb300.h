@@ -170,8 +170,10 @@ typedef struct moe_act_params {
  *  PRECOMPUTED); topk_w [T,k] fp32 (written; ignored if PRECOMPUTED);
  *  x [T,H] bf16; a_fp8 [cap,H] e4m3; a_sf ASF [ceil(H/512)][align4(cap)];
  *  expert_ends [E] int32 (written); src2dst [T,k] int32 (written);
- *  workspace: moe_route_scatter_workspace_size(T,E,k) bytes of scratch,
- *  16-byte aligned, contents need not be initialised.
+ *  workspace: moe_route_scatter_workspace_size(T,E,k) bytes of scratch
+ *  (ceil(T/64) * E int32 chunk histograms and a 4-byte completion count,
+ *  rounded up to 16 bytes), 16-byte aligned, contents need not be
+ *  initialised; calls that share a workspace must not overlap on the GPU.
  * Sizes: T >= 0 (T == 0 writes expert_ends = 0 and nothing else),
  *  1 <= E <= 4096 (E <= 1024 for the two routing modes), 1 <= k <= min(E, 32),
  *  H % 128 == 0, A >= 1, cap >= T*k + E*(A-1). Logits must be finite.
@@ -211,9 +213,10 @@ MOE_API int moe_route_scatter(moe_ctx* ctx, const moe_route_args* args, moe_stre
  *
  * Same operation, arguments, results and errors as moe_route_scatter, except
  * that args->workspace and args->workspace_bytes are ignored: the scratch (the
- * per-chunk expert histograms, ceil(T/64) * E int32) lives in a 1 MiB device
- * array inside the library. Every GPU that loads the library holds that array
- * until the process exits. Limit: ceil(T/64) * E * 4 <= 1 MiB (T <= 4096 with
+ * per-chunk expert histograms, ceil(T/64) * E int32, and a 4-byte completion
+ * count) lives in a device array of 1 MiB + 16 bytes inside the library. Every
+ * GPU that loads the library holds that array until the process exits.
+ * Limit: ceil(T/64) * E * 4 <= 1 MiB (T <= 4096 with
  * any E <= 4096; T = 65536 with E <= 256); larger sizes return
  * MOE_ERR_UNSUPPORTED. Allocates nothing.
  *

@@ -7,19 +7,20 @@
 // [DG] §2.2.4 (compact layout: per-token-group quantisation, ep_scatter into
 // expert-contiguous segments) and 附录 C (src2dst).
 //
-// Four launches, all with grids fixed by (T, E, k, H) so a CUDA graph can
+// Three launches, all with grids fixed by (T, E, k, H) so a CUDA graph can
 // replay them while routing changes:
 //   1. route_kernel         one warp per token: scores -> selection keys, top-k
 //      from per-lane sorted lists with warp max/min reductions, weights
-//      (skipped when the caller supplies the routing).
+//      (replaced by a 4-byte memset when the caller supplies the routing).
 //   2. rank_count_kernel    one block per chunk of 64 tokens: one warp ranks
 //      the chunk's routes per expert in row-major (token, slot) order with
 //      match_any; rank inside the chunk -> src2dst, chunk histogram ->
-//      workspace.
-//   3. endpoints_kernel     one block: per expert, exclusive prefix of the
-//      chunk histograms over chunks (coalesced, independent loads), then a
-//      block scan of the A-aligned counts -> expert_ends.
-//   4. scatter_quant_kernel one warp per token: final src2dst = start[e] +
+//      workspace. The last block to finish then computes the endpoints: per
+//      expert, exclusive prefix of the chunk histograms over chunks
+//      (coalesced, independent loads), then a block scan of the A-aligned
+//      counts -> expert_ends (endpoints_block; endpoints_kernel runs the same
+//      code alone for counts given by the caller, or T = 0).
+//   3. scatter_quant_kernel one warp per token: final src2dst = start[e] +
 //      chunk prefix + rank, then the token row is quantised once (16 lanes per
 //      128-column group, or 4 per 32-column group in the MXFP8 recipe; uint4
 //      loads) and its codes and packed scale words are stored to each
@@ -140,11 +141,15 @@ __device__ __forceinline__ void route_token(const float* __restrict__ l, const f
 }
 
 // One warp per token over the whole grid.
+// Block 0 also zeroes the completion count of the rank/count launch that
+// follows (`done`, in the workspace).
 template <int EPL, int MODE>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits,
                                                     const float* __restrict__ bias, int32_t* __restrict__ ids,
-                                                    float* __restrict__ topw, int T, int E, int k) {
+                                                    float* __restrict__ topw, int T, int E, int k,
+                                                    unsigned int* __restrict__ done) {
   const int lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && done) *done = 0u;
   const int wpb = blockDim.x >> 5;
   for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb)
     route_token<EPL, MODE>(logits + (size_t)t * E, bias, E, k, lane, ids + (size_t)t * k, topw + (size_t)t * k);
@@ -154,9 +159,17 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
 // per expert in row-major (token, slot) order -- 32 at a time by one warp,
 // peers with the same expert ranked by lane via match_any -- and the rank
 // inside the chunk goes to src2dst, the chunk histogram to the workspace.
+__device__ void endpoints_block(const int32_t* __restrict__ counts, int32_t* __restrict__ ws, int nchunks, int E,
+                                int A, int32_t* __restrict__ ends, long cap, uint32_t* err, int32_t* cnt_s,
+                                int32_t* warp_sums, int32_t* carry);
+
+// The last block to finish (a completion count in the workspace, zeroed by
+// the launch sequence before this kernel and again by that block) then runs
+// the endpoint step over all the histograms.
 __global__ void __launch_bounds__(256) rank_count_kernel(const int32_t* __restrict__ ids,
                                                          int32_t* __restrict__ s2d, int32_t* __restrict__ ws,
-                                                         int T, int E, int k) {
+                                                         int T, int E, int k, int A, int32_t* __restrict__ ends,
+                                                         long cap, uint32_t* err) {
   extern __shared__ int32_t smem_i32[];
   int32_t* cnt = smem_i32;                 // [E] running count per expert
   int32_t* ids_s = smem_i32 + E;           // [kScatterChunk * k] the chunk's expert ids
@@ -185,6 +198,20 @@ __global__ void __launch_bounds__(256) rank_count_kernel(const int32_t* __restri
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) ws[(size_t)c * E + e] = cnt[e];
+  // last block: the endpoints (histograms of every block are visible after
+  // the fences around the completion count)
+  __shared__ int last;
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t carry;
+  unsigned int* done = reinterpret_cast<unsigned int*>(ws + (size_t)gridDim.x * E);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  endpoints_block(nullptr, ws, (int)gridDim.x, E, A, ends, cap, err, cnt, warp_sums, &carry);
+  if (threadIdx.x == 0) *done = 0u;
 }
 
 // Endpoints. With `counts` given, count[e] = counts[e]; otherwise count[e] is
@@ -194,15 +221,16 @@ __global__ void __launch_bounds__(256) rank_count_kernel(const int32_t* __restri
 // with independent loads, the run totals are scanned across the P lanes, and
 // the run is written back. The block then scans the A-aligned counts over
 // experts: start[e] = align_up(end[e-1], A), end[e] = start[e] + count[e].
-__global__ void __launch_bounds__(1024) endpoints_kernel(const int32_t* __restrict__ counts,
-                                                         int32_t* __restrict__ ws, int nchunks, int E,
-                                                         int A, int32_t* __restrict__ ends, long cap,
-                                                         uint32_t* err) {
-  extern __shared__ int32_t cnt_s[];       // [E]
-  __shared__ int32_t warp_sums[32];
-  __shared__ int32_t carry;
+// The block's work, with any block size (a multiple of 32): cnt_s [E] and
+// warp_sums [32] in shared memory, carry one shared int. The histograms are
+// read with ld.global.cg: in the fused launch they were written by other
+// blocks of the same kernel.
+__device__ void endpoints_block(const int32_t* __restrict__ counts, int32_t* __restrict__ ws, int nchunks, int E,
+                                int A, int32_t* __restrict__ ends, long cap, uint32_t* err, int32_t* cnt_s,
+                                int32_t* warp_sums, int32_t* carry) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) carry = 0;
+  const int nwarps = (int)blockDim.x >> 5;
+  if (threadIdx.x == 0) *carry = 0;
   if (counts) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = counts[e];
   } else {
@@ -222,7 +250,7 @@ __global__ void __launch_bounds__(1024) endpoints_kernel(const int32_t* __restri
         for (int c0 = c_lo; c0 < c_hi; c0 += U) {
           int v[U];
 #pragma unroll
-          for (int u = 0; u < U; ++u) v[u] = (c0 + u < c_hi) ? ws[(size_t)(c0 + u) * E + e] : 0;
+          for (int u = 0; u < U; ++u) v[u] = (c0 + u < c_hi) ? __ldcg(ws + (size_t)(c0 + u) * E + e) : 0;
 #pragma unroll
           for (int u = 0; u < U; ++u) tot += v[u];
         }
@@ -237,7 +265,7 @@ __global__ void __launch_bounds__(1024) endpoints_kernel(const int32_t* __restri
         for (int c0 = c_lo; c0 < c_hi; c0 += U) {
           int v[U];
 #pragma unroll
-          for (int u = 0; u < U; ++u) v[u] = (c0 + u < c_hi) ? ws[(size_t)(c0 + u) * E + e] : 0;
+          for (int u = 0; u < U; ++u) v[u] = (c0 + u < c_hi) ? __ldcg(ws + (size_t)(c0 + u) * E + e) : 0;
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             if (c0 + u < c_hi) ws[(size_t)(c0 + u) * E + e] = run;
@@ -249,7 +277,7 @@ __global__ void __launch_bounds__(1024) endpoints_kernel(const int32_t* __restri
     }
   }
   __syncthreads();
-  for (int base = 0; base < E; base += 1024) {
+  for (int base = 0; base < E; base += blockDim.x) {
     const int e = base + threadIdx.x;
     const int total = (e < E) ? cnt_s[e] : 0;
     const int aligned = (e < E) ? (int)align_up64(total, A) : 0;
@@ -262,22 +290,32 @@ __global__ void __launch_bounds__(1024) endpoints_kernel(const int32_t* __restri
     if (lane == 31) warp_sums[warp] = v;
     __syncthreads();
     if (warp == 0) {
-      int s = warp_sums[lane];
+      int sm = (lane < nwarps) ? warp_sums[lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(kFull, s, o);
-        if (lane >= o) s += n;
+        const int n = __shfl_up_sync(kFull, sm, o);
+        if (lane >= o) sm += n;
       }
-      warp_sums[lane] = s;
+      if (lane < nwarps) warp_sums[lane] = sm;
     }
     __syncthreads();
-    const int start = carry + (v - aligned) + (warp > 0 ? warp_sums[warp - 1] : 0);
+    const int start = *carry + (v - aligned) + (warp > 0 ? warp_sums[warp - 1] : 0);
     if (e < E) ends[e] = start + total;
     __syncthreads();
-    if (threadIdx.x == 0) carry += warp_sums[31];
+    if (threadIdx.x == 0) *carry += warp_sums[nwarps - 1];
     __syncthreads();
   }
   if (threadIdx.x == 0 && E > 0 && cap >= 0 && (long)ends[E - 1] > cap) raise_error(err, MOE_DEVERR_CAPACITY);
+}
+
+__global__ void __launch_bounds__(1024) endpoints_kernel(const int32_t* __restrict__ counts,
+                                                         int32_t* __restrict__ ws, int nchunks, int E,
+                                                         int A, int32_t* __restrict__ ends, long cap,
+                                                         uint32_t* err) {
+  extern __shared__ int32_t cnt_s[];  // [E]
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t carry;
+  endpoints_block(counts, ws, nchunks, E, A, ends, cap, err, cnt_s, warp_sums, &carry);
 }
 
 __device__ __forceinline__ uint32_t e4m3x4(const float* f, float sc) {
@@ -376,31 +414,34 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(const uint16_t* __re
 }
 
 template <int EPL, int MODE>
-cudaError_t launch_route(const moe_route_args& a, int num_sms, cudaStream_t st) {
+cudaError_t launch_route(const moe_route_args& a, int num_sms, unsigned int* done, cudaStream_t st) {
   const int blocks = (int)lmin((a.T + 7) / 8, (long)num_sms * 8);
-  route_kernel<EPL, MODE><<<blocks, 256, 0, st>>>(a.logits, a.corr_bias, a.topk_ids, a.topk_w, a.T, a.E, a.k);
+  route_kernel<EPL, MODE><<<blocks, 256, 0, st>>>(a.logits, a.corr_bias, a.topk_ids, a.topk_w, a.T, a.E, a.k,
+                                                  done);
   return cudaGetLastError();
 }
 
 template <int MODE>
-cudaError_t dispatch_epl(const moe_route_args& a, int num_sms, cudaStream_t st) {
+cudaError_t dispatch_epl(const moe_route_args& a, int num_sms, unsigned int* done, cudaStream_t st) {
   const int epl = (a.E + 31) / 32;
-  if (epl <= 1) return launch_route<1, MODE>(a, num_sms, st);
-  if (epl <= 2) return launch_route<2, MODE>(a, num_sms, st);
-  if (epl <= 4) return launch_route<4, MODE>(a, num_sms, st);
-  if (epl <= 8) return launch_route<8, MODE>(a, num_sms, st);
-  if (epl <= 16) return launch_route<16, MODE>(a, num_sms, st);
-  if (epl <= 24) return launch_route<24, MODE>(a, num_sms, st);
-  return launch_route<32, MODE>(a, num_sms, st);
+  if (epl <= 1) return launch_route<1, MODE>(a, num_sms, done, st);
+  if (epl <= 2) return launch_route<2, MODE>(a, num_sms, done, st);
+  if (epl <= 4) return launch_route<4, MODE>(a, num_sms, done, st);
+  if (epl <= 8) return launch_route<8, MODE>(a, num_sms, done, st);
+  if (epl <= 16) return launch_route<16, MODE>(a, num_sms, done, st);
+  if (epl <= 24) return launch_route<24, MODE>(a, num_sms, done, st);
+  return launch_route<32, MODE>(a, num_sms, done, st);
 }
 
 }  // namespace
 
+// Chunk histograms [nchunks][E] int32, then the 4-byte completion count of
+// the rank/count launch, rounded up to 16 bytes.
 size_t route_scatter_ws_bytes(int T, int E, int k) {
   (void)k;
   const size_t nchunks = (size_t)(T + kScatterChunk - 1) / kScatterChunk;
-  const size_t b = nchunks * (size_t)E * sizeof(int32_t);
-  return b < 16 ? 16 : (b + 15) / 16 * 16;
+  const size_t b = nchunks * (size_t)E * sizeof(int32_t) + sizeof(uint32_t);
+  return (b + 15) / 16 * 16;
 }
 
 cudaError_t launch_expert_ends(const int32_t* counts, int E, int A, int32_t* ends, uint32_t* err,
@@ -412,34 +453,40 @@ cudaError_t launch_expert_ends(const int32_t* counts, int E, int A, int32_t* end
 cudaError_t launch_route_scatter(const moe_route_args& a, int num_sms, uint32_t* err, cudaStream_t st) {
   const int nchunks = (a.T + kScatterChunk - 1) / kScatterChunk;
   cudaError_t ce = cudaSuccess;
+  int32_t* ws = (int32_t*)a.workspace;
   if (a.T > 0) {
+    // completion count of rank_count_kernel, zeroed by the routing kernel
+    // (or a 4-byte memset when the routing is given)
+    unsigned int* done = reinterpret_cast<unsigned int*>(ws + (size_t)nchunks * a.E);
     if (a.routing_mode == MOE_ROUTE_SOFTMAX_TOPK)
-      ce = dispatch_epl<MOE_ROUTE_SOFTMAX_TOPK>(a, num_sms, st);
+      ce = dispatch_epl<MOE_ROUTE_SOFTMAX_TOPK>(a, num_sms, done, st);
     else if (a.routing_mode == MOE_ROUTE_SIGMOID_BIAS_TOPK)
-      ce = dispatch_epl<MOE_ROUTE_SIGMOID_BIAS_TOPK>(a, num_sms, st);
+      ce = dispatch_epl<MOE_ROUTE_SIGMOID_BIAS_TOPK>(a, num_sms, done, st);
+    else
+      ce = cudaMemsetAsync(done, 0, sizeof(unsigned int), st);
     if (ce != cudaSuccess) return ce;
     const size_t smem = (size_t)(a.E + kScatterChunk * a.k) * sizeof(int32_t);
-    rank_count_kernel<<<nchunks, 256, smem, st>>>(a.topk_ids, a.src2dst, (int32_t*)a.workspace, a.T, a.E, a.k);
+    rank_count_kernel<<<nchunks, 256, smem, st>>>(a.topk_ids, a.src2dst, ws, a.T, a.E, a.k, a.A, a.expert_ends,
+                                                  a.cap, err);
     if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
-  }
-  endpoints_kernel<<<1, 1024, (size_t)a.E * sizeof(int32_t), st>>>(nullptr, (int32_t*)a.workspace, nchunks,
-                                                                   a.E, a.A, a.expert_ends, a.cap, err);
-  if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
-  if (a.T > 0) {
     const int blocks = (int)lmin((a.T + 7) / 8, (long)num_sms * 16);
-    scatter_quant_kernel<<<blocks, 256, 0, st>>>(a.x, a.topk_ids, a.src2dst, (const int32_t*)a.workspace,
-                                                 a.expert_ends, a.a_fp8, a.a_sf, a.T, a.E, a.k, a.A, a.H,
+    scatter_quant_kernel<<<blocks, 256, 0, st>>>(a.x, a.topk_ids, a.src2dst, (const int32_t*)ws, a.expert_ends,
+                                                 a.a_fp8, a.a_sf, a.T, a.E, a.k, a.A, a.H,
                                                  (int)align_up64(a.cap, 4), a.cap, a.quant_group == 32, err);
-    ce = cudaGetLastError();
+    return cudaGetLastError();
   }
-  return ce;
+  // no tokens: every expert is empty
+  endpoints_kernel<<<1, 1024, (size_t)a.E * sizeof(int32_t), st>>>(nullptr, ws, 0, a.E, a.A, a.expert_ends, a.cap,
+                                                                   err);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------- no-allocation variant
-// Scratch of moe_route_scatter_noalloc: the per-chunk expert histograms live
-// in this file-scope device array instead of a caller-provided workspace.
-// Every GPU that loads the library holds these 1 MiB until the process exits.
-constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
+// Scratch of moe_route_scatter_noalloc: the per-chunk expert histograms (up
+// to 1 MiB) and the rank/count completion count live in this file-scope
+// device array instead of a caller-provided workspace. Every GPU that loads
+// the library holds these 1 MiB + 16 bytes until the process exits.
+constexpr size_t kNoAllocScratchBytes = (size_t(1) << 20) + 16;
 static __device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
 
 namespace {

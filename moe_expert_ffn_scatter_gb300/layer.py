@@ -126,16 +126,19 @@ class MoEFFNLayer:
                             T=self.T, E=self.E, k=self.k, H=self.H, A=self.A, cap=self.cap, stream=stream,
                             quant_group=self.group)
 
-    def ffn(self, stream=None):
+    def ffn(self, stream=None, out=None):
+        """out: [T,H] bf16 device buffer for the result (default self.out)."""
         B.moe_ffn_forward(self.ctx, a_fp8=self.a_fp8, a_sf=self.a_sf, expert_ends=self.expert_ends, w13=self.w13,
                           w13_sf=self.w13_sf, w2=self.w2, w2_sf=self.w2_sf, gateup=self.gateup,
                           act_fp8=self.act_fp8, act_sf=self.act_sf, down=self.down, topk_w=self.topk_w,
-                          src2dst=self.src2dst, out=self.out, T=self.T, E=self.E, k=self.k, H=self.H, I=self.I,
+                          src2dst=self.src2dst, out=self.out if out is None else out, T=self.T, E=self.E, k=self.k, H=self.H, I=self.I,
                           A=self.A, cap=self.cap, w_format=self.gemm1_format, act_kind=self.act_kind,
                           limit=self.limit, rsf=self.rsf, stream=stream, situ=self.situ, act_group=self.group)
 
-    def forward(self, x, logits=None, bias=None, stream=None):
-        """x [T,H] bf16, logits [T,E] fp32 (device) -> self.out [T,H] bf16."""
+    def forward(self, x, logits=None, bias=None, stream=None, out=None):
+        """x [T,H] bf16, logits [T,E] fp32 (device) -> out (default self.out)
+        [T,H] bf16. A caller that overlaps the read-back of one step's output
+        with the next step passes alternating `out` buffers."""
         self.route_scatter(x, logits, bias, stream=stream)
-        self.ffn(stream=stream)
-        return self.out
+        self.ffn(stream=stream, out=out)
+        return self.out if out is None else out

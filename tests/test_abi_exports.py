@@ -62,7 +62,8 @@ def test_host_validation_without_device(lib):
     assert lib.moe_act_quant(None, None, None, None, None, 1, 128, 10, 128, ctypes.byref(p), None) == -1
     assert lib.moe_combine(None, None, 8, None, None, 1, 1, 1.0, None, None) == -1
     assert lib.moe_expert_ends_from_counts(None, None, 4, 128, None, None) == -1
-    assert lib.moe_route_scatter_workspace_size(4096, 32, 6) == 64 * 32 * 4
+    # chunk histograms + the 4-byte completion count, rounded up to 16 bytes
+    assert lib.moe_route_scatter_workspace_size(4096, 32, 6) == 64 * 32 * 4 + 16
     assert lib.moe_route_scatter_workspace_size(-1, 32, 6) == 0
 
 
