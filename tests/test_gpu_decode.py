@@ -126,6 +126,35 @@ def test_decode_tcgen05_batches(ctx, orc, wfmt, T):
 
 
 @WFMTS
+@pytest.mark.parametrize("T", [1, 8, 24])
+def test_decode_plain_gemv_path(ctx, orc, wfmt, T):
+    """The per-(token, slot) GEMV path ([SD] §3) at the gpt-oss shape: forced
+    for T <= 8, and taken by AUTO for T = 24 without a workspace."""
+    d = inputs(T) if T <= 8 else inputs_big(T)
+    ids, w = orc.route_softmax_topk(d.logits, synth.DECODE_K)
+    H = I = synth.DECODE_H
+    path = B.MOE_DECODE_GEMV if T <= 8 else B.MOE_DECODE_AUTO
+    y1, act, y2, out, loc = run_decode(ctx, d, ids, w, wfmt, H, I, 0, synth.DECODE_E, path=path)
+    ry1, ract, ry2, rout = orc.decode(d.x, ids, w, loc, wfmt, I)
+    check_first_gemv(y1, ry1)
+    check_decode_tolerance(out, rout)
+
+
+@WFMTS
+@pytest.mark.parametrize("layout", [B.MOE_GLU_INTERLEAVED, B.MOE_GLU_HALVES], ids=["interleaved", "halves"])
+def test_decode_plain_gemv_small_odd_shape(ctx, orc, wfmt, layout):
+    """H = I = 160 (a multiple of 32, not of 64): only the plain GEMV path
+    applies and AUTO takes it; both GLU layouts; 5 tokens over 8 experts."""
+    T, E, k, H = 5, 8, 4, 160
+    d = synth.decode_inputs(T, E=E, H=H, I=H, seed=77)
+    ids, w = orc.route_softmax_topk(d.logits, k)
+    y1, act, y2, out, loc = run_decode(ctx, d, ids, w, wfmt, H, H, 0, E, glu_layout=layout)
+    ry1, ract, ry2, rout = orc.decode(d.x, ids, w, loc, wfmt, H, interleaved=layout == B.MOE_GLU_INTERLEAVED)
+    check_first_gemv(y1, ry1)
+    check_decode_tolerance(out, rout)
+
+
+@WFMTS
 def test_decode_tcgen05_halves_layout(ctx, orc, wfmt):
     """GLU halves layout: gate rows [0, I), up rows [I, 2I) of w_gu."""
     T = 24
