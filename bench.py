@@ -599,6 +599,38 @@ def actq_microbench(ctx, B, synth, torch, np, hbm, reps=50):
                           "live_rows": live_rows}
     if "full" in res and "dense" in res:
         res["full_over_dense"] = res["full"]["us"] / res["dense"]["us"]
+    # Back to back: 20 launches in a row over 20 device copies of the live-row
+    # input (0.5 GB of live rows in all, so every launch reads HBM), timed
+    # together: the kernel's own time per launch without the per-launch event
+    # and launch overhead of the figures above.
+    gu, counts = synth.actq_inputs(full=False)
+    g0 = torch.from_numpy(gu.view(np.int16)).view(torch.bfloat16).cuda()
+    copies = [g0.clone() for _ in range(20)]
+    del g0
+    out = torch.empty((rows, I), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((I // 512, rows), dtype=torch.int32, device="cuda")
+    ends = torch.empty((E,), dtype=torch.int32, device="cuda")
+    B.moe_expert_ends_from_counts(ctx, torch.from_numpy(counts).cuda(), 128, ends)
+    ts = []
+    for rep in range(6):
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for gc in copies:
+            B.moe_act_quant(ctx, gc, out, sf, ends, E, 128, rows, I)
+        s1.record()
+        torch.cuda.synchronize()
+        if rep >= 1:
+            ts.append(s0.elapsed_time(s1) / len(copies))
+    live_rows = int(counts.sum())
+    nbytes = live_rows * (2 * I * 2 + I + 4 * (I // 512))
+    us = 1e3 * statistics.median(ts)
+    res["live_back_to_back"] = {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9,
+                                "frac_of_hbm": nbytes / (us * 1e-6) / 1e9 / hbm, "live_rows": live_rows,
+                                "launches": len(copies)}
+    del copies
+    torch.cuda.empty_cache()
     return res
 
 
