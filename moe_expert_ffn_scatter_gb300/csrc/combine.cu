@@ -16,11 +16,10 @@ namespace moe {
 
 namespace {
 
-#ifndef MOE_COMBINE_BPS
-#define MOE_COMBINE_BPS 3
-#endif
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
-constexpr int kCombineBlocksPerSm = MOE_COMBINE_BPS;  // grid: one wave of resident blocks
+// Grid: one wave of resident blocks (80 registers per thread: 3 blocks of 256
+// threads per SM; 2 or 4 measured slower).
+constexpr int kCombineBlocksPerSm = 3;
 
 __global__ void __launch_bounds__(256, kCombineBlocksPerSm) combine_kernel(const uint16_t* __restrict__ down, int H,
                                                       const float* __restrict__ topk_w,
