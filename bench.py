@@ -68,6 +68,23 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def max_over_ranks(ms, pg, device="cuda"):
+    """Length of a timed region over all ranks: each rank runs its own replica
+    (no data-path collective), so the job takes as long as its slowest rank."""
+    if not pg:
+        return ms
+    import torch
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_rate(world, units_per_step, steps, ms):
+    """Units processed by all ranks per second over a region of `ms`
+    milliseconds (weak scaling: every rank processes units_per_step)."""
+    return world * units_per_step * steps / (ms / 1e3)
+
+
 def kernel_source_hash():
     import hashlib
     h = hashlib.sha256()
@@ -330,11 +347,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     if pg: pg.barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if pg:
-        tt = torch.tensor([total_ms], device="cuda")
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), pg)
     if B.moe_get_device_error(ctx) != 0:
         raise RuntimeError("device error during the timed region")
     names = ["route_scatter", "gemm1_act", "gemm2", "combine"]
@@ -342,7 +355,7 @@ def run_ours(args):
            for j, n in enumerate(names)}
     ms_step = total_ms / args.steps
     R = cfg.R
-    value = world * R * args.steps / (total_ms / 1e3)
+    value = whole_job_rate(world, R, args.steps, total_ms)
 
     pk, pk_kind = peaks()
     fp8_peak = 2.0 * pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
@@ -434,12 +447,7 @@ def run_ours(args):
                 stream.wait_event(ev)
             a1.record(stream)
             torch.cuda.synchronize()
-            ms = a0.elapsed_time(a1)
-            if pg:
-                tt = torch.tensor([ms], device="cuda")
-                pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-                ms = float(tt.item())
-            return ms
+            return max_over_ranks(a0.elapsed_time(a1), pg)
 
         def run_seq(n):
             for _ in range(n):
@@ -458,12 +466,13 @@ def run_ours(args):
         for oh in ohs[:min(2, args.steps)]:
             if not np.array_equal(oh.view(torch.int16).numpy(), ref_out):
                 raise RuntimeError("pipelined and sequential end-to-end outputs differ")
-        e2e = {"value": world * R * args.steps / (e_ms / 1e3), "unit": UNIT,
+        e2e = {"value": whole_job_rate(world, R, args.steps, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": xh.numel() * 2 + lh.numel() * 4, "d2h_bytes_per_step": ohs[0].numel() * 2,
                "ms_per_step": e_ms / args.steps,
                "pipelined": "upload of step i+1 and read-back of step i on their own streams, overlapping "
                             "step i's compute (double-buffered device inputs/outputs)",
-               "sequential_value": world * R * args.steps / (s_ms / 1e3), "sequential_ms_per_step": s_ms / args.steps,
+               "sequential_value": whole_job_rate(world, R, args.steps, s_ms),
+               "sequential_ms_per_step": s_ms / args.steps,
                "api": "MoEFFNLayer.forward: moe_route_scatter + moe_ffn_forward, pinned host x/logits in, out back"}
 
     extras = {}
