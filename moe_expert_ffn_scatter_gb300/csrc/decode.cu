@@ -478,16 +478,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
           const uint32_t wa = *reinterpret_cast<const uint32_t*>(rowA + 16 * grp + 4 * tig);
           const uint32_t wb = *reinterpret_cast<const uint32_t*>(rowB + 16 * grp + 4 * tig);
           const uint4 xv = *reinterpret_cast<const uint4*>(xg + 2 * (32 * grp + 8 * tig));
-          float e1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, e2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          // both halves of the 32-wide scale group accumulate in one fragment
+          float e1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
           mma_f16(e1, e2m1x2_to_f16x2(wa), e2m1x2_to_f16x2(wb), e2m1x2_to_f16x2(wa >> 8), e2m1x2_to_f16x2(wb >> 8),
                   xv.x, xv.y);
-          mma_f16(e2, e2m1x2_to_f16x2(wa >> 16), e2m1x2_to_f16x2(wb >> 16), e2m1x2_to_f16x2(wa >> 24),
+          mma_f16(e1, e2m1x2_to_f16x2(wa >> 16), e2m1x2_to_f16x2(wb >> 16), e2m1x2_to_f16x2(wa >> 24),
                   e2m1x2_to_f16x2(wb >> 24), xv.z, xv.w);
           const float sA = pow2_f32((int)sfA[grp] - 127), sB = pow2_f32((int)sfB[grp] - 127);
-          d[0] = fmaf(e1[0] + e2[0], sA, d[0]);
-          d[1] = fmaf(e1[1] + e2[1], sA, d[1]);
-          d[2] = fmaf(e1[2] + e2[2], sB, d[2]);
-          d[3] = fmaf(e1[3] + e2[3], sB, d[3]);
+          d[0] = fmaf(e1[0], sA, d[0]);
+          d[1] = fmaf(e1[1], sA, d[1]);
+          d[2] = fmaf(e1[2], sB, d[2]);
+          d[3] = fmaf(e1[3], sB, d[3]);
         }
       }
     }
