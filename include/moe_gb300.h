@@ -141,7 +141,7 @@ typedef struct moe_act_params {
                           call asks for another pair, so calls with different
                           pairs must not overlap on different streams. */
     int32_t quant_group; /* group of the e4m3 result: 128 (also 0), or 32 for
-                            the MXFP8 recipe (next row f4): out_sf is then
+                            the MXFP8 recipe ([DG] §6): out_sf is then
                             [I/128][align4(rows)], four group-32 bytes a word */
 } moe_act_params;
 
@@ -194,7 +194,7 @@ typedef struct moe_route_args {
     size_t workspace_bytes;
     int32_t T, E, k, H, A, cap;
     int32_t quant_group; /* input quantisation group: 128 (also 0), or 32 for
-                            the MXFP8 recipe (next row f4); a_sf then holds
+                            the MXFP8 recipe ([DG] §6); a_sf then holds
                             the four group-32 scale bytes of each 128 columns
                             in one word: [H/128][align4(cap)] */
 } moe_route_args;
@@ -247,7 +247,7 @@ MOE_API int moe_route_scatter_noalloc(moe_ctx* ctx, const moe_route_args* args, 
  * are gate rows 128b..128b+127 and rows 256b+128..256b+255 are up rows
  * I+128b..: every 256-column GEMM tile then holds one matching gate/up group,
  * which lets moe_ffn_forward run SiLU*mul and the quantisation inside GEMM1.
- * FP8 weights (next row f4, [DG] §6 recipes) are prepared with the output
+ * FP8 weights ([DG] §6 recipes) are prepared with the output
  * format MOE_GEMM_W_E4M3 and the input flag MOE_GEMM_W_IN_E4M3: w_in is
  * e4m3 [E][N][K] and is copied (rows reordered with the gate/up flag). Their
  * scales are per (row, 32-K) bytes [E][N][K/32] (MXFP8 recipe), or, with the
@@ -275,8 +275,8 @@ MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t
  *                           * e2m1(w[e,n,k]) 2^(sw(e,n,k/32)-127) )
  * for r in [start[e], expert_ends[e]) only; fp32 accumulation in tensor
  * memory (tcgen05, sm_103a). a [cap,K] e4m3; a_sf ASF [ceil(K/512)][ld_sf],
- * or with the flag MOE_GEMM_A_GROUP32 in w_format (MXFP8 recipe, next row
- * f4: sa(r, k/32)) [K/128][ld_sf], four group-32 bytes per word;
+ * or with the flag MOE_GEMM_A_GROUP32 in w_format (MXFP8 recipe, [DG] §6:
+ * sa(r, k/32)) [K/128][ld_sf], four group-32 bytes per word;
  * w, w_sf prepared by moe_prepare_weights in format w_format ([E][N][K/2]
  * packed e2m1 or [E][N][K] e4m3; scales [E][K/128][N]); out [cap,N] bf16.
  * Requires 1 <= E <= 4096, K % 128 == 0, N % 256 == 0, cap % 128 == 0,

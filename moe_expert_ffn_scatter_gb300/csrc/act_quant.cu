@@ -11,7 +11,7 @@
 // 4w..4w+3. One warp per item, 16 columns per lane (two uint4 loads from the
 // gate half, two from the up half); a group of 128 columns is 8 lanes, its
 // amax a 3-step xor reduction; lane 0 assembles the four scale bytes into the
-// int32 word of the MN-major scale array. SiTU (next row f2) reads gate' and
+// int32 word of the MN-major scale array. SiTU ([DG] §2.4.1) reads gate' and
 // up' from two per-context tables over all bf16 patterns.
 #include "common.cuh"
 #include "kernels.h"

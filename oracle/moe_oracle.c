@@ -465,8 +465,8 @@ void orc_grouped_gemm(const uint8_t* a, const int32_t* a_sf, int ld_sf, int K, i
  * up = gateup[r, I + j] ([DG] §2.4.1, [gate; up] halves); with a clamp limit
  * L the gate is clamped from above and up on both sides ([DG] §2.4.1 default
  * branch: "up 双向钳、gate 只钳上限"); h = silu(gate) * up kept in fp32
- * (silu_mul_keep_fp32), or with SiTU h = gate'(gate) * up'(up) (next row
- * f2, the situ branch of [DG] §2.4.1); then group-128 quantisation with
+ * (silu_mul_keep_fp32), or with SiTU h = gate'(gate) * up'(up) (the situ
+ * branch of [DG] §2.4.1); then group-128 quantisation with
  * packed UE8M0 scales. */
 /* min(a, b) and max(a, b) in which a NaN operand, quiet or signalling, yields
  * the other operand (IEEE minNum / maxNum): the reading taken for the pages'

@@ -132,7 +132,7 @@ def test_every_gate_bit_pattern(ctx, orc, kind, limit):
 
 @pytest.mark.parametrize("betas", [(4.0, 25.0), (1.5, 7.0)], ids=["kimi", "other"])
 def test_situ_microbench_shape_bit_exact(ctx, orc, betas):
-    """SiTU (next row f2) over the live rows: codes and scales bit-exact, the
+    """SiTU ([DG] §2.4.1) over the live rows: codes and scales bit-exact, the
     padding untouched; a second beta pair refills the context's tables."""
     gateup, counts = synth.actq_inputs()
     gateup, live = nan_padding(orc, gateup, counts)
@@ -167,7 +167,7 @@ def test_situ_every_bit_pattern(ctx, orc, half):
 @pytest.mark.parametrize("kind,I", [(B.MOE_ACT_SILU, 2048), (B.MOE_ACT_SILU_CLAMP, 384), (B.MOE_ACT_SITU, 640)],
                          ids=["silu", "clamp_I384", "situ_I640"])
 def test_group32_mxfp8_recipe_bit_exact(ctx, orc, kind, I):
-    """Group-32 e4m3 output (MXFP8 recipe, next row f4): one scale per 32
+    """Group-32 e4m3 output (MXFP8 recipe, [DG] §6): one scale per 32
     columns, four per word; live rows only, padding untouched."""
     g = np.random.default_rng(I)
     counts = np.array([100, 0, 37, 260], np.int32)

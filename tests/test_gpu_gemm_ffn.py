@@ -116,7 +116,7 @@ def test_gemm_no_live_rows(ctx, orc):
 
 @pytest.mark.parametrize("recipe", ["mxfp8", "fp8_block128"])
 def test_gemm_fp8_weight_recipes(ctx, orc, recipe):
-    """FP8 weights (next row f4): e4m3 with per-32 scales and group-32 A
+    """FP8 weights ([DG] §6 recipes): e4m3 with per-32 scales and group-32 A
     scales (MXFP8), or with 128 x 128 block scales (FP8 block128), prepared
     from their canonical layouts; against the oracle within the fp32
     accumulation bound, padding rows untouched."""
@@ -260,7 +260,7 @@ def test_fused_act_quant_equals_separate_kernel(ctx, act, fmt):
 @pytest.mark.parametrize("recipe", ["mxfp8", "fp8_block128"])
 @pytest.mark.parametrize("fused", [False, True], ids=["unfused", "fused"])
 def test_tiny_layer_fp8_recipes_vs_oracle(ctx, orc, recipe, fused):
-    """The whole layer under the FP8 recipes of next row f4."""
+    """The whole layer under the FP8 recipes of [DG] §6."""
     cfg = synth.FFNConfig("tiny fp8", T=96, E=4, k=2, H=256, I=256, seed=18)
     inp = synth.ffn_inputs(cfg, weights=False)
     g = np.random.default_rng(19)
@@ -289,7 +289,7 @@ def test_tiny_layer_fp8_recipes_vs_oracle(ctx, orc, recipe, fused):
 
 
 def test_tiny_layer_situ_vs_oracle(ctx, orc):
-    """Layer with the SiTU activation (next row f2), fused GEMM1 epilogue."""
+    """Layer with the SiTU activation ([DG] §2.4.1), fused GEMM1 epilogue."""
     cfg = synth.FFNConfig("tiny situ", T=64, E=4, k=2, H=256, I=128, seed=16)
     inp = synth.ffn_inputs(cfg)
     layer = make_layer(ctx, cfg, inp, act_kind=B.MOE_ACT_SITU)

@@ -138,7 +138,7 @@ def test_topk_selection_edge_cases(ctx, orc, name, logits, k, bias):
 
 @pytest.mark.parametrize("H", [256, 384, 4096])
 def test_scatter_group32_mxfp8_recipe(ctx, orc, H):
-    """Input quantisation with group 32 (MXFP8 recipe, next row f4): codes and
+    """Input quantisation with group 32 (MXFP8 recipe, [DG] §6): codes and
     the four-bytes-a-word scale array bit-exact, padding untouched; H = 384
     leaves half a 256-column pass."""
     g = np.random.default_rng(H)
