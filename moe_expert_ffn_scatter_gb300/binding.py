@@ -141,9 +141,18 @@ def _check(name, status):
 
 
 def ptr(t):
-    """Device (or host) pointer of a tensor; None passes NULL."""
+    """Device pointer of a CUDA tensor; None passes NULL.
+
+    Every buffer the library takes is a dense device array, so a host tensor
+    (whose address a kernel cannot dereference) or a strided view (whose
+    elements are not where the library reads them) is refused here, before
+    anything is enqueued."""
     if t is None:
         return None
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor, got shape {tuple(t.shape)} strides {t.stride()}")
     return t.data_ptr()
 
 

@@ -19,6 +19,16 @@ def ceil_div(a, b):
     return (a + b - 1) // b
 
 
+def _expect(name, t, shape, dtype, device):
+    """The library sees only pointers, so a caller buffer of the wrong size or
+    type would be read or written past its end on the device: refuse it here."""
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device:
+        raise ValueError(f"{name}: expected {tuple(shape)} {dtype} on {device}, "
+                         f"got {tuple(t.shape)} {t.dtype} on {t.device}")
+
+
 class MoEFFNLayer:
     def __init__(self, ctx, *, T, E, k, H, I, A=128, cap=None, routing=B.MOE_ROUTE_SOFTMAX_TOPK,
                  act_kind=B.MOE_ACT_SILU, limit=0.0, rsf=1.0, w_format=B.MOE_GEMM_W_E2M1, fused=True,
@@ -30,7 +40,8 @@ class MoEFFNLayer:
         activations; w_format E4M3 widens the weights), "mxfp8" (e4m3 weights
         with per-32 scales, group-32 activations) or "fp8_block128" (e4m3
         weights with one scale per 128 x 128 block, group-128 activations)."""
-        assert recipe in ("mxfp4", "mxfp8", "fp8_block128")
+        if recipe not in ("mxfp4", "mxfp8", "fp8_block128"):
+            raise ValueError(f"unknown recipe {recipe!r}")
         self.ctx = ctx
         self.T, self.E, self.k, self.H, self.I, self.A = T, E, k, H, I, A
         if cap is None:
@@ -120,6 +131,15 @@ class MoEFFNLayer:
 
     # ------------------------------------------------------------------ steps
     def route_scatter(self, x, logits=None, bias=None, stream=None):
+        """x [T,H] bf16; logits [T,E] fp32 unless the routing is precomputed
+        (then topk_ids / topk_w are filled by the caller); bias [E] fp32 for
+        sigmoid routing with correction bias."""
+        dev = self.out.device
+        _expect("x", x, (self.T, self.H), torch.bfloat16, dev)
+        if self.routing != B.MOE_ROUTE_PRECOMPUTED:
+            _expect("logits", logits, (self.T, self.E), torch.float32, dev)
+        if self.routing == B.MOE_ROUTE_SIGMOID_BIAS_TOPK and bias is not None:
+            _expect("bias", bias, (self.E,), torch.float32, dev)
         B.moe_route_scatter(self.ctx, routing_mode=self.routing, x=x, logits=logits, corr_bias=bias,
                             topk_ids=self.topk_ids, topk_w=self.topk_w, expert_ends=self.expert_ends,
                             src2dst=self.src2dst, a_fp8=self.a_fp8, a_sf=self.a_sf, workspace=self.ws,
@@ -128,10 +148,15 @@ class MoEFFNLayer:
 
     def ffn(self, stream=None, out=None):
         """out: [T,H] bf16 device buffer for the result (default self.out)."""
+        if out is None:
+            out = self.out
+        _expect("out", out, (self.T, self.H), torch.bfloat16, self.out.device)
+        if self.w13 is None:
+            raise RuntimeError("load_weights() has not been called")
         B.moe_ffn_forward(self.ctx, a_fp8=self.a_fp8, a_sf=self.a_sf, expert_ends=self.expert_ends, w13=self.w13,
                           w13_sf=self.w13_sf, w2=self.w2, w2_sf=self.w2_sf, gateup=self.gateup,
                           act_fp8=self.act_fp8, act_sf=self.act_sf, down=self.down, topk_w=self.topk_w,
-                          src2dst=self.src2dst, out=self.out if out is None else out, T=self.T, E=self.E, k=self.k, H=self.H, I=self.I,
+                          src2dst=self.src2dst, out=out, T=self.T, E=self.E, k=self.k, H=self.H, I=self.I,
                           A=self.A, cap=self.cap, w_format=self.gemm1_format, act_kind=self.act_kind,
                           limit=self.limit, rsf=self.rsf, stream=stream, situ=self.situ, act_group=self.group)
 

@@ -89,3 +89,28 @@ def test_struct_layouts_match_header(tmp_path):
         assert int(got[name]) == ctypes.sizeof(cls), name
         for fname, _ in cls._fields_:
             assert int(got["%s.%s" % (name, fname)]) == getattr(cls, fname).offset, (name, fname)
+
+
+def test_binding_refuses_host_and_strided_tensors():
+    """The binding hands only device pointers into dense buffers to the
+    library: a host tensor or a strided view is refused before any call."""
+    import torch
+
+    assert B.ptr(None) is None
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        B.ptr(torch.zeros(16, dtype=torch.int32))
+
+
+def test_layer_buffer_checks():
+    """The layer checks caller tensors' shapes and dtypes (the library sees
+    only pointers, so a short buffer would be overrun on the device)."""
+    import torch
+    from moe_expert_ffn_scatter_gb300.layer import _expect
+
+    cpu = torch.device("cpu")
+    _expect("x", torch.zeros((4, 8), dtype=torch.bfloat16), (4, 8), torch.bfloat16, cpu)
+    for bad in (torch.zeros((4, 7), dtype=torch.bfloat16), torch.zeros((4, 8), dtype=torch.float32)):
+        with pytest.raises(ValueError, match="x: expected"):
+            _expect("x", bad, (4, 8), torch.bfloat16, cpu)
+    with pytest.raises(ValueError, match="required"):
+        _expect("logits", None, (4, 2), torch.float32, cpu)
