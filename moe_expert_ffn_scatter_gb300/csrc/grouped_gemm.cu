@@ -64,9 +64,11 @@ constexpr uint32_t OFF_BAR = OFF_SFA_IN + STAGES * SFA_BYTES;
 constexpr uint32_t NUM_BARS = 3 * STAGES + 3;
 constexpr uint32_t OFF_TMEM_PTR = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_PTR + 4;
-constexpr uint32_t OFF_ENDS = OFF_ABORT + 12;                   // expert_ends copy, 16-byte aligned
+constexpr uint32_t OFF_ENDS = OFF_ABORT + 12;                   // expert_ends copy
 constexpr int kMaxExperts = 4096;
-constexpr uint32_t SMEM_USED = OFF_ENDS + kMaxExperts * 4;
+constexpr uint32_t STG_BYTES = 2048;                              // per epilogue warp: 32 rows x 64 bytes
+constexpr uint32_t OFF_STG = (OFF_ENDS + kMaxExperts * 4 + 15) / 16 * 16;
+constexpr uint32_t SMEM_USED = OFF_STG + 4 * STG_BYTES;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = 256;             // stage s: SFA cols 256+16s, SFB cols 264+16s
@@ -92,6 +94,34 @@ __device__ __forceinline__ int expert_of_tile(const int32_t* ends, int E, int m0
     if ((int)align_up64(ends[mid], BM) > m0) hi = mid; else lo = mid + 1;
   }
   return lo;
+}
+
+// Stores 64 bytes of each of the warp's 32 rows: lane r holds row r's four
+// 16-byte units in u, row r goes to dst + r * ld (bytes), and rows r >= nrows
+// are not written. The rows pass through the warp's staging buffer so that
+// each global store instruction covers 64 contiguous bytes of 8 rows, where a
+// direct store from the row-per-lane layout touches 32 rows. Unit j of row r
+// sits at 16 * (j ^ ((r >> 1) & 3)) in its row: the writes and the reads are
+// both free of bank conflicts.
+__device__ __forceinline__ void store_rows64(uint32_t stg, int lane, const uint32_t (&u)[16], uint8_t* dst,
+                                             size_t ld, int nrows) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)),
+                 "r"(u[4 * j]), "r"(u[4 * j + 1]), "r"(u[4 * j + 2]), "r"(u[4 * j + 3])
+                 : "memory");
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = 8 * k + (lane >> 2), j = lane & 3;
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(stg + r * 64 + ((j ^ ((r >> 1) & 3)) << 4))
+                 : "memory");
+    if (r < nrows) *reinterpret_cast<uint4*>(dst + (size_t)r * ld + 16 * j) = v;
+  }
+  __syncwarp();
 }
 
 // Epilogue kinds: bf16 output, or (GEMM1 with gate/up rows interleaved in
@@ -283,13 +313,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty_bar);
-      const int row = m0 + 32 * q + lane;
+      const int rbase = m0 + 32 * q;  // the warp's first row
+      const int row = rbase + lane;
+      const uint32_t stg = sbase + OFF_STG + q * STG_BYTES;
       if (kEpi == kEpiBf16) {
-        if (row < row_end) {
-          uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * N + n0);
+        // 32 columns (64 bytes) of the warp's rows at a time
 #pragma unroll
-          for (int i = 0; i < BN / 8; ++i)
-            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t u[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) u[i] = packed[16 * c + i];
+          store_rows64(stg, lane, u, reinterpret_cast<uint8_t*>(out + (size_t)rbase * N + n0 + 32 * c),
+                       (size_t)N * 2, row_end - rbase);
         }
       } else {
         // This thread holds its row's gate (columns 0-127) and up (128-255)
@@ -332,22 +367,28 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
 #pragma unroll
           for (int j = 0; j < 4; ++j) bq[j] = b;
         }
-        if (row < row_end) {
-          uint4* dst = reinterpret_cast<uint4*>(out_q + (size_t)row * I + (size_t)grp * 128);
+        // the 128 e4m3 codes of the row, 64 bytes (4 x 16 codes) at a time;
+        // every lane takes part in the staging, rows past the end are not stored
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t u[16];
+#pragma unroll
+          for (int vv = 0; vv < 4; ++vv) {
+            const int v = 4 * hb + vv;
             const float sc = pow2_f32(127 - (int)bq[v >> 1]);
-            uint32_t wq[4];
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
               const int j = 16 * v + 4 * w;  // h[j] = packed[j/2] (j even), packed[64 + j/2] (j odd)
               const float h0 = __uint_as_float(packed[j / 2]), h1 = __uint_as_float(packed[64 + j / 2]);
               const float h2 = __uint_as_float(packed[j / 2 + 1]), h3 = __uint_as_float(packed[64 + j / 2 + 1]);
-              wq[w] = e4m3x2_satfinite(__fmul_rn(h0, sc), __fmul_rn(h1, sc)) |
-                      (e4m3x2_satfinite(__fmul_rn(h2, sc), __fmul_rn(h3, sc)) << 16);
+              u[4 * vv + w] = e4m3x2_satfinite(__fmul_rn(h0, sc), __fmul_rn(h1, sc)) |
+                              (e4m3x2_satfinite(__fmul_rn(h2, sc), __fmul_rn(h3, sc)) << 16);
             }
-            dst[v] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
           }
+          store_rows64(stg, lane, u, out_q + (size_t)rbase * I + (size_t)grp * 128 + 64 * hb, (size_t)I,
+                       row_end - rbase);
+        }
+        if (row < row_end) {
           if (out_g32) {
             out_sf[(size_t)grp * ld_out_sf + row] = (int32_t)(bq[0] | (bq[1] << 8) | (bq[2] << 16) | (bq[3] << 24));
           } else {
