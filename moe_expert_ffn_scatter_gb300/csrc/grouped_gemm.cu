@@ -64,11 +64,16 @@ constexpr uint32_t OFF_BAR = OFF_SFA_IN + STAGES * SFA_BYTES;
 constexpr uint32_t NUM_BARS = 3 * STAGES + 3;
 constexpr uint32_t OFF_TMEM_PTR = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_PTR + 4;
-constexpr uint32_t OFF_ENDS = OFF_ABORT + 12;                   // expert_ends copy
-constexpr int kMaxExperts = 4096;
+constexpr uint32_t OFF_ENDS = OFF_ABORT + 12;                   // expert_ends copy (E <= kSmemExperts)
+constexpr int kSmemExperts = 1024;
 constexpr uint32_t STG_BYTES = 2048;                              // per epilogue warp: 32 rows x 64 bytes
-constexpr uint32_t OFF_STG = (OFF_ENDS + kMaxExperts * 4 + 15) / 16 * 16;
-constexpr uint32_t SMEM_USED = OFF_STG + 4 * STG_BYTES;
+constexpr uint32_t OFF_STG = (OFF_ENDS + kSmemExperts * 4 + 15) / 16 * 16;
+// SiLU window: the table entries of the bf16 gate values with |g| in
+// [2^-6, 2^6) (exponent field 121..132), positive then negative, 1536 each.
+constexpr uint32_t kWinBase = 121u << 7;  // bits 0x3C80
+constexpr uint32_t kWinHalf = 12u * 128u;
+constexpr uint32_t OFF_WIN = OFF_STG + 4 * STG_BYTES;
+constexpr uint32_t SMEM_USED = OFF_WIN + 2 * kWinHalf * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = 256;             // stage s: SFA cols 256+16s, SFB cols 264+16s
@@ -94,6 +99,15 @@ __device__ __forceinline__ int expert_of_tile(const int32_t* ends, int E, int m0
     if ((int)align_up64(ends[mid], BM) > m0) hi = mid; else lo = mid + 1;
   }
   return lo;
+}
+
+// SiLU of the bf16 gate value with bits `bits` (low 16): from the shared
+// window when |g| lies in it, else from the per-context table in global memory.
+__device__ __forceinline__ float silu_windowed(const float* win, const float* __restrict__ tbl, uint32_t bits) {
+  const uint32_t b = bits & 0xFFFFu;
+  const uint32_t off = (b & 0x7FFFu) - kWinBase;
+  if (off < kWinHalf) return win[off + ((b & 0x8000u) ? kWinHalf : 0u)];
+  return __ldg(tbl + b);
 }
 
 // Stores 64 bytes of each of the warp's 32 rows: lane r holds row r's four
@@ -151,8 +165,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   const uint32_t tmem_empty_bar = bar0 + 8u * (3 * STAGES + 1);
   const uint32_t done_bar = bar0 + 8u * (3 * STAGES + 2);
 
-  int32_t* ends_s = reinterpret_cast<int32_t*>(smem + OFF_ENDS);
-  for (int i = threadIdx.x; i < E; i += blockDim.x) ends_s[i] = __ldg(ends + i);
+  // The endpoints, from a shared copy when they fit, else from global memory.
+  const int32_t* ends_s = ends;
+  if (E <= kSmemExperts) {
+    int32_t* copy = reinterpret_cast<int32_t*>(smem + OFF_ENDS);
+    for (int i = threadIdx.x; i < E; i += blockDim.x) copy[i] = __ldg(ends + i);
+    ends_s = copy;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 2);   // producer's expect_tx arrive + scale transposer's arrive
@@ -290,6 +309,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     // ------------------------------------------------------ epilogue
     const int q = warp & 3;
     const float silu_limit = (kEpi == kEpiSiluClamp) ? spec_silu(limit) : 0.0f;
+    // The epilogue warps fill the SiLU window (the single-warp-per-scheduler
+    // epilogue waits out every table lookup; shared memory answers far sooner
+    // than the small L1 left beside this kernel's shared memory).
+    float* win = reinterpret_cast<float*>(smem + OFF_WIN);
+    if (kEpi == kEpiSilu || kEpi == kEpiSiluClamp) {
+      for (int i = threadIdx.x - 128; i < (int)(2 * kWinHalf); i += 128)
+        win[i] = __ldg(silu_tbl + (i < (int)kWinHalf ? kWinBase + i : 0x8000u + kWinBase + (i - kWinHalf)));
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+    }
     uint32_t acc_ph = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
@@ -349,8 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
               ua = fminf(fmaxf(ua, -limit), limit);
               ub = fminf(fmaxf(ub, -limit), limit);
             }
-            sa = silu_of_bf16<kEpi == kEpiSiluClamp>(silu_tbl, packed[i], ga, limit, silu_limit);
-            sb = silu_of_bf16<kEpi == kEpiSiluClamp>(silu_tbl, packed[i] >> 16, gb, limit, silu_limit);
+            // with the clamp, gate values above the limit (or NaN) take spec_silu(limit)
+            const bool over_a = kEpi == kEpiSiluClamp && !(ga <= limit) && !isnan(limit);
+            const bool over_b = kEpi == kEpiSiluClamp && !(gb <= limit) && !isnan(limit);
+            sa = over_a ? silu_limit : silu_windowed(win, silu_tbl, packed[i]);
+            sb = over_b ? silu_limit : silu_windowed(win, silu_tbl, packed[i] >> 16);
           }
           const float2 hh = mul2(make_float2(sa, sb), make_float2(ua, ub));
           packed[i] = __float_as_uint(hh.x);       // h[2i]

@@ -109,6 +109,15 @@ def test_gemm_many_tiles_persistent(ctx, orc):
     assert assert_gemm_close(got, ref, ends, ab) > 0.99
 
 
+def test_gemm_more_experts_than_the_shared_endpoint_copy(ctx, orc):
+    """E = 1100: the tile search reads the endpoints from global memory (the
+    shared copy holds 1024); live experts on both sides of index 1024."""
+    counts = np.zeros(1100, np.int32)
+    counts[[3, 1023, 1024, 1099]] = [40, 130, 1, 77]
+    got, ref, ends, ab = gemm_case(ctx, orc, counts, 256, 128, B.MOE_GEMM_W_E2M1, seed=6)
+    assert assert_gemm_close(got, ref, ends, ab) > 0.99
+
+
 def test_gemm_no_live_rows(ctx, orc):
     got = gemm_case(ctx, orc, [0, 0], 256, 128, B.MOE_GEMM_W_E2M1, cap=256)[0]
     assert np.all(got == 0xABAB)
@@ -255,6 +264,40 @@ def test_fused_act_quant_equals_separate_kernel(ctx, act, fmt):
     assert np.array_equal(o0, o1)
     live = live_rows(e0, cfg.cap)
     assert np.all(a1[~live] == 0xAB)
+
+
+@pytest.mark.parametrize("act", ["silu", "silu_clamp"])
+def test_fused_silu_across_gate_magnitudes(ctx, act):
+    """The fused epilogue reads SiLU from a shared-memory window for
+    |g| in [2^-6, 2^6) and from the full table otherwise. Weight rows scaled by
+    2^-24 .. 2^8 put gate values below, inside and above the window; the fused
+    layer must still equal the unfused one (GEMM1 -> bf16 -> act-quant) bit for
+    bit."""
+    clamp = act == "silu_clamp"
+    cfg = synth.FFNConfig("gate range", T=512, E=4, k=2, H=256, I=256, seed=21, clamp=clamp,
+                          limit=2.5 if clamp else 0.0)
+    inp = synth.ffn_inputs(cfg)
+    g = np.random.default_rng(22)
+    row_exp = g.integers(-24, 9, size=(cfg.E, 2 * cfg.I, 1))
+    w13_sf = np.broadcast_to(127 + row_exp, inp.w13_sf.shape).astype(np.uint8).copy()
+    inp = type(inp)(inp.x, inp.logits, inp.bias, inp.w13, w13_sf, inp.w2, inp.w2_sf)
+    res = []
+    for fused in (False, True):
+        layer = make_layer(ctx, cfg, inp, fused=fused)
+        layer.act_fp8.fill_(0xAB)
+        layer.act_sf.view(torch.uint8).fill_(0xAB)
+        layer.forward(dev_bf16(inp.x), dev(inp.logits))
+        torch.cuda.synchronize()
+        assert B.moe_get_device_error(ctx) == 0
+        if not fused:
+            ends = host(layer.expert_ends).copy()
+            gate = bf16_bits_to_f64(host_u16(layer.gateup)[live_rows(ends, cfg.cap), :cfg.I])
+            mag = np.abs(gate[gate != 0])
+            assert (mag < 2.0 ** -6).any() and (mag >= 2.0 ** 6).any()
+            assert ((mag >= 2.0 ** -6) & (mag < 2.0 ** 6)).any()
+        res.append((host(layer.act_fp8).copy(), host(layer.act_sf).copy(), host_u16(layer.out).copy()))
+    for a, b in zip(*res):
+        assert np.array_equal(a, b)
 
 
 @pytest.mark.parametrize("recipe", ["mxfp8", "fp8_block128"])
