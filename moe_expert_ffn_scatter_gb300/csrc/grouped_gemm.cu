@@ -28,8 +28,11 @@
 //             words of each stage into that tcgen05.cp source layout
 //             (shared -> shared), then completes the stage's full barrier.
 //   warps 4-7 epilogue: tcgen05.ld of the accumulator (each warp its 32-lane
-//             quarter), bf16 conversion into registers, accumulator released,
-//             then row-masked 16-byte stores (rows >= end[e] are skipped).
+//             quarter), bf16 conversion into registers, accumulator released;
+//             then (GEMM1 fused) SiLU from a shared-memory window of the table,
+//             times up, and the e4m3/UE8M0 quantisation; the rows go out through
+//             a 2 KB per-warp shared buffer, 64 contiguous bytes of 8 rows per
+//             store instruction (rows >= end[e] are skipped).
 // The tile list is (live 128-row tile, 256-column tile); the number of live
 // tiles, align_up(end[E-1], 128) / 128, and each tile's expert come from the
 // device-side endpoint tensor, so the grid never depends on routing counts.
