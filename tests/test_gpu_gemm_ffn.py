@@ -266,10 +266,11 @@ def test_fused_act_quant_equals_separate_kernel(ctx, act, fmt):
     assert np.all(a1[~live] == 0xAB)
 
 
-@pytest.mark.parametrize("act", ["silu", "silu_clamp"])
+@pytest.mark.parametrize("act", ["silu", "silu_clamp", "situ"])
 def test_fused_silu_across_gate_magnitudes(ctx, act):
     """The fused epilogue reads SiLU from a shared-memory window for
-    |g| in [2^-6, 2^6) and from the full table otherwise. Weight rows scaled by
+    |g| in [2^-6, 2^6) and from the full table otherwise (SiTU reads its
+    tables in global memory). Weight rows scaled by
     2^-24 .. 2^8 put gate values below, inside and above the window; the fused
     layer must still equal the unfused one (GEMM1 -> bf16 -> act-quant) bit for
     bit."""
@@ -283,7 +284,7 @@ def test_fused_silu_across_gate_magnitudes(ctx, act):
     inp = type(inp)(inp.x, inp.logits, inp.bias, inp.w13, w13_sf, inp.w2, inp.w2_sf)
     res = []
     for fused in (False, True):
-        layer = make_layer(ctx, cfg, inp, fused=fused)
+        layer = make_layer(ctx, cfg, inp, fused=fused, act_kind=B.MOE_ACT_SITU if act == "situ" else None)
         layer.act_fp8.fill_(0xAB)
         layer.act_sf.view(torch.uint8).fill_(0xAB)
         layer.forward(dev_bf16(inp.x), dev(inp.logits))
