@@ -9,8 +9,9 @@ Every function is a direct wrapper over the C function of the same name
 without the ``orc_`` prefix; see oracle/moe_oracle.c for the definitions and
 the page sections they restate.
 
-Parity unpinned: ``glu_oai`` (the gpt-oss GLU formula of the decode path; the
-pages give its parameters only).
+Parity partly unpinned: ``glu_oai`` (the gpt-oss GLU of the decode path). Its
+clamp and the place of alpha are pinned by ``tests/test_oracle_glu.py``; where
+beta enters is a reading that no page fixes.
 """
 import ctypes
 import os

@@ -656,8 +656,10 @@ void orc_ffn_dense(const uint16_t* x, int T, int H, int I, const int32_t* ids, c
  * with one fp32 scale per expert; wfmt 1: MXFP4 [E,N,K/2] with UE8M0
  * group-32 scales [E,N,K/32]. Intermediates y1, act, y2 are bf16.
  *
- * GLU (parity unpinned: the pages give only the parameters alpha=1.702,
- * beta=1, limit=7 and the interleaved layout, [KM] Phase 1 差异矩阵):
+ * GLU (parameters alpha=1.702, beta=1, limit=7 and the interleaved layout,
+ * [KM] Phase 1 差异矩阵). [DG] §2.4.1 clamps up on both sides and the gate
+ * from above only; [DG] §2.1.3 makes alpha the scale of the SiLU part. Where
+ * beta enters is a reading (parity unpinned for that part):
  *   g = min(g, L); u = clamp(u, -L, L); act = (g * sigmoid(alpha g)) * (u + beta). */
 float orc_glu_oai(float g, float u, float alpha, float beta, float limit) {
     if (limit > 0.0f) { g = min_num(g, limit); u = min_num(max_num(u, -limit), limit); }

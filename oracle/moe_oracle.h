@@ -6,8 +6,9 @@
  * check and the benchmark's CPU-baseline leg load it; the CUDA library never
  * includes this header, never links this code and shares no helper with it.
  *
- * Parity unpinned (no page fixes them, see the per-function notes):
- *   - orc_glu_oai: the gpt-oss GLU formula used by the decode path.
+ * Parity partly unpinned (see the per-function notes):
+ *   - orc_glu_oai: the gpt-oss GLU of the decode path; its clamp and the
+ *     place of alpha are pinned, the place of beta is a reading.
  *
  * Conventions
  *   bf16 values travel as uint16_t bit patterns; fp8-e4m3 codes as uint8_t;
