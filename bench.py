@@ -115,8 +115,75 @@ def workload_config(cfg):
 
 
 # ----------------------------------------------------------------- clocks
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (the driver's
+    libnvidia-ml, read-only queries) on a background thread every ~2 ms, so
+    that even a timed region of a few milliseconds holds several samples.
+    start()/stop() bracket the timed region itself."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, device):
+        import ctypes
+        import threading
+        self.ct, self.threading = ctypes, threading
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        # the CUDA device's PCI address: NVML numbers the GPUs on its own
+        import torch
+        props = torch.cuda.get_device_properties(device)
+        if all(hasattr(props, f) for f in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+            bus = b"%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.h))
+        else:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(int(device), ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError("no NVML handle for device %d" % device)
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.rows, self.run, self.thread = [], False, None
+
+    def _sample(self):
+        ct = self.ct
+        clk, mx, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        ok = self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk)) == 0  # NVML_CLOCK_SM
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
+        self.reasons_fn(self.h, ct.byref(rs))
+        if ok:
+            self.rows.append((clk.value, mx.value, rs.value))
+
+    def _loop(self):
+        while self.run:
+            self._sample()
+            time.sleep(0.002)
+
+    def start(self):
+        self.rows, self.run = [], True
+        self.thread = self.threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.run = False
+        self.thread.join()
+        self._sample()  # at least one reading taken as the region ends
+        sm = [r[0] for r in self.rows]
+        reasons = sorted({n for r in self.rows for bit, n in self.REASONS.items() if r[2] & bit})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in self.rows),
+                "reasons": reasons, "samples": len(self.rows), "source": "NVML, every ~2 ms inside the timed region"}
+
+
+def clock_sampler(device):
+    try:
+        return NvmlClockSampler(device)
+    except (OSError, AttributeError):
+        return ClockSampler(device)
+
+
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """Fallback: nvidia-smi every 20 ms; only the samples stamped inside the
+    timed region count."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -131,29 +198,40 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.device), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        time.sleep(0.3)  # nvidia-smi start-up; its samples before the region are dropped below
+        self.t0 = time.time()
 
     def stop(self):
+        t1 = time.time()
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.05)
         self.proc.terminate()
         self.proc.wait()
         rows = []
+        import datetime
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) == 9:
-                rows.append(parts)
+            if len(parts) != 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if self.t0 <= ts <= t1:
+                rows.append(parts[1:])
         os.unlink(self.path)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no sample inside the timed region"]}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "source": "nvidia-smi, every 20 ms inside the timed region"}
 
 
 # ------------------------------------------------------------ CPU baseline
@@ -335,11 +413,10 @@ def run_ours(args):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
+    clocks = clock_sampler(local)
     if pg: pg.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
     t_start.record(stream)
     for i in range(args.steps):
         step(evs[i])
