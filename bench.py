@@ -167,6 +167,7 @@ class NvmlClockSampler:
         self.run = False
         self.thread.join()
         self._sample()  # at least one reading taken as the region ends
+        self.lib.nvmlShutdown()
         sm = [r[0] for r in self.rows]
         reasons = sorted({n for r in self.rows for bit, n in self.REASONS.items() if r[2] & bit})
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in self.rows),
