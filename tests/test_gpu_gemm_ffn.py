@@ -332,6 +332,40 @@ def test_tiny_layer_fp8_recipes_vs_oracle(ctx, orc, recipe, fused):
     check_ffn_tolerance(host_u16(out), ref)
 
 
+def test_fused_layer_with_more_experts_than_the_shared_endpoint_copy(ctx, orc):
+    """E = 1100 experts (the GEMM's shared endpoint copy holds 1024, so the tile
+    search reads global memory), routing given for experts on both sides of
+    index 1024: the fused layer equals the unfused one bit for bit, and its
+    output stays within the FFN tolerance of the oracle."""
+    E, T, k, H, I = 1100, 64, 2, 256, 128
+    g = np.random.default_rng(31)
+    pool = np.array([5, 600, 1023, 1024, 1050, 1099], np.int32)
+    ids = np.stack([g.choice(pool, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    w = g.uniform(0.2, 1.0, size=(T, k)).astype(np.float32)
+    w /= w.sum(axis=1, keepdims=True)
+    x = synth.bf16_normal(g, (T, H))
+    w13 = synth.e2m1_packed(g, (E, 2 * I, H // 2))
+    w13_sf = synth.ue8m0_bytes(g, (E, 2 * I, H // 32))
+    w2 = synth.e2m1_packed(g, (E, H, I // 2))
+    w2_sf = synth.ue8m0_bytes(g, (E, H, I // 32))
+    res = []
+    for fused in (False, True):
+        layer = MoEFFNLayer(ctx, T=T, E=E, k=k, H=H, I=I, routing=B.MOE_ROUTE_PRECOMPUTED, fused=fused)
+        layer.load_weights(w13, w13_sf, w2, w2_sf)
+        layer.topk_ids.copy_(torch.from_numpy(ids))
+        layer.topk_w.copy_(torch.from_numpy(w))
+        layer.act_fp8.fill_(0xAB)
+        layer.act_sf.view(torch.uint8).fill_(0xAB)
+        out = layer.forward(dev_bf16(x))
+        torch.cuda.synchronize()
+        assert B.moe_get_device_error(ctx) == 0
+        res.append((host(layer.act_fp8).copy(), host(layer.act_sf).copy(), host_u16(out).copy()))
+    for a_, b_ in zip(*res):
+        assert np.array_equal(a_, b_)
+    ref = orc.ffn_tokens(x, ids, w, w13, w13_sf, w2, w2_sf, np.arange(T, dtype=np.int32))
+    check_ffn_tolerance(res[1][2], ref)
+
+
 def test_tiny_layer_situ_vs_oracle(ctx, orc):
     """Layer with the SiTU activation ([DG] §2.4.1), fused GEMM1 epilogue."""
     cfg = synth.FFNConfig("tiny situ", T=64, E=4, k=2, H=256, I=128, seed=16)
