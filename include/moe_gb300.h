@@ -214,19 +214,21 @@ MOE_API int moe_route_scatter(moe_ctx* ctx, const moe_route_args* args, moe_stre
  * Same operation, arguments, results and errors as moe_route_scatter, except
  * that args->workspace and args->workspace_bytes are ignored: the scratch (the
  * per-chunk expert histograms, ceil(T/64) * E int32, and a 4-byte completion
- * count) lives in a device array of 1 MiB + 16 bytes inside the library. Every
- * GPU that loads the library holds that array until the process exits.
+ * count) lives in a device array of 1 MiB + 16 bytes inside the library.
  * Limit: ceil(T/64) * E * 4 <= 1 MiB (T <= 4096 with
  * any E <= 4096; T = 65536 with E <= 256); larger sizes return
- * MOE_ERR_UNSUPPORTED. Allocates nothing.
+ * MOE_ERR_UNSUPPORTED. The call allocates nothing.
  *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) and caches it: make that first call before any stream
- * capture. All calls share the one array: calls that may overlap on the GPU
- * (on different streams, or from different threads, without ordering between
- * them) race and give wrong results; order them. Nothing in the array needs
- * clearing between calls: each call writes every histogram entry before
- * reading it. */
+ * The array belongs to the library's device code: it comes into being on a
+ * GPU when that code is loaded there. moe_ctx_create loads it and looks up the
+ * array's device address on the context's device (cudaGetSymbolAddress), so
+ * the array exists from the context's creation on and stays until the process
+ * exits; this entry point itself does no set-up. All calls share the one
+ * array: calls that may overlap on the GPU (on different streams, or from
+ * different threads, without ordering between them) race and give wrong
+ * results; order them. Nothing in the array needs clearing between calls:
+ * each call writes every histogram entry before reading it, and zeroes the
+ * completion count before the launch that counts in it. */
 MOE_API int moe_route_scatter_noalloc(moe_ctx* ctx, const moe_route_args* args, moe_stream_t stream);
 
 /* ------------------------------------------------------- weight prepare

@@ -16,6 +16,7 @@ struct moe_ctx {
   float* d_silu;  // 65,536-entry SiLU table of the exp/SiLU specification
   float* d_situ;  // 2 x 65,536-entry SiTU tables (gate', up') for situ_bs / situ_bl
   float situ_bs, situ_bl;
+  void* d_route_scratch;  // device address of the built-in scratch of moe_route_scatter_noalloc
   moe::EncodeTiledFn encode;
 };
 
@@ -103,6 +104,7 @@ MOE_API int moe_ctx_create(moe_ctx** out, int device) {
       cudaMemset(c->d_err, 0, sizeof(uint32_t)) != cudaSuccess ||
       moe::launch_silu_table(c->d_silu, 0) != cudaSuccess ||
       moe::launch_situ_table(c->d_situ, c->situ_bs, c->situ_bl, 0) != cudaSuccess ||
+      moe::route_scatter_noalloc_scratch(&c->d_route_scratch) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(c->d_situ);
     cudaFree(c->d_silu);
@@ -148,33 +150,9 @@ MOE_API size_t moe_route_scatter_workspace_size(int T, int E, int k) {
   return moe::route_scatter_ws_bytes(T, E, k);
 }
 
-MOE_API int moe_route_scatter(moe_ctx* ctx, const moe_route_args* a, moe_stream_t stream) {
-  if (!ctx || !a) return MOE_ERR_INVALID_ARG;
-  if (a->T < 0 || a->E < 1 || a->E > 4096 || a->k < 1 || a->k > 32 || a->k > a->E || a->H < 128 ||
-      a->H % 128 != 0 || a->A < 1 || a->cap < 0 ||
-      (a->quant_group != 0 && a->quant_group != 128 && a->quant_group != 32))
-    return MOE_ERR_INVALID_ARG;
-  if (a->routing_mode != MOE_ROUTE_SOFTMAX_TOPK && a->routing_mode != MOE_ROUTE_SIGMOID_BIAS_TOPK &&
-      a->routing_mode != MOE_ROUTE_PRECOMPUTED)
-    return MOE_ERR_INVALID_ARG;
-  if (a->routing_mode != MOE_ROUTE_PRECOMPUTED && (a->E > 1024 || !a->logits || !a->topk_w))
-    return MOE_ERR_INVALID_ARG;
-  if (a->routing_mode == MOE_ROUTE_SIGMOID_BIAS_TOPK && !a->corr_bias) return MOE_ERR_INVALID_ARG;
-  if (!a->topk_ids || !a->expert_ends || !a->workspace) return MOE_ERR_INVALID_ARG;
-  if (a->T > 0 && (!a->x || !a->a_fp8 || !a->a_sf || !a->src2dst)) return MOE_ERR_INVALID_ARG;
-  if (a->workspace_bytes < moe::route_scatter_ws_bytes(a->T, a->E, a->k) || !al(a->workspace, 16))
-    return MOE_ERR_INVALID_ARG;
-  if (a->T > 0 && (!al(a->x, 16) || !al(a->a_fp8, 8) || !al(a->a_sf, 4))) return MOE_ERR_INVALID_ARG;
-  if ((long)a->cap < (long)a->T * a->k + (long)a->E * (a->A - 1)) return MOE_ERR_CAPACITY;
-  if ((long)a->cap * a->H > 0x7FFFFFFFFFFFL) return MOE_ERR_INVALID_ARG;
-  DeviceGuard g(ctx->device);
-  if (!g.ok) return MOE_ERR_CUDA;
-  return cuda_status(moe::launch_route_scatter(*a, ctx->num_sms, ctx->d_err, S(stream)));
-}
-
-// Argument checks of moe_route_scatter_noalloc: those of moe_route_scatter
-// minus the workspace, plus the size limit of the built-in scratch array.
-static int check_route_noalloc(const moe_route_args* a) {
+// Argument checks shared by moe_route_scatter and moe_route_scatter_noalloc
+// (everything but the scratch: the caller's workspace, or the built-in array).
+static int check_route_args(const moe_route_args* a) {
   if (a->T < 0 || a->E < 1 || a->E > 4096 || a->k < 1 || a->k > 32 || a->k > a->E || a->H < 128 ||
       a->H % 128 != 0 || a->A < 1 || a->cap < 0 ||
       (a->quant_group != 0 && a->quant_group != 128 && a->quant_group != 32))
@@ -190,18 +168,30 @@ static int check_route_noalloc(const moe_route_args* a) {
   if (a->T > 0 && (!al(a->x, 16) || !al(a->a_fp8, 8) || !al(a->a_sf, 4))) return MOE_ERR_INVALID_ARG;
   if ((long)a->cap < (long)a->T * a->k + (long)a->E * (a->A - 1)) return MOE_ERR_CAPACITY;
   if ((long)a->cap * a->H > 0x7FFFFFFFFFFFL) return MOE_ERR_INVALID_ARG;
-  if (moe::route_scatter_ws_bytes(a->T, a->E, a->k) > moe::route_scatter_noalloc_max_bytes())
-    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
+}
+
+MOE_API int moe_route_scatter(moe_ctx* ctx, const moe_route_args* a, moe_stream_t stream) {
+  if (!ctx || !a) return MOE_ERR_INVALID_ARG;
+  const int rc = check_route_args(a);
+  if (rc != MOE_OK) return rc;
+  if (!a->workspace || a->workspace_bytes < moe::route_scatter_ws_bytes(a->T, a->E, a->k) || !al(a->workspace, 16))
+    return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return MOE_ERR_CUDA;
+  return cuda_status(moe::launch_route_scatter(*a, ctx->num_sms, ctx->d_err, S(stream)));
 }
 
 MOE_API int moe_route_scatter_noalloc(moe_ctx* ctx, const moe_route_args* a, moe_stream_t stream) {
   if (!ctx || !a) return MOE_ERR_INVALID_ARG;
-  const int rc = check_route_noalloc(a);
+  const int rc = check_route_args(a);
   if (rc != MOE_OK) return rc;
+  if (moe::route_scatter_ws_bytes(a->T, a->E, a->k) > moe::route_scatter_noalloc_max_bytes())
+    return MOE_ERR_UNSUPPORTED;
   DeviceGuard g(ctx->device);
   if (!g.ok) return MOE_ERR_CUDA;
-  return cuda_status(moe::launch_route_scatter_noalloc(*a, ctx->device, ctx->num_sms, ctx->d_err, S(stream)));
+  return cuda_status(moe::launch_route_scatter_noalloc(*a, ctx->d_route_scratch, ctx->num_sms, ctx->d_err,
+                                                       S(stream)));
 }
 
 MOE_API int moe_prepare_weights(moe_ctx* ctx, const uint8_t* w_in, const uint8_t* sf_in, int E, int N,

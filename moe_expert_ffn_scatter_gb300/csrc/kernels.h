@@ -17,7 +17,8 @@ constexpr int kScatterChunk = 64;
 
 size_t route_scatter_ws_bytes(int T, int E, int k);
 size_t route_scatter_noalloc_max_bytes();
-cudaError_t launch_route_scatter_noalloc(const moe_route_args& a, int device, int num_sms, uint32_t* err,
+cudaError_t route_scatter_noalloc_scratch(void** addr);
+cudaError_t launch_route_scatter_noalloc(const moe_route_args& a, void* scratch, int num_sms, uint32_t* err,
                                          cudaStream_t st);
 cudaError_t launch_expert_ends(const int32_t* counts, int E, int A, int32_t* ends, uint32_t* err,
                                cudaStream_t st);

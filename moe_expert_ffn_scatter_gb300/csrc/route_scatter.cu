@@ -26,7 +26,6 @@
 //      loads) and its codes and packed scale words are stored to each
 //      destination row.
 #include <climits>
-#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -485,35 +484,27 @@ cudaError_t launch_route_scatter(const moe_route_args& a, int num_sms, uint32_t*
 // Scratch of moe_route_scatter_noalloc: the per-chunk expert histograms (up
 // to 1 MiB) and the rank/count completion count live in this file-scope
 // device array instead of a caller-provided workspace. Every GPU that loads
-// the library holds these 1 MiB + 16 bytes until the process exits.
+// this module holds these 1 MiB + 16 bytes until the process exits.
 constexpr size_t kNoAllocScratchBytes = (size_t(1) << 20) + 16;
 static __device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
 
-namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-}  // namespace
-
 size_t route_scatter_noalloc_max_bytes() { return kNoAllocScratchBytes; }
 
-// `device` must be the current device. Its first call on a device looks the
-// array's device address up once (the host-side symbol is only a stand-in,
-// never a device address) and caches it.
-cudaError_t launch_route_scatter_noalloc(const moe_route_args& a, int device, int num_sms, uint32_t* err,
+// Device address of the scratch array on the current device. In host code
+// the array's name is only a stand-in, never a device address; the address
+// comes from the runtime. Looking it up also loads this module on the device
+// (with lazy loading the array is created then). Called once per context, at
+// its creation, with the context's device current.
+cudaError_t route_scatter_noalloc_scratch(void** addr) {
+  *addr = nullptr;
+  return cudaGetSymbolAddress(addr, g_route_scratch);
+}
+
+// `scratch` is the address route_scatter_noalloc_scratch returned for the
+// current device.
+cudaError_t launch_route_scatter_noalloc(const moe_route_args& a, void* scratch, int num_sms, uint32_t* err,
                                          cudaStream_t st) {
-  if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
-  void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[device]) {
-      void* p = nullptr;
-      const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
-      if (e != cudaSuccess) return e;
-      g_scratch_addr[device] = p;
-    }
-    scratch = g_scratch_addr[device];
-  }
+  if (!scratch) return cudaErrorInvalidDevicePointer;
   moe_route_args b = a;
   b.workspace = scratch;
   b.workspace_bytes = kNoAllocScratchBytes;

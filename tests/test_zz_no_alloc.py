@@ -55,6 +55,55 @@ def test_noalloc_equals_workspace_entry_point_on_two_calls_in_a_row(cuda_lib):
     ctx.close()
 
 
+def run_given_routing(ctx, noalloc, ids, x, E, H, A, cap):
+    """Routing given (MOE_ROUTE_PRECOMPUTED): the completion count in the
+    scratch is zeroed by a 4-byte memset instead of by the routing kernel.
+    T = 0 takes the endpoint kernel alone, which reads the scratch as its
+    workspace."""
+    T, k = ids.shape
+    o = outputs(T, E, k, H, cap)
+    o["topk_ids"] = torch.from_numpy(ids).cuda()
+    kw = dict(routing_mode=B.MOE_ROUTE_PRECOMPUTED, x=torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda(),
+              T=T, E=E, k=k, H=H, A=A, cap=cap, **o)
+    if noalloc:
+        B.moe_route_scatter_noalloc(ctx, **kw)
+    else:
+        ws = torch.empty((max(16, B.moe_route_scatter_workspace_size(T, E, k)),), dtype=torch.uint8, device="cuda")
+        B.moe_route_scatter(ctx, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_error(ctx) == 0
+    return {key: v.cpu().numpy() for key, v in o.items()}
+
+
+def test_noalloc_given_routing_and_no_tokens_after_a_large_call(cuda_lib):
+    """Each case runs right after a full-size no-allocation call, so the
+    shared array holds that call's histograms and completion count."""
+    ctx = B.Context(0)
+    big = synth.DEEPSEEK
+    big_inp = synth.ffn_inputs(big, weights=False)
+    g = np.random.default_rng(41)
+    E, k, H, A = 4, 2, 256, 128
+    counts = np.array([96, 0, 129, 1], np.int64)  # the endpoint example of the live-row page
+    ids = synth.ids_with_counts(g, counts, k)
+    x = synth.bf16_normal(g, (ids.shape[0], H))
+    cap = synth.align_up(ids.size + E * (A - 1), A)
+    ref_given = run_given_routing(ctx, False, ids, x, E, H, A, cap)
+    T0_ids = np.zeros((0, 6), np.int32)
+    T0_x = np.zeros((0, 4096), np.uint16)
+    ref_empty = run_given_routing(ctx, False, T0_ids, T0_x, 32, 4096, 128, 32 * 127 + 128)
+    for case in ("given", "empty"):
+        run(ctx, True, big, big_inp, B.MOE_ROUTE_SOFTMAX_TOPK)
+        if case == "given":
+            got, ref = run_given_routing(ctx, True, ids, x, E, H, A, cap), ref_given
+            assert np.array_equal(got["expert_ends"], [96, 128, 257, 385])
+        else:
+            got, ref = run_given_routing(ctx, True, T0_ids, T0_x, 32, 4096, 128, 32 * 127 + 128), ref_empty
+            assert np.array_equal(got["expert_ends"], np.zeros(32, np.int32))
+        for key in ref:
+            assert np.array_equal(got[key], ref[key]), (case, key)
+    ctx.close()
+
+
 def test_noalloc_rejects_sizes_beyond_the_scratch_array(cuda_lib):
     ctx = B.Context(0)
     T, E, k, H = 65536 + 64, 256, 1, 128  # ceil(T/64) * E * 4 bytes just above 1 MiB
