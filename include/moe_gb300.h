@@ -174,7 +174,8 @@ typedef struct moe_act_params {
  *  (ceil(T/64) * E int32 chunk histograms and a 4-byte completion count,
  *  rounded up to 16 bytes), 16-byte aligned, contents need not be
  *  initialised; calls that share a workspace must not overlap on the GPU.
- * Sizes: T >= 0 (T == 0 writes expert_ends = 0 and nothing else),
+ * Sizes: T >= 0 (T == 0 writes expert_ends = 0 and nothing else; the
+ *  per-token pointers may then be NULL),
  *  1 <= E <= 4096 (E <= 1024 for the two routing modes), 1 <= k <= min(E, 32),
  *  H % 128 == 0, A >= 1, cap >= T*k + E*(A-1). Logits must be finite.
  * Errors: MOE_ERR_INVALID_ARG (null pointer, bad size), MOE_ERR_CAPACITY

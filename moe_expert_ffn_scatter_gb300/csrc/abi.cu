@@ -163,8 +163,8 @@ static int check_route_args(const moe_route_args* a) {
   if (a->routing_mode != MOE_ROUTE_PRECOMPUTED && (a->E > 1024 || !a->logits || !a->topk_w))
     return MOE_ERR_INVALID_ARG;
   if (a->routing_mode == MOE_ROUTE_SIGMOID_BIAS_TOPK && !a->corr_bias) return MOE_ERR_INVALID_ARG;
-  if (!a->topk_ids || !a->expert_ends) return MOE_ERR_INVALID_ARG;
-  if (a->T > 0 && (!a->x || !a->a_fp8 || !a->a_sf || !a->src2dst)) return MOE_ERR_INVALID_ARG;
+  if (!a->expert_ends) return MOE_ERR_INVALID_ARG;
+  if (a->T > 0 && (!a->topk_ids || !a->x || !a->a_fp8 || !a->a_sf || !a->src2dst)) return MOE_ERR_INVALID_ARG;
   if (a->T > 0 && (!al(a->x, 16) || !al(a->a_fp8, 8) || !al(a->a_sf, 4))) return MOE_ERR_INVALID_ARG;
   if ((long)a->cap < (long)a->T * a->k + (long)a->E * (a->A - 1)) return MOE_ERR_CAPACITY;
   if ((long)a->cap * a->H > 0x7FFFFFFFFFFFL) return MOE_ERR_INVALID_ARG;

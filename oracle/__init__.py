@@ -70,6 +70,10 @@ def _declare(L):
         "orc_ffn_dense": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _F, _F, _F, _F, _P]),
         "orc_decode": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
                               _I, _F, _F, _F, _P, _P, _P, _P]),
+        "orc_decode_gemv1": (None, [_P, _I, _I, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+        "orc_decode_glu": (None, [_P, _I, _I, _P, _I, _I, _I, _I, _F, _F, _F, _P]),
+        "orc_decode_gemv2": (None, [_P, _I, _I, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+        "orc_decode_sum": (None, [_P, _I, _I, _P, _P, _I, _I, _I, _P]),
         "orc_decode_dense": (None, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                                     _P, _I, _F, _F, _F, _P]),
         "orc_num_threads": (_I, []),
@@ -312,6 +316,63 @@ def decode(x, ids, topk_w, weights, wfmt, I, expert_start=0, n_local=None, inter
                      int(bool(interleaved)), float(alpha), float(beta), float(limit),
                      _p(y1), _p(act), _p(y2), _p(out))
     return y1, act, y2, out
+
+
+def decode_gemv1(x, ids, weights, wfmt, I, expert_start=0, n_local=None, fill=0x7FC0):
+    """Step 1 of the decode path alone: y1 [T, k, 2I] of the local slots."""
+    x = _c(x, np.uint16)
+    ids = _c(ids, np.int32)
+    T, H = x.shape
+    k = ids.shape[1]
+    a = _decode_args(weights)
+    if n_local is None:
+        n_local = a["b_gu"].shape[0]
+    y1 = np.full((T, k, 2 * I), fill, np.uint16)
+    lib().orc_decode_gemv1(_p(x), T, H, I, _p(ids), k, expert_start, n_local, wfmt, _p(a["w_gu"]),
+                           _p(a["gu_scale"]), _p(a["gu_sf"]), _p(a["b_gu"]), _p(y1))
+    return y1
+
+
+def decode_glu(y1, ids, I, expert_start=0, n_local=None, interleaved=True, alpha=1.702, beta=1.0, limit=7.0,
+               fill=0x7FC0):
+    """Step 2 alone: act [T*k, I] from y1 [T, k, 2I]."""
+    y1 = _c(y1, np.uint16)
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    if n_local is None:
+        n_local = int(ids.max()) + 1 - expert_start
+    act = np.full((T * k, I), fill, np.uint16)
+    lib().orc_decode_glu(_p(y1), T, I, _p(ids), k, expert_start, n_local, int(bool(interleaved)), float(alpha),
+                         float(beta), float(limit), _p(act))
+    return act
+
+
+def decode_gemv2(act, ids, weights, wfmt, H, I, expert_start=0, n_local=None, fill=0x7FC0):
+    """Step 3 alone: y2 [T, k, H] from act [T*k, I]."""
+    act = _c(act, np.uint16)
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    a = _decode_args(weights)
+    if n_local is None:
+        n_local = a["b_gu"].shape[0]
+    y2 = np.full((T, k, H), fill, np.uint16)
+    lib().orc_decode_gemv2(_p(act), T, H, I, _p(ids), k, expert_start, n_local, wfmt, _p(a["w_d"]),
+                           _p(a["d_scale"]), _p(a["d_sf"]), _p(a["b_d"]), _p(y2))
+    return y2
+
+
+def decode_sum(y2, ids, topk_w, expert_start=0, n_local=None):
+    """Step 4 alone: out [T, H] from y2 [T, k, H]."""
+    y2 = _c(y2, np.uint16)
+    ids = _c(ids, np.int32)
+    topk_w = _c(topk_w, np.float32)
+    T, k = ids.shape
+    H = y2.shape[2]
+    if n_local is None:
+        n_local = int(ids.max()) + 1 - expert_start
+    out = np.zeros((T, H), np.uint16)
+    lib().orc_decode_sum(_p(y2), T, H, _p(ids), _p(topk_w), k, expert_start, n_local, _p(out))
+    return out
 
 
 def decode_dense(x, ids, topk_w, weights, wfmt, I, expert_start=0, n_local=None, interleaved=True,

@@ -695,39 +695,90 @@ static void dec_glu(const uint16_t* y1, int I, int interleaved, float alpha, flo
     }
 }
 
+/* The four steps of the decode path, each over every (token, slot) whose
+ * expert is local ([SD] §3 kernel flow). Each step takes the previous step's
+ * bf16 output as its input, so a checker can run any step on another
+ * implementation's intermediate. Slots of non-local experts are not written. */
+static int dec_local(const int32_t* ids, long slot, int expert_start, int n_local) {
+    int lid = ids[slot] - expert_start;
+    return (lid < 0 || lid >= n_local) ? -1 : lid;
+}
+
+/* Step 1: y1[t, j] = bf16(W_gu[e] x[t] * scale + b_gu[e]). */
+void orc_decode_gemv1(const uint16_t* x, int T, int H, int I, const int32_t* ids, int k, int expert_start,
+                      int n_local, int wfmt, const uint8_t* w_gu, const float* gu_scale, const uint8_t* gu_sf,
+                      const uint16_t* b_gu, uint16_t* y1) {
+#pragma omp parallel
+    {
+        float* xin = (float*)malloc(sizeof(float) * (size_t)H);
+#pragma omp for collapse(2)
+        for (int t = 0; t < T; t++)
+            for (int j = 0; j < k; j++) {
+                long slot = (long)t * k + j;
+                int lid = dec_local(ids, slot, expert_start, n_local);
+                if (lid < 0) continue;
+                for (int h = 0; h < H; h++) xin[h] = orc_bf16_to_float(x[(long)t * H + h]);
+                dec_gemv(wfmt, xin, H, 2 * I, lid, w_gu, gu_scale, gu_sf, b_gu, y1 + slot * 2 * I);
+            }
+        free(xin);
+    }
+}
+
+/* Step 2: act[t*k + j] = GLU(y1[t, j]). */
+void orc_decode_glu(const uint16_t* y1, int T, int I, const int32_t* ids, int k, int expert_start, int n_local,
+                    int glu_interleaved, float alpha, float beta, float limit, uint16_t* act) {
+    for (long slot = 0; slot < (long)T * k; slot++) {
+        if (dec_local(ids, slot, expert_start, n_local) < 0) continue;
+        dec_glu(y1 + slot * 2 * I, I, glu_interleaved, alpha, beta, limit, act + slot * I);
+    }
+}
+
+/* Step 3: y2[t, j] = bf16(W_d[e] act[t*k + j] * scale + b_d[e]). */
+void orc_decode_gemv2(const uint16_t* act, int T, int H, int I, const int32_t* ids, int k, int expert_start,
+                      int n_local, int wfmt, const uint8_t* w_d, const float* d_scale, const uint8_t* d_sf,
+                      const uint16_t* b_d, uint16_t* y2) {
+#pragma omp parallel
+    {
+        float* xin = (float*)malloc(sizeof(float) * (size_t)I);
+#pragma omp for collapse(2)
+        for (int t = 0; t < T; t++)
+            for (int j = 0; j < k; j++) {
+                long slot = (long)t * k + j;
+                int lid = dec_local(ids, slot, expert_start, n_local);
+                if (lid < 0) continue;
+                for (int i = 0; i < I; i++) xin[i] = orc_bf16_to_float(act[slot * I + i]);
+                dec_gemv(wfmt, xin, I, H, lid, w_d, d_scale, d_sf, b_d, y2 + slot * H);
+            }
+        free(xin);
+    }
+}
+
+/* Step 4: out[t] = bf16(sum over local slots j, in slot order, of w[t, j] * y2[t, j]),
+ * one fp32 fma per slot. */
+void orc_decode_sum(const uint16_t* y2, int T, int H, const int32_t* ids, const float* topk_w, int k,
+                    int expert_start, int n_local, uint16_t* out) {
+    for (int t = 0; t < T; t++)
+        for (int h = 0; h < H; h++) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; j++) {
+                long slot = (long)t * k + j;
+                if (dec_local(ids, slot, expert_start, n_local) < 0) continue;
+                acc = fmaf(topk_w[slot], orc_bf16_to_float(y2[slot * H + h]), acc);
+            }
+            out[(long)t * H + h] = orc_bf16_from_float(acc);
+        }
+}
+
 void orc_decode(const uint16_t* x, int T, int H, int I, const int32_t* ids, const float* topk_w, int k,
                 int expert_start, int n_local, int wfmt,
                 const uint8_t* w_gu, const float* gu_scale, const uint8_t* gu_sf, const uint16_t* b_gu,
                 const uint8_t* w_d, const float* d_scale, const uint8_t* d_sf, const uint16_t* b_d,
                 int glu_interleaved, float alpha, float beta, float limit,
                 uint16_t* y1, uint16_t* act, uint16_t* y2, uint16_t* out) {
-#pragma omp parallel
-    {
-        float* xin = (float*)malloc(sizeof(float) * (size_t)(H > I ? H : I));
-#pragma omp for collapse(2)
-        for (int t = 0; t < T; t++)
-            for (int j = 0; j < k; j++) {
-                int lid = ids[(long)t * k + j] - expert_start;
-                if (lid < 0 || lid >= n_local) continue;
-                long slot = (long)t * k + j;
-                for (int h = 0; h < H; h++) xin[h] = orc_bf16_to_float(x[(long)t * H + h]);
-                dec_gemv(wfmt, xin, H, 2 * I, lid, w_gu, gu_scale, gu_sf, b_gu, y1 + slot * 2 * I);
-                dec_glu(y1 + slot * 2 * I, I, glu_interleaved, alpha, beta, limit, act + slot * I);
-                for (int i = 0; i < I; i++) xin[i] = orc_bf16_to_float(act[slot * I + i]);
-                dec_gemv(wfmt, xin, I, H, lid, w_d, d_scale, d_sf, b_d, y2 + slot * H);
-            }
-        free(xin);
-    }
-    for (int t = 0; t < T; t++)
-        for (int h = 0; h < H; h++) {
-            float acc = 0.0f;
-            for (int j = 0; j < k; j++) {
-                int lid = ids[(long)t * k + j] - expert_start;
-                if (lid < 0 || lid >= n_local) continue;
-                acc = fmaf(topk_w[(long)t * k + j], orc_bf16_to_float(y2[((long)t * k + j) * H + h]), acc);
-            }
-            out[(long)t * H + h] = orc_bf16_from_float(acc);
-        }
+    orc_decode_gemv1(x, T, H, I, ids, k, expert_start, n_local, wfmt, w_gu, gu_scale, gu_sf, b_gu, y1);
+    orc_decode_glu(y1, T, I, ids, k, expert_start, n_local, glu_interleaved, alpha, beta, limit, act);
+    orc_decode_gemv2(act, T, H, I, ids, k, expert_start, n_local, wfmt, w_d, d_scale, d_sf, b_d, y2);
+    orc_decode_sum(y2, T, H, ids, topk_w, k, expert_start, n_local, out);
 }
 
 /* Dense twin of the decode path: every local expert on every token, then the

@@ -96,6 +96,16 @@ void orc_ffn_dense(const uint16_t* x, int T, int H, int I, const int32_t* ids, c
 
 /* decode GEMV path (bf16 activations, FP8-per-expert or MXFP4 weights) */
 float orc_glu_oai(float g, float u, float alpha, float beta, float limit);
+void orc_decode_gemv1(const uint16_t* x, int T, int H, int I, const int32_t* ids, int k, int expert_start,
+                      int n_local, int wfmt, const uint8_t* w_gu, const float* gu_scale, const uint8_t* gu_sf,
+                      const uint16_t* b_gu, uint16_t* y1);
+void orc_decode_glu(const uint16_t* y1, int T, int I, const int32_t* ids, int k, int expert_start, int n_local,
+                    int glu_interleaved, float alpha, float beta, float limit, uint16_t* act);
+void orc_decode_gemv2(const uint16_t* act, int T, int H, int I, const int32_t* ids, int k, int expert_start,
+                      int n_local, int wfmt, const uint8_t* w_d, const float* d_scale, const uint8_t* d_sf,
+                      const uint16_t* b_d, uint16_t* y2);
+void orc_decode_sum(const uint16_t* y2, int T, int H, const int32_t* ids, const float* topk_w, int k,
+                    int expert_start, int n_local, uint16_t* out);
 void orc_decode(const uint16_t* x, int T, int H, int I, const int32_t* ids, const float* topk_w, int k,
                 int expert_start, int n_local, int wfmt,
                 const uint8_t* w_gu, const float* gu_scale, const uint8_t* gu_sf, const uint16_t* b_gu,

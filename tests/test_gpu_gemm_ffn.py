@@ -8,7 +8,8 @@ from moe_expert_ffn_scatter_gb300 import binding as B
 from moe_expert_ffn_scatter_gb300 import synth
 from moe_expert_ffn_scatter_gb300.layer import MoEFFNLayer
 from tests.gpu_util import check_ffn_tolerance, dev, dev_bf16, filled, host, host_u16
-from tests.refs import bf16_bits_to_f64, bf16_ulp, e2m1_decode, e4m3_decode_torch, e4m3_encode_torch
+from tests.refs import (bf16_bits_to_f64, bf16_ulp, e2m1_decode, e4m3_decode_torch, e4m3_encode_torch,
+                        unpack_scale_bytes)
 
 pytestmark = pytest.mark.gpu
 
@@ -380,25 +381,126 @@ def test_tiny_layer_situ_vs_oracle(ctx, orc):
     check_ffn_tolerance(host_u16(out), ref)
 
 
-def test_deepseek_layer_sampled_tokens(ctx, orc):
+def sampled_rows_gemm(orc, a, a_sf_words, ends, rows, w, w_sf, K, a_group=128):
+    """The oracle's grouped GEMM on selected live rows of a full-size buffer:
+    the rows are regrouped by expert into a small endpoint layout (with their
+    scale words) and multiplied by their experts' weights. Returns the
+    oracle's outputs in the order of `rows` and the sum of |products| of each
+    output (the fp32 accumulation bound)."""
+    E = ends.shape[0]
+    start = np.concatenate([[0], (ends[:-1] + 127) // 128 * 128])
+    exp_of = np.searchsorted(ends, rows, side="right")
+    assert np.all((rows >= start[exp_of]) & (rows < ends[exp_of]))
+    order = np.argsort(exp_of, kind="stable")
+    counts = np.bincount(exp_of, minlength=E).astype(np.int32)
+    _, ends_s = orc.endpoints(counts, 128)
+    start_s = np.concatenate([[0], (ends_s[:-1] + 127) // 128 * 128])
+    cap_s = synth.align_up(max(int(ends_s[-1]), 128), 128)
+    ld_s = synth.align4(cap_s)
+    pos = np.empty(rows.shape[0], np.int64)
+    seen = np.zeros(E, np.int64)
+    for i in order:
+        e = exp_of[i]
+        pos[i] = start_s[e] + seen[e]
+        seen[e] += 1
+    a_s = np.zeros((cap_s, K), np.uint8)
+    a_s[pos] = a[rows]
+    sf_s = np.zeros((a_sf_words.shape[0], ld_s), np.int32)
+    sf_s[:, pos] = a_sf_words[:, rows]
+    N = w.shape[1]
+    ref = orc.grouped_gemm(a_s, sf_s, ends_s, 128, w, w_sf)[pos]
+    G = K // a_group
+    sfb = unpack_scale_bytes(sf_s, cap_s, G)[pos].astype(np.int64)
+    ad = np.abs(e4m3_decode_torch(a[rows])) * np.repeat(2.0 ** (sfb - 127), a_group, axis=1)
+    abssum = np.zeros((rows.shape[0], N))
+    for e in np.unique(exp_of):
+        sel = exp_of == e
+        wd = np.abs(e2m1_decode(w[e], K)) * np.repeat(2.0 ** (w_sf[e].astype(np.int64) - 127), 32, axis=1)
+        abssum[sel] = ad[sel] @ wd.T
+    return ref, abssum
+
+
+def assert_rows_close(got, ref, abssum):
+    g = bf16_bits_to_f64(got)
+    r = bf16_bits_to_f64(ref)
+    bad = np.abs(g - r) > bf16_ulp(r) * 1.0001 + 2.0 ** -18 * abssum + 1e-30
+    assert not bad.any(), "%d of %d elements outside the bound" % (bad.sum(), bad.size)
+
+
+def test_deepseek_layer_full_size(ctx, orc):
+    """The DeepSeek-style layer (E = 32, top-6, T = 4,096, H = 4,096,
+    I = 2,048, capacity 28,672) at full size, unfused and fused:
+      - routing, endpoints and src2dst equal the oracle's;
+      - every live row's act-quant (e4m3 codes and packed UE8M0 words) equals
+        the oracle's act-quant of the GPU's own gate/up buffer, bit for bit
+        (all 24,576 live rows);
+      - the fused layer (SiLU*mul + quantisation in GEMM1's epilogue) gives
+        the unfused layer's codes, scale words and output bit for bit, and
+        leaves every padding row's sentinel;
+      - GEMM1 and GEMM2 on 256 sampled live rows each: within one bf16 step
+        plus the fp32 summation bound of the oracle's GEMM of the GPU's own
+        input rows;
+      - 256 sampled tokens of the output within the layer tolerance of the
+        oracle's whole layer."""
     cfg = synth.DEEPSEEK
     inp = synth.ffn_inputs(cfg)
-    layer = make_layer(ctx, cfg, inp)
-    out = layer.forward(dev_bf16(inp.x), dev(inp.logits))
-    torch.cuda.synchronize()
-    assert B.moe_get_device_error(ctx) == 0
+    res = {}
+    for fused in (False, True):
+        layer = make_layer(ctx, cfg, inp, fused=fused)
+        layer.act_fp8.fill_(0xAB)
+        layer.act_sf.view(torch.uint8).fill_(0xAB)
+        layer.down.view(torch.uint8).fill_(0xAB)
+        out = layer.forward(dev_bf16(inp.x), dev(inp.logits))
+        torch.cuda.synchronize()
+        assert B.moe_get_device_error(ctx) == 0
+        r = dict(act=host(layer.act_fp8).copy(), sf=host(layer.act_sf).copy(), out=host_u16(out).copy(),
+                 ends=host(layer.expert_ends).copy(), ids=host(layer.topk_ids).copy(),
+                 s2d=host(layer.src2dst).copy(), down=host_u16(layer.down).copy())
+        if not fused:
+            r["gateup"] = host_u16(layer.gateup).copy()
+            r["a"] = host(layer.a_fp8).copy()
+            r["a_sf"] = host(layer.a_sf).copy()
+        res[fused] = r
+        del layer, out
+        torch.cuda.empty_cache()
+    u, f = res[False], res[True]
     ids, w = oracle_layer(orc, cfg, inp)
-    assert np.array_equal(host(layer.topk_ids), ids)
-    toks = np.random.default_rng(11).choice(cfg.T, 48, replace=False).astype(np.int32)
+    ends, s2d, _, _ = orc.scatter(ids, inp.x, cfg.E, cfg.A, cfg.cap)
+    for r in (u, f):
+        assert np.array_equal(r["ids"], ids)
+        assert np.array_equal(r["ends"], ends)
+        assert np.array_equal(r["s2d"], s2d)
+    live = live_rows(ends, cfg.cap)
+    assert live.sum() == cfg.R
+    # act-quant of every live row from the GPU's gate/up
+    ract, rsf = orc.act_quant(u["gateup"], ends, cfg.A)
+    assert np.array_equal(u["act"][live], ract[live])
+    assert np.array_equal(u["sf"][:, :cfg.cap][:, live], rsf[:, :cfg.cap][:, live])
+    # fused == unfused, sentinels intact
+    for key in ("act", "sf", "out"):
+        assert np.array_equal(f[key], u[key]), key
+    assert np.all(f["act"][~live] == 0xAB)
+    assert np.all(f["sf"].view(np.uint8).reshape(f["sf"].shape[0], -1, 4)[:, :cfg.cap][:, ~live] == 0xAB)
+    assert np.all(f["down"][~live] == 0xABAB)
+    # the two GEMMs on sampled live rows
+    g = np.random.default_rng(11)
+    rows = np.sort(g.choice(np.flatnonzero(live), 256, replace=False))
+    ref1, ab1 = sampled_rows_gemm(orc, u["a"], u["a_sf"], ends, rows, inp.w13, inp.w13_sf, cfg.H)
+    assert_rows_close(u["gateup"][rows], ref1, ab1)
+    ref2, ab2 = sampled_rows_gemm(orc, u["act"], u["sf"], ends, rows, inp.w2, inp.w2_sf, cfg.I)
+    assert_rows_close(u["down"][rows], ref2, ab2)
+    # the whole layer on sampled tokens
+    toks = np.sort(g.choice(cfg.T, 256, replace=False)).astype(np.int32)
     ref = orc.ffn_tokens(inp.x, ids, w, inp.w13, inp.w13_sf, inp.w2, inp.w2_sf, toks)
-    check_ffn_tolerance(host_u16(out)[toks], ref)
+    check_ffn_tolerance(u["out"][toks], ref)
 
 
 def test_kimi_layer_sampled_tokens(ctx, orc):
     """Kimi-shaped layer at full size (E = 896, top-16, sigmoid + bias
     routing, SiLU*mul with clamp 25, capacity 146,560 rows): routing, the
-    endpoint tensor and sampled output rows against the oracle. The oracle
-    takes each group of tokens with only the experts those tokens use."""
+    endpoint tensor, and 256 sampled output rows against the oracle's whole
+    layer. The oracle takes the sampled tokens with only the experts those
+    tokens use (drawn expert by expert, as the layer's weights were)."""
     cfg = synth.KIMI
     inp = synth.ffn_inputs(cfg)
     layer = MoEFFNLayer(ctx, T=cfg.T, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I, A=cfg.A, cap=cfg.cap,
@@ -413,16 +515,23 @@ def test_kimi_layer_sampled_tokens(ctx, orc):
     _, ends = orc.endpoints(orc.expert_counts(ids, cfg.E), cfg.A)
     assert np.array_equal(host(layer.expert_ends), ends)
     got = host_u16(out)
-    toks = np.random.default_rng(15).choice(cfg.T, 16, replace=False).astype(np.int32)
-    for grp in toks.reshape(4, 4):
-        used = np.unique(ids[grp])
-        remap = np.full(cfg.E, -1, np.int32)
-        remap[used] = np.arange(used.size, dtype=np.int32)
-        w13, w13_sf, w2, w2_sf = synth.stacked_expert_weights(cfg, used)
-        ids_c = np.zeros_like(ids)
-        ids_c[grp] = remap[ids[grp]]
-        ref = orc.ffn_tokens(inp.x, ids_c, w, w13, w13_sf, w2, w2_sf, grp, clamp=True, limit=cfg.limit)
-        check_ffn_tolerance(got[grp], ref)
+    del layer, out
+    torch.cuda.empty_cache()
+    toks = np.sort(np.random.default_rng(15).choice(cfg.T, 256, replace=False)).astype(np.int32)
+    used = np.unique(ids[toks])
+    remap = np.full(cfg.E, -1, np.int32)
+    remap[used] = np.arange(used.size, dtype=np.int32)
+    parts = None
+    for i, e in enumerate(used):
+        p = synth.expert_weights(cfg, int(e))
+        if parts is None:
+            parts = [np.empty((used.size,) + q.shape, q.dtype) for q in p]
+        for dst, q in zip(parts, p):
+            dst[i] = q
+    ids_c = np.zeros_like(ids)
+    ids_c[toks] = remap[ids[toks]]
+    ref = orc.ffn_tokens(inp.x, ids_c, w, *parts, toks, clamp=True, limit=cfg.limit)
+    check_ffn_tolerance(got[toks], ref)
 
 
 def test_layer_graph_replay_permuted_routing_deterministic(ctx, orc):

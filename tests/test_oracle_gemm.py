@@ -256,3 +256,73 @@ def test_decode_first_gemv_vs_numpy(orc, wfmt):
             ref = W @ x[t] + bf16_bits_to_f64(weights["b_gu"][e])
             got = bf16_bits_to_f64(y1[t, j])
             assert np.all(np.abs(got - ref) <= 0.5 * bf16_ulp(ref) * (1 + 1e-9) + 1e-30)
+
+
+@pytest.mark.parametrize("wfmt", [0, 1])
+def test_decode_steps_compose_to_the_whole_path(orc, wfmt):
+    """The four decode steps, each run on the previous step's output, give
+    the whole path bit for bit (non-local slots included)."""
+    T, E, H, I, k = 3, 6, 128, 128, 4
+    d = synth.decode_inputs(T, E=E, H=H, I=I, seed=11)
+    ids, w = orc.route_softmax_topk(d.logits, k)
+    es, nl = 1, 4
+    loc = {kk: v[es:es + nl] for kk, v in (d.fp8 if wfmt == 0 else d.mxfp4).items()}
+    y1, act, y2, out = orc.decode(d.x, ids, w, loc, wfmt, I, expert_start=es, n_local=nl)
+    s1 = orc.decode_gemv1(d.x, ids, loc, wfmt, I, es, nl)
+    s2 = orc.decode_glu(s1, ids, I, es, nl)
+    s3 = orc.decode_gemv2(s2, ids, loc, wfmt, H, I, es, nl)
+    s4 = orc.decode_sum(s3, ids, w, es, nl)
+    for a, b in ((s1, y1), (s2, act), (s3, y2), (s4, out)):
+        assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("wfmt", [0, 1])
+def test_decode_second_gemv_vs_numpy(orc, wfmt):
+    """The down GEMV on a given act: fp64 numpy matmul on the dequantised
+    weights, one rounding to bf16 (within half a bf16 step)."""
+    T, E, H, I, k = 2, 4, 128, 256, 2
+    d = synth.decode_inputs(T, E=E, H=H, I=I, seed=12)
+    ids, _ = orc.route_softmax_topk(d.logits, k)
+    weights = d.fp8 if wfmt == 0 else d.mxfp4
+    act = synth.bf16_normal(np.random.default_rng(13), (T * k, I))
+    y2 = orc.decode_gemv2(act, ids, weights, wfmt, H, I)
+    a = bf16_bits_to_f64(act)
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            if wfmt == 0:
+                W = e4m3_decode_torch(weights["w_d"][e]) * float(weights["d_scale"][e])
+            else:
+                W = deq_weights(weights["w_d"][e:e + 1], weights["d_sf"][e:e + 1])[0]
+            ref = W @ a[t * k + j] + bf16_bits_to_f64(weights["b_d"][e])
+            got = bf16_bits_to_f64(y2[t, j])
+            assert np.all(np.abs(got - ref) <= 0.5 * bf16_ulp(ref) * (1 + 1e-9) + 1e-30)
+
+
+@pytest.mark.parametrize("interleaved", [True, False])
+def test_decode_glu_step_reads_gate_and_up_from_the_layout(orc, interleaved):
+    """Interleaved rows pair (2i, 2i+1), halves rows pair (i, I+i); each act
+    value is the scalar GLU of its pair rounded to bf16."""
+    T, k, I = 2, 2, 64
+    ids = np.array([[0, 1], [1, 0]], np.int32)
+    y1 = synth.bf16_normal(np.random.default_rng(14), (T, k, 2 * I), std=4.0)
+    act = orc.decode_glu(y1, ids, I, 0, 2, interleaved=interleaved)
+    for s in range(T * k):
+        row = y1.reshape(T * k, 2 * I)[s]
+        for i in range(I):
+            g, u = (row[2 * i], row[2 * i + 1]) if interleaved else (row[i], row[I + i])
+            v = orc.glu_oai(orc.bf16_to_float(g), orc.bf16_to_float(u), 1.702, 1.0, 7.0)
+            assert act[s, i] == orc.bf16_from_float(v)
+
+
+def test_decode_sum_closed_forms(orc):
+    """One local slot with weight 1 returns y2; two slots of the same row with
+    weights 1/2 return it too (both products exact); a non-local slot adds
+    nothing."""
+    T, k, H = 2, 3, 32
+    y = synth.bf16_normal(np.random.default_rng(15), (T, 1, H))
+    y2 = np.repeat(y, k, axis=1)
+    ids = np.array([[0, 9, 9], [1, 1, 9]], np.int32)
+    w = np.array([[1.0, 5.0, 5.0], [0.5, 0.5, 7.0]], np.float32)
+    out = orc.decode_sum(y2, ids, w, 0, 2)
+    assert np.array_equal(out, y[:, 0])
