@@ -103,8 +103,12 @@ typedef void* moe_stream_t; /* cudaStream_t */
  * moe_ctx_create: binds `device`, reads its SM count, allocates the 4-byte
  *   device error word and the SiLU table (entry i = silu of the bf16 value
  *   with bits i under the library's exp specification; the activation step
- *   looks SiLU up there, its input being a bf16 gate value). Returns
- *   MOE_ERR_CUDA if the device is unusable.
+ *   looks SiLU up there, its input being a bf16 gate value). It also sets up
+ *   the grouped GEMM: the number of CTA pairs of its two-SM kernel that the
+ *   device runs at once (cluster occupancy). The environment variable
+ *   MOE_GEMM_CTA_PAIRS, read here, caps that number (0 selects the one-CTA
+ *   kernel for every call; the results are the same). Returns MOE_ERR_CUDA if
+ *   the device is unusable.
  * moe_ctx_destroy: frees the context (NULL is ignored).
  * moe_get_device_error: synchronises `stream`, reads the error word into
  *   *bits (host) and clears it. */

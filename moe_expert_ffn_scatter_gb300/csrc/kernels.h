@@ -67,8 +67,12 @@ struct GemmArgs {
 };
 // Per-device set-up (shared-memory opt-in); called once per context.
 cudaError_t init_grouped_gemm();
-// Returns MOE_OK or a MOE_ERR_* code.
-int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, uint32_t* err,
+// CTA pairs of the pair kernel resident at once on the current device (0: the
+// one-CTA kernel only); queried once per context.
+int grouped_gemm_pairs();
+// Returns MOE_OK or a MOE_ERR_* code. pairs > 0 and E <= 1024 take the
+// CTA-pair kernel with that many pairs, otherwise the one-CTA kernel.
+int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, int pairs, uint32_t* err,
                         cudaStream_t st);
 
 cudaError_t init_decode();

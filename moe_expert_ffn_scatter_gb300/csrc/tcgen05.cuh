@@ -79,6 +79,13 @@ static __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, vo
   }
 }
 
+// wait_phase with an inlined first probe: a phase that has already completed
+// costs one try_wait, not a call.
+__device__ __forceinline__ bool wait_phase_fast(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                uint32_t* err) {
+  return mbar_try_wait(bar, parity) || wait_phase(bar, parity, abort_flag, err);
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             uint32_t bar) {
   asm volatile(

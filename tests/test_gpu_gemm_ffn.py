@@ -1,5 +1,7 @@
 """Grouped block-scaled GEMM, combine and the whole layer on the GPU against
 the oracle."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -167,6 +169,65 @@ def test_gemm_fp8_weight_recipes(ctx, orc, recipe):
     for e in range(E):
         abssum[start[e]:ends[e]] = ad[start[e]:ends[e]] @ wabs[e].T
     assert_gemm_close(got, ref, ends, abssum)
+
+
+def context_with_pairs(n):
+    """A context whose grouped GEMM runs at most n CTA pairs (0: the one-CTA
+    kernel), through MOE_GEMM_CTA_PAIRS, read at context creation."""
+    old = os.environ.get("MOE_GEMM_CTA_PAIRS")
+    os.environ["MOE_GEMM_CTA_PAIRS"] = str(n)
+    try:
+        return B.Context(0)
+    finally:
+        if old is None:
+            del os.environ["MOE_GEMM_CTA_PAIRS"]
+        else:
+            os.environ["MOE_GEMM_CTA_PAIRS"] = old
+
+
+@pytest.mark.parametrize("fmt", [B.MOE_GEMM_W_E2M1, B.MOE_GEMM_W_E4M3], ids=["e2m1", "e4m3"])
+def test_pair_kernel_equals_one_cta_kernel(ctx, orc, fmt):
+    """The two-SM kernel (cta_group::2, as many pairs as fit, and capped at two
+    pairs so that each pair loops over many tiles and wraps its stage ring)
+    and the one-CTA kernel give the same bits, within the oracle's bound:
+    experts whose last 256-row tile holds 128 rows or fewer (the odd CTA's
+    rows past the expert's end), exactly 256 and 257 rows, an empty expert,
+    K with a partial group of four 128-blocks."""
+    counts = [5, 0, 300, 129, 1, 256, 257, 128, 384]
+    outs = []
+    for c in (ctx, context_with_pairs(2), context_with_pairs(0)):
+        got, ref, ends, ab = gemm_case(c, orc, counts, 768, 640, fmt, seed=8)
+        assert_gemm_close(got, ref, ends, ab)
+        outs.append(got)
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("act", ["silu", "silu_clamp", "situ"])
+def test_pair_kernel_fused_layer_equals_one_cta_kernel(orc, act):
+    """The whole layer (fused GEMM1 epilogue, GEMM2) through the two-SM kernel
+    and through the one-CTA kernel: codes, scale words and output bit for bit."""
+    clamp = act == "silu_clamp"
+    kind = {"silu": B.MOE_ACT_SILU, "silu_clamp": B.MOE_ACT_SILU_CLAMP, "situ": B.MOE_ACT_SITU}[act]
+    cfg = synth.FFNConfig("pair", T=900, E=7, k=3, H=512, I=512, seed=23, clamp=clamp, limit=2.5 if clamp else 0.0)
+    inp = synth.ffn_inputs(cfg)
+    res = []
+    for n in (None, 3, 0):
+        c = B.Context(0) if n is None else context_with_pairs(n)
+        layer = make_layer(c, cfg, inp, act_kind=kind)
+        layer.act_fp8.fill_(0xAB)
+        layer.act_sf.view(torch.uint8).fill_(0xAB)
+        layer.forward(dev_bf16(inp.x), dev(inp.logits))
+        torch.cuda.synchronize()
+        assert B.moe_get_device_error(c) == 0
+        res.append((host(layer.act_fp8).copy(), host(layer.act_sf).copy(), host_u16(layer.out).copy()))
+    for r in res[1:]:
+        for a_, b_ in zip(res[0], r):
+            assert np.array_equal(a_, b_)
+    ids, w = oracle_layer(orc, cfg, inp)
+    toks = np.arange(0, cfg.T, 7, dtype=np.int32)
+    ref = orc.ffn_tokens(inp.x, ids, w, inp.w13, inp.w13_sf, inp.w2, inp.w2_sf, toks, clamp=clamp, limit=cfg.limit,
+                         situ=(4.0, 25.0) if act == "situ" else None)
+    check_ffn_tolerance(res[0][2][toks], ref)
 
 
 def test_combine_bit_exact(ctx, orc):
