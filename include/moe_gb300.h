@@ -105,10 +105,13 @@ typedef void* moe_stream_t; /* cudaStream_t */
  *   with bits i under the library's exp specification; the activation step
  *   looks SiLU up there, its input being a bf16 gate value). It also sets up
  *   the grouped GEMM: the number of CTA pairs of its two-SM kernel that the
- *   device runs at once (cluster occupancy). The environment variable
- *   MOE_GEMM_CTA_PAIRS, read here, caps that number (0 selects the one-CTA
- *   kernel for every call; the results are the same). Returns MOE_ERR_CUDA if
- *   the device is unusable.
+ *   device runs at once (cluster occupancy). A grouped GEMM call takes the
+ *   two-SM kernel when E <= 1024 and the capacity holds at least 160 routed
+ *   rows per expert (cap - 127 E >= 160 E), else the one-CTA kernel; the
+ *   results are the same bit for bit. The environment variable
+ *   MOE_GEMM_CTA_PAIRS, read here, overrides the choice: n > 0 takes the
+ *   two-SM kernel with at most n pairs for every call, 0 the one-CTA kernel.
+ *   Returns MOE_ERR_CUDA if the device is unusable.
  * moe_ctx_destroy: frees the context (NULL is ignored).
  * moe_get_device_error: synchronises `stream`, reads the error word into
  *   *bits (host) and clears it. */

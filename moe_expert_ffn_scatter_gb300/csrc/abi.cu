@@ -12,7 +12,8 @@
 struct moe_ctx {
   int device;
   int num_sms;
-  int gemm_pairs;  // CTA pairs of the pair GEMM kernel resident at once (0: one-CTA kernel)
+  int gemm_pairs;         // CTA pairs of the pair GEMM kernel resident at once (0: one-CTA kernel)
+  bool gemm_pairs_forced;  // take the pair kernel whatever the rows per expert
   uint32_t* d_err;
   float* d_silu;  // 65,536-entry SiLU table of the exp/SiLU specification
   float* d_situ;  // 2 x 65,536-entry SiTU tables (gate', up') for situ_bs / situ_bl
@@ -117,6 +118,7 @@ MOE_API int moe_ctx_create(moe_ctx** out, int device) {
   if (const char* cap_pairs = getenv("MOE_GEMM_CTA_PAIRS")) {
     const long v = strtol(cap_pairs, nullptr, 10);
     if (v >= 0 && v < c->gemm_pairs) c->gemm_pairs = (int)v;
+    c->gemm_pairs_forced = v > 0;
   }
   *out = c;
   return MOE_OK;
@@ -240,7 +242,7 @@ MOE_API int moe_grouped_gemm(moe_ctx* ctx, const uint8_t* a, const int32_t* a_sf
   if (rc != MOE_OK) return rc;
   if (cap == 0) return MOE_OK;
   DeviceGuard dg(ctx->device);
-  return moe::launch_grouped_gemm(g, ctx->encode, ctx->num_sms, ctx->gemm_pairs, ctx->d_err, S(stream));
+  return moe::launch_grouped_gemm(g, ctx->encode, ctx->num_sms, ctx->gemm_pairs, ctx->gemm_pairs_forced, ctx->d_err, S(stream));
 }
 
 // Activation parameters: SiLU, SiLU with a clamp limit L > 0, or SiTU with
@@ -298,7 +300,7 @@ MOE_API int moe_grouped_gemm_act_quant(moe_ctx* ctx, const uint8_t* a, const int
   if (cap == 0) return MOE_OK;
   DeviceGuard dg(ctx->device);
   if ((rc = prepare_act(ctx, act, S(stream))) != MOE_OK) return rc;
-  return moe::launch_grouped_gemm(g, ctx->encode, ctx->num_sms, ctx->gemm_pairs, ctx->d_err, S(stream));
+  return moe::launch_grouped_gemm(g, ctx->encode, ctx->num_sms, ctx->gemm_pairs, ctx->gemm_pairs_forced, ctx->d_err, S(stream));
 }
 
 MOE_API int moe_act_quant(moe_ctx* ctx, const uint16_t* gateup, uint8_t* out, int32_t* out_sf,
@@ -362,14 +364,14 @@ MOE_API int moe_ffn_forward(moe_ctx* ctx, const moe_ffn_args* a, moe_stream_t st
   DeviceGuard dg(ctx->device);
   if ((rc = prepare_act(ctx, &a->act, S(stream))) != MOE_OK) return rc;
   if (a->cap > 0) {
-    if ((rc = moe::launch_grouped_gemm(g1, ctx->encode, ctx->num_sms, ctx->gemm_pairs, ctx->d_err, S(stream))) != MOE_OK) return rc;
+    if ((rc = moe::launch_grouped_gemm(g1, ctx->encode, ctx->num_sms, ctx->gemm_pairs, ctx->gemm_pairs_forced, ctx->d_err, S(stream))) != MOE_OK) return rc;
     if (!fused &&
         (rc = cuda_status(moe::launch_act_quant(a->gateup, a->act_fp8, a->act_sf, a->expert_ends, a->E, a->A,
                                                 a->cap, a->I, a->act.kind, a->act.limit, ctx->d_silu,
                                                 ctx->d_situ, act_group(&a->act), ctx->num_sms, ctx->d_err,
                                                 S(stream)))) != MOE_OK)
       return rc;
-    if ((rc = moe::launch_grouped_gemm(g2, ctx->encode, ctx->num_sms, ctx->gemm_pairs, ctx->d_err, S(stream))) != MOE_OK) return rc;
+    if ((rc = moe::launch_grouped_gemm(g2, ctx->encode, ctx->num_sms, ctx->gemm_pairs, ctx->gemm_pairs_forced, ctx->d_err, S(stream))) != MOE_OK) return rc;
   }
   return cuda_status(moe::launch_combine(a->down, a->H, a->topk_w, a->src2dst, a->T, a->k, a->rsf, a->out,
                                          ctx->num_sms, S(stream)));

@@ -1015,10 +1015,19 @@ int launch_pair_impl(const GemmArgs& g, EncodeTiledFn encode, int max_pairs, uin
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// The pair kernel computes 256-row tiles: an expert's last tile leaves the odd
+// CTA idle when it holds 128 rows or fewer. With few rows per expert (the
+// routed rows estimated from the capacity, cap >= routes + E (A - 1), never
+// from counts, so that a captured launch stays valid) most pair tiles would
+// be half idle, and the one-CTA kernel's 128-row tiles do better.
+constexpr long kPairMinRowsPerExpert = 160;
+
 template <int kEpi>
-int launch_fmt(const GemmArgs& g, EncodeTiledFn encode, int num_sms, int pairs, uint32_t* err, cudaStream_t st) {
+int launch_fmt(const GemmArgs& g, EncodeTiledFn encode, int num_sms, int pairs, bool force_pairs, uint32_t* err,
+               cudaStream_t st) {
   const bool fp4 = !(g.w_format & MOE_GEMM_W_E4M3);
-  if (pairs > 0 && g.E <= pr::kMaxExperts)
+  const bool rows_enough = (long)g.cap - 127L * g.E >= kPairMinRowsPerExpert * g.E;
+  if (pairs > 0 && g.E <= pr::kMaxExperts && (force_pairs || rows_enough))
     return fp4 ? launch_pair_impl<true, kEpi>(g, encode, pairs, err, st)
                : launch_pair_impl<false, kEpi>(g, encode, pairs, err, st);
   return fp4 ? launch_impl<true, kEpi>(g, encode, num_sms, err, st)
@@ -1067,12 +1076,12 @@ int grouped_gemm_pairs() {
   return n;
 }
 
-int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, int pairs, uint32_t* err,
-                        cudaStream_t st) {
-  if (g.epi == 1) return launch_fmt<kEpiSilu>(g, encode, num_sms, pairs, err, st);
-  if (g.epi == 2) return launch_fmt<kEpiSiluClamp>(g, encode, num_sms, pairs, err, st);
-  if (g.epi == 3) return launch_fmt<kEpiSitu>(g, encode, num_sms, pairs, err, st);
-  return launch_fmt<kEpiBf16>(g, encode, num_sms, pairs, err, st);
+int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, int pairs, bool force_pairs,
+                        uint32_t* err, cudaStream_t st) {
+  if (g.epi == 1) return launch_fmt<kEpiSilu>(g, encode, num_sms, pairs, force_pairs, err, st);
+  if (g.epi == 2) return launch_fmt<kEpiSiluClamp>(g, encode, num_sms, pairs, force_pairs, err, st);
+  if (g.epi == 3) return launch_fmt<kEpiSitu>(g, encode, num_sms, pairs, force_pairs, err, st);
+  return launch_fmt<kEpiBf16>(g, encode, num_sms, pairs, force_pairs, err, st);
 }
 
 }  // namespace moe

@@ -70,10 +70,12 @@ cudaError_t init_grouped_gemm();
 // CTA pairs of the pair kernel resident at once on the current device (0: the
 // one-CTA kernel only); queried once per context.
 int grouped_gemm_pairs();
-// Returns MOE_OK or a MOE_ERR_* code. pairs > 0 and E <= 1024 take the
-// CTA-pair kernel with that many pairs, otherwise the one-CTA kernel.
-int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, int pairs, uint32_t* err,
-                        cudaStream_t st);
+// Returns MOE_OK or a MOE_ERR_* code. The CTA-pair kernel (at most `pairs`
+// pairs) runs when pairs > 0, E <= 1024 and either `force_pairs` or the
+// capacity holds at least 160 routed rows per expert beyond the alignment
+// gaps (cap - 127 E >= 160 E); otherwise the one-CTA kernel.
+int launch_grouped_gemm(const GemmArgs& g, EncodeTiledFn encode, int num_sms, int pairs, bool force_pairs,
+                        uint32_t* err, cudaStream_t st);
 
 cudaError_t init_decode();
 // mma.sync path when allowed and applicable (decode_mma_sync_ok), else the

@@ -172,8 +172,9 @@ def test_gemm_fp8_weight_recipes(ctx, orc, recipe):
 
 
 def context_with_pairs(n):
-    """A context whose grouped GEMM runs at most n CTA pairs (0: the one-CTA
-    kernel), through MOE_GEMM_CTA_PAIRS, read at context creation."""
+    """A context whose grouped GEMM always runs the two-SM kernel with at most
+    n CTA pairs (n = 0: always the one-CTA kernel), through
+    MOE_GEMM_CTA_PAIRS, read at context creation."""
     old = os.environ.get("MOE_GEMM_CTA_PAIRS")
     os.environ["MOE_GEMM_CTA_PAIRS"] = str(n)
     try:
@@ -195,7 +196,7 @@ def test_pair_kernel_equals_one_cta_kernel(ctx, orc, fmt):
     K with a partial group of four 128-blocks."""
     counts = [5, 0, 300, 129, 1, 256, 257, 128, 384]
     outs = []
-    for c in (ctx, context_with_pairs(2), context_with_pairs(0)):
+    for c in (context_with_pairs(1000), context_with_pairs(2), context_with_pairs(0)):
         got, ref, ends, ab = gemm_case(c, orc, counts, 768, 640, fmt, seed=8)
         assert_gemm_close(got, ref, ends, ab)
         outs.append(got)
@@ -211,8 +212,8 @@ def test_pair_kernel_fused_layer_equals_one_cta_kernel(orc, act):
     cfg = synth.FFNConfig("pair", T=900, E=7, k=3, H=512, I=512, seed=23, clamp=clamp, limit=2.5 if clamp else 0.0)
     inp = synth.ffn_inputs(cfg)
     res = []
-    for n in (None, 3, 0):
-        c = B.Context(0) if n is None else context_with_pairs(n)
+    for n in (1000, 3, 0):
+        c = context_with_pairs(n)
         layer = make_layer(c, cfg, inp, act_kind=kind)
         layer.act_fp8.fill_(0xAB)
         layer.act_sf.view(torch.uint8).fill_(0xAB)
