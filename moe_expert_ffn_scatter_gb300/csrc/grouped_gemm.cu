@@ -798,6 +798,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) grouped
       int s = 0;
       uint32_t ph = 0, acc_ph = 0;
       const uint32_t ibase = pr::idesc_base(kBfp4);
+      // shared-memory descriptors of stage 0's operands; a stage, a k-block
+      // within it and a 32-byte K step move only the start-address field (16-byte units)
+      const uint64_t da0 = desc_sw128(sbase + pr::OFF_A), db0 = desc_sw128(sbase + pr::OFF_B);
       bool ok = true;
       for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
         if (!(ok = pr::wait_phase_cluster(tmem_empty_bar, acc_ph ^ 1u, abort_flag, err))) break;
@@ -813,13 +816,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) grouped
           for (int b = 0; b < nsub; ++b) {
             const int kc = kc0 + b;
             const uint32_t tsfa = tsf + (a_g32 ? 4u * b : 0u), tsfb = tsf + 8u + 8u * b;
-            const uint32_t a_addr = sbase + pr::OFF_A + s * pr::A_BYTES + b * pr::A_SUB;
-            const uint32_t b_addr = sbase + pr::OFF_B + s * pr::B_BYTES + b * pr::B_SUB;
+            const uint64_t da = da0 + ((s * pr::A_BYTES + b * pr::A_SUB) >> 4);
+            const uint64_t db = db0 + ((s * pr::B_BYTES + b * pr::B_SUB) >> 4);
+            const uint32_t ib = ibase | ((uint32_t)(kc & 3) << 29);
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
-              const uint32_t idesc = ibase | ((uint32_t)k4 << 4) | ((uint32_t)(a_g32 ? k4 : (kc & 3)) << 29);
-              pr::mma_pair(tmem, desc_sw128(a_addr + 32u * k4), desc_sw128(b_addr + 32u * k4), idesc, tsfa, tsfb,
-                           (kc | k4) != 0);
+              const uint32_t idesc = a_g32 ? (ibase | ((uint32_t)k4 << 4) | ((uint32_t)k4 << 29)) : (ib | ((uint32_t)k4 << 4));
+              pr::mma_pair(tmem, da + 2u * k4, db + 2u * k4, idesc, tsfa, tsfb, (kc | k4) != 0);
             }
           }
           pr::commit_pair(empty_bar(s));
