@@ -184,9 +184,14 @@ typedef struct moe_act_params {
  * Sizes: T >= 0 (T == 0 writes expert_ends = 0 and nothing else; the
  *  per-token pointers may then be NULL),
  *  1 <= E <= 4096 (E <= 1024 for the two routing modes), 1 <= k <= min(E, 32),
- *  H % 128 == 0, A >= 1, cap >= T*k + E*(A-1). Logits must be finite.
+ *  H % 128 == 0, H <= 28,160 (the scatter quantises each token row into
+ *  shared memory first; larger H: MOE_ERR_UNSUPPORTED), A >= 1,
+ *  cap >= T*k + E*(A-1). Logits must be finite.
  * Errors: MOE_ERR_INVALID_ARG (null pointer, bad size), MOE_ERR_CAPACITY
- *  (cap below the bound above). */
+ *  (cap below the bound above), MOE_ERR_UNSUPPORTED (H above the limit).
+ * Launches: routing, rank/count (+ endpoints), scatter; the scatter starts
+ *  while rank/count still runs (programmatic dependent launch) and waits for
+ *  it before it reads anything rank/count writes. */
 typedef struct moe_route_args {
     int32_t routing_mode;
     const float* logits;

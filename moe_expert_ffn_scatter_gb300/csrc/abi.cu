@@ -101,7 +101,8 @@ MOE_API int moe_ctx_create(moe_ctx** out, int device) {
   }
   c->situ_bs = 4.0f;  // Kimi's SiTU pair, filled now so that ordinary use never refills
   c->situ_bl = 25.0f;
-  if (moe::init_grouped_gemm() != cudaSuccess || moe::init_decode() != cudaSuccess ||
+  if (moe::init_grouped_gemm() != cudaSuccess || moe::init_route_scatter() != cudaSuccess ||
+      moe::init_decode() != cudaSuccess ||
       moe::init_decode_gemm() != cudaSuccess ||
       cudaMemset(c->d_err, 0, sizeof(uint32_t)) != cudaSuccess ||
       moe::launch_silu_table(c->d_silu, 0) != cudaSuccess ||
@@ -176,6 +177,7 @@ static int check_route_args(const moe_route_args* a) {
   if (a->T > 0 && (!al(a->x, 16) || !al(a->a_fp8, 8) || !al(a->a_sf, 4))) return MOE_ERR_INVALID_ARG;
   if ((long)a->cap < (long)a->T * a->k + (long)a->E * (a->A - 1)) return MOE_ERR_CAPACITY;
   if ((long)a->cap * a->H > 0x7FFFFFFFFFFFL) return MOE_ERR_INVALID_ARG;
+  if (moe::scatter_stash_bytes(a->H, a->quant_group == 32) > moe::kScatterStashMax) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 

@@ -16,6 +16,11 @@ inline long lmax(long a, long b) { return a > b ? a : b; }
 constexpr int kScatterChunk = 64;
 
 size_t route_scatter_ws_bytes(int T, int E, int k);
+// Shared memory of a scatter block for rows of H columns (the per-warp stashes)
+// and its upper limit: larger H are refused by the route/scatter entry points.
+size_t scatter_stash_bytes(int H, bool g32);
+constexpr size_t kScatterStashMax = 227 * 1024;
+cudaError_t init_route_scatter();
 size_t route_scatter_noalloc_max_bytes();
 cudaError_t route_scatter_noalloc_scratch(void** addr);
 cudaError_t launch_route_scatter_noalloc(const moe_route_args& a, void* scratch, int num_sms, uint32_t* err,

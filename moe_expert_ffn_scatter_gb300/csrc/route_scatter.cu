@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "pipeline.cuh"
 
 namespace moe {
 
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(256) rank_count_kernel(const int32_t* __restri
                                                          int32_t* __restrict__ s2d, int32_t* __restrict__ ws,
                                                          int T, int E, int k, int A, int32_t* __restrict__ ends,
                                                          long cap, uint32_t* err) {
+  pdl_launch_dependents();  // the scatter launch may start quantising its rows now
   extern __shared__ int32_t smem_i32[];
   int32_t* cnt = smem_i32;                 // [E] running count per expert
   int32_t* ids_s = smem_i32 + E;           // [kScatterChunk * k] the chunk's expert ids
@@ -322,6 +324,14 @@ __device__ __forceinline__ uint32_t e4m3x4(const float* f, float sc) {
          (e4m3x2_satfinite(__fmul_rn(f[2], sc), __fmul_rn(f[3], sc)) << 16);
 }
 
+// One warp per token, in two phases. Before griddepcontrol.wait, which
+// returns once the rank/count launch has completed (the kernel is launched to
+// start while that launch still runs): the token row is quantised once (16
+// lanes per 128-column group, or 4 per 32-column group in the MXFP8 recipe;
+// uint4 loads, four in flight per lane) into the warp's shared-memory stash,
+// codes then scale bytes. After it: the final src2dst of each slot and the
+// copies of the stash to every destination row (16-byte stores) and of the
+// scale bytes, as packed words, to every destination's column of a_sf.
 __global__ void __launch_bounds__(256) scatter_quant_kernel(const uint16_t* __restrict__ x,
                                                             const int32_t* __restrict__ ids,
                                                             int32_t* __restrict__ s2d,
@@ -331,27 +341,17 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(const uint16_t* __re
                                                             int32_t* __restrict__ a_sf, int T, int E,
                                                             int k, int A, int H, int ld_sf, long cap,
                                                             bool g32, uint32_t* err) {
+  extern __shared__ __align__(16) uint8_t stash_all[];
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
-  const int G = H / 128;
+  const int nsb = g32 ? H / 32 : H / 128;  // scale bytes of a row
+  const int nwords = (nsb + 3) / 4;         // packed scale words of a row
+  const int stride = H + (nsb + 15) / 16 * 16;
+  uint8_t* stash = stash_all + (size_t)(threadIdx.x >> 5) * stride;
   const int npass = (H + 255) / 256;
+  bool waited = false;
   for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
-    int dst = -1;
-    if (lane < k) {
-      const int e = ids[(size_t)t * k + lane];
-      const int lr = s2d[(size_t)t * k + lane];
-      if (e >= 0 && e < E && lr >= 0) {
-        const int start = (e == 0) ? 0 : (int)align_up64(ends[e - 1], A);
-        dst = start + ws[(size_t)(t / kScatterChunk) * E + e] + lr;
-        if ((long)dst >= cap) {
-          raise_error(err, MOE_DEVERR_CAPACITY);
-          dst = -1;
-        }
-      }
-      s2d[(size_t)t * k + lane] = dst;
-    }
     const uint16_t* xr = x + (size_t)t * H;
-    uint32_t word = 0;
     for (int it0 = 0; it0 < npass; it0 += 4) {
       uint4 v[4];
 #pragma unroll
@@ -377,38 +377,67 @@ __global__ void __launch_bounds__(256) scatter_quant_kernel(const uint16_t* __re
         for (int o = g32 ? 2 : 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
         const uint32_t b = active ? group_scale_byte(amax) : 0u;
         const float sc = pow2_f32(127 - (int)b);
-        uint2 codes;
-        codes.x = e4m3x4(f, sc);
-        codes.y = e4m3x4(f + 4, sc);
-        for (int j = 0; j < k; ++j) {
-          const int d = __shfl_sync(kFull, dst, j);
-          if (d >= 0 && active) *reinterpret_cast<uint2*>(a_fp8 + (size_t)d * H + col) = codes;
-        }
-        if (g32) {
-          // each half-warp covers 128 columns: its four group bytes, lanes
-          // 0/4/8/12 (+16), make one word
-          uint32_t w2[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            w2[h] = __shfl_sync(kFull, b, 16 * h) | (__shfl_sync(kFull, b, 16 * h + 4) << 8) |
-                    (__shfl_sync(kFull, b, 16 * h + 8) << 16) | (__shfl_sync(kFull, b, 16 * h + 12) << 24);
-          if (dst >= 0) {
-            a_sf[(size_t)(2 * it) * ld_sf + dst] = (int32_t)w2[0];
-            if (it * 256 + 128 < H) a_sf[(size_t)(2 * it + 1) * ld_sf + dst] = (int32_t)w2[1];
-          }
-          continue;
-        }
-        const uint32_t b_lo = __shfl_sync(kFull, b, 0);
-        const uint32_t b_hi = __shfl_sync(kFull, b, 16);
-        const int g0 = 2 * it;
-        word |= b_lo << (8 * (g0 & 3));
-        if (g0 + 1 < G) word |= b_hi << (8 * ((g0 + 1) & 3));
-        if (((g0 + 1) & 3) == 3 || g0 + 2 >= G) {
-          if (dst >= 0) a_sf[(size_t)(g0 >> 2) * ld_sf + dst] = (int32_t)word;
-          word = 0;
+        if (active) {
+          uint2 codes;
+          codes.x = e4m3x4(f, sc);
+          codes.y = e4m3x4(f + 4, sc);
+          *reinterpret_cast<uint2*>(stash + col) = codes;
+          if ((lane & (g32 ? 3 : 15)) == 0) stash[H + (g32 ? col / 32 : col / 128)] = (uint8_t)b;
         }
       }
     }
+    __syncwarp();
+    if (!waited) {
+      pdl_wait();  // src2dst ranks, chunk prefixes and endpoints are complete from here on
+      waited = true;
+    }
+    int dst = -1;
+    if (lane < k) {
+      const int e = ids[(size_t)t * k + lane];
+      const int lr = s2d[(size_t)t * k + lane];
+      if (e >= 0 && e < E && lr >= 0) {
+        const int start = (e == 0) ? 0 : (int)align_up64(ends[e - 1], A);
+        dst = start + ws[(size_t)(t / kScatterChunk) * E + e] + lr;
+        if ((long)dst >= cap) {
+          raise_error(err, MOE_DEVERR_CAPACITY);
+          dst = -1;
+        }
+      }
+      s2d[(size_t)t * k + lane] = dst;
+    }
+    // codes: 16 bytes per lane per step, four steps in registers, stored to every destination
+    const int n16 = H / 16;
+    for (int c0 = 0; c0 < n16; c0 += 128) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + 32 * u + lane;
+        if (c < n16) v[u] = *reinterpret_cast<const uint4*>(stash + 16 * c);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int d = __shfl_sync(kFull, dst, j);
+        if (d < 0) continue;
+        uint8_t* row = a_fp8 + (size_t)d * H;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + 32 * u + lane;
+          if (c < n16) *reinterpret_cast<uint4*>(row + 16 * c) = v[u];
+        }
+      }
+    }
+    // scale words: byte (g % 4) of word g / 4, unused bytes of the last word 0
+    for (int w0 = 0; w0 < nwords; w0 += 32) {
+      const int w = w0 + lane;
+      uint32_t word = 0;
+      if (w < nwords)
+        for (int i = 0; i < 4; ++i)
+          if (4 * w + i < nsb) word |= (uint32_t)stash[H + 4 * w + i] << (8 * i);
+      for (int j = 0; j < k; ++j) {
+        const int d = __shfl_sync(kFull, dst, j);
+        if (d >= 0 && w < nwords) a_sf[(size_t)w * ld_sf + d] = (int32_t)word;
+      }
+    }
+    __syncwarp();  // the stash is refilled by the warp's next token
   }
 }
 
@@ -433,6 +462,18 @@ cudaError_t dispatch_epl(const moe_route_args& a, int num_sms, unsigned int* don
 }
 
 }  // namespace
+
+// Shared memory of a scatter block: eight warps' stashes of a quantised row
+// (H codes, then the scale bytes rounded up to 16).
+size_t scatter_stash_bytes(int H, bool g32) {
+  const int nsb = g32 ? H / 32 : H / 128;
+  return (size_t)8 * (size_t)(H + (nsb + 15) / 16 * 16);
+}
+
+cudaError_t init_route_scatter() {
+  return cudaFuncSetAttribute(scatter_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kScatterStashMax);
+}
 
 // Chunk histograms [nchunks][E] int32, then the 4-byte completion count of
 // the rank/count launch, rounded up to 16 bytes.
@@ -469,10 +510,10 @@ cudaError_t launch_route_scatter(const moe_route_args& a, int num_sms, uint32_t*
                                                   a.cap, err);
     if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
     const int blocks = (int)lmin((a.T + 7) / 8, (long)num_sms * 16);
-    scatter_quant_kernel<<<blocks, 256, 0, st>>>(a.x, a.topk_ids, a.src2dst, (const int32_t*)ws, a.expert_ends,
-                                                 a.a_fp8, a.a_sf, a.T, a.E, a.k, a.A, a.H,
-                                                 (int)align_up64(a.cap, 4), a.cap, a.quant_group == 32, err);
-    return cudaGetLastError();
+    return launch_maybe_pdl(scatter_quant_kernel, dim3(blocks), dim3(256), scatter_stash_bytes(a.H, a.quant_group == 32),
+                            st, true, a.x, (const int32_t*)a.topk_ids, a.src2dst, (const int32_t*)ws,
+                            (const int32_t*)a.expert_ends, a.a_fp8, a.a_sf, a.T, a.E, a.k, a.A, a.H,
+                            (int)align_up64(a.cap, 4), (long)a.cap, a.quant_group == 32, err);
   }
   // no tokens: every expert is empty
   endpoints_kernel<<<1, 1024, (size_t)a.E * sizeof(int32_t), st>>>(nullptr, ws, 0, a.E, a.A, a.expert_ends, a.cap,
