@@ -158,6 +158,7 @@ __global__ void weighted_sum_kernel(const uint16_t* __restrict__ y2, const int32
                                     const float* __restrict__ topk_w, int T, int k, int expert_start,
                                     int n_local, int H, uint16_t* __restrict__ out) {
   pdl_wait();
+  pdl_launch_dependents();  // a dependent kernel waits for this grid before reading `out`
   const long total = (long)T * H;
   for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long)gridDim.x * blockDim.x) {
@@ -177,22 +178,24 @@ __global__ void weighted_sum_kernel(const uint16_t* __restrict__ y2, const int32
 // For T <= 8 tokens the two GEMVs are skinny GEMMs: [16 weight rows] x [K] x
 // [8 token columns]. One CTA per SM walks a contiguous range of tiles; a tile
 // is 16 rows of one distinct local expert, so every selected expert's weights
-// are read once however many tokens chose it. Warp 8 (one lane) is the
-// producer: it bulk-copies the tile's rows (and MXFP4 scale bytes) into a
-// ring of shared-memory stages. Warps 0-7 split K: each converts its weight
-// slices in registers (e4m3x2 / e2m1x2 -> f16x2, exact) and runs
-// mma.sync m16n8k16 (f16 x f16 -> f32) against the token columns, staged as
-// f16 scaled per token by a power of two so that no bf16 value overflows or
-// loses bits in f16. The eight partial tiles are summed in warp order, scaled
-// back, and written to every (token, slot) that selected the expert; the
-// first launch applies the GLU to its gate/up row pairs on the way out.
+// are read once however many tokens chose it. Warp 16 is the producer: its
+// lanes 0-15 bulk-copy the tile's rows, one each, and lane 0 the bias (and
+// MXFP4 scale bytes), into a ring of shared-memory stages. Warps 0-15 split
+// K: each converts its weight slices in registers (e4m3x2 / e2m1x2 -> f16x2,
+// exact) and runs mma.sync m16n8k16 (f16 x f16 -> f32) against the token
+// columns, staged as f16 scaled per token by a power of two so that no bf16
+// value overflows or loses bits in f16. The sixteen partial tiles are summed
+// in warp order, scaled back, and written to every (token, slot) that
+// selected the expert; the first launch applies the GLU to its gate/up row
+// pairs on the way out.
 constexpr int kTcRows = 16;       // MMA M: weight rows per tile / stage
 constexpr int kTcTok = 8;         // MMA N: token columns
 constexpr int kTcConsumers = 16;  // warps splitting K
 constexpr int kTcThreads = (kTcConsumers + 1) * 32;
 constexpr int kTcMaxStages = 8;
 constexpr int kTcMaxSlots = 256;  // T * k
-constexpr size_t kTcSmemMax = 200 * 1024;
+// dynamic shared memory: 227 KB per block less the kernel's static arrays
+constexpr size_t kTcSmemMax = 222 * 1024;
 
 struct TcArgs {
   const uint16_t* x;      // x [T][K] (per_slot = 0) or act [T*k][K] (per_slot = 1)
@@ -252,8 +255,11 @@ template <int WFMT>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int K = a.K, N = a.N, nst = a.nst;
-  uint8_t* xs = smem;                                                          // [8][x_stride] f16 columns
-  float* red = reinterpret_cast<float*>(smem + (size_t)kTcTok * a.x_stride);  // [2][warps][128]
+  // token columns: min(T, 8) of them; MMA columns >= T read column T - 1
+  // (their outputs are never written), so the buffer is sized by T
+  const int xcols = a.T < kTcTok ? a.T : kTcTok;
+  uint8_t* xs = smem;                                                      // [xcols][x_stride] f16 columns
+  float* red = reinterpret_cast<float*>(smem + (size_t)xcols * a.x_stride);  // [2][warps][128]
   uint8_t* stages = reinterpret_cast<uint8_t*>(red + 2 * kTcConsumers * 128);
   uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (size_t)nst * a.stage_bytes);  // full[nst], empty[nst]
   __shared__ int uniq[kTcMaxSlots];
@@ -270,8 +276,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
   const size_t row_bytes = (WFMT == MOE_WFMT_FP8_PER_EXPERT) ? (size_t)K : (size_t)K / 2;
   const int sf_row = K / 32;
   const int TK = a.T * a.k;
-  // The next kernel (second GEMV, or the weighted sum) may be scheduled as
-  // soon as SMs free up; it waits for this one before reading its outputs.
+  // The first launch may read routing, token rows or weights that the kernel
+  // before it on the stream wrote, so it waits for that kernel before it reads
+  // anything, and only then lets the second GEMV be scheduled (which reads the
+  // routing ids before its own wait, and the first launch's activations after
+  // it). The weighted sum waits for the second launch before reading y2.
+  if (!a.per_slot) pdl_wait();
   pdl_launch_dependents();
 
   const int words = K / 2;
@@ -362,21 +372,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
 
   if (warp == kTcConsumers) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // Lane r < 16 copies stage row r (the rows' copies are issued in
+    // parallel); lane 0 also arms the stage and copies its bias and scales.
+    {
       int n = 0;
       for (int tile = t_begin; tile < t_end; ++tile, ++n) {
         const int lid = uniq[tile / tps], q = tile % tps;
         const int s = n % nst;
-        if (n >= nst && !pipe_wait(smem_addr(bars + nst + s), ((n / nst) & 1) ^ 1, abort_v, a.err)) break;
+        int okw = 1;
+        if (lane == 0 && n >= nst) okw = pipe_wait(smem_addr(bars + nst + s), ((n / nst) & 1) ^ 1, abort_v, a.err);
+        if (!__shfl_sync(kFull, okw, 0)) break;
         const uint32_t full = smem_addr(bars + s);
         uint8_t* st = stages + (size_t)s * a.stage_bytes;
         const uint8_t* wexp = a.W + (size_t)lid * N * row_bytes;
         const uint16_t* bexp = a.bias + (size_t)lid * N;
         const uint32_t sf_bytes = (WFMT == MOE_WFMT_MXFP4_G32) ? (uint32_t)(kTcRows * sf_row) : 0u;
-        pipe_mbar_expect_tx(full, (uint32_t)(kTcRows * row_bytes) + sf_bytes + kTcRows * 2);
-        for (int r = 0; r < kTcRows; ++r)
-          pipe_bulk_load(smem_addr(st + (size_t)r * a.row_stride), wexp + (size_t)tc_src_row(a, q, r) * row_bytes,
+        if (lane == 0) pipe_mbar_expect_tx(full, (uint32_t)(kTcRows * row_bytes) + sf_bytes + kTcRows * 2);
+        __syncwarp();
+        if (lane < kTcRows)
+          pipe_bulk_load(smem_addr(st + (size_t)lane * a.row_stride), wexp + (size_t)tc_src_row(a, q, lane) * row_bytes,
                          (uint32_t)row_bytes, full);
+        if (lane != 0) continue;
         const bool halves = a.glu && !a.interleaved;
         const int run0 = halves ? 8 * q : kTcRows * q;  // first source row of each block run
         const int run1 = halves ? a.I + 8 * q : 0;
@@ -391,8 +407,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
                            (uint32_t)(8 * sf_row), full);
         }
       }
-      for (int m = (n > nst ? n - nst : 0); m < n; ++m)
-        pipe_wait(smem_addr(bars + (m % nst)), (m / nst) & 1, abort_v, a.err, false);
+      n = __shfl_sync(kFull, n, 0);
+      if (lane == 0)
+        for (int m = (n > nst ? n - nst : 0); m < n; ++m)
+          pipe_wait(smem_addr(bars + (m % nst)), (m / nst) & 1, abort_v, a.err, false);
     }
     return;
   }
@@ -450,7 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
     if (ok) {
       const uint8_t* rowA = st + (size_t)g * a.row_stride;
       const uint8_t* rowB = st + (size_t)(g + 8) * a.row_stride;
-      const uint8_t* xg = xs + (size_t)g * a.x_stride;
+      const uint8_t* xg = xs + (size_t)(g < xcols ? g : xcols - 1) * a.x_stride;
       if (WFMT == MOE_WFMT_FP8_PER_EXPERT) {
         float d2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int kb = warp; kb < K / 64; kb += kTcConsumers) {
@@ -583,7 +601,8 @@ static uint32_t pad_to(uint32_t v, uint32_t residue) {  // smallest >= v with v 
 }
 
 template <int WFMT>
-TcGeom tc_geom(int K) {
+TcGeom tc_geom(int K, int T) {
+  const size_t xcols = (size_t)(T < kTcTok ? (T > 1 ? T : 1) : kTcTok);
   TcGeom g{};
   const uint32_t rb = (WFMT == MOE_WFMT_FP8_PER_EXPERT) ? (uint32_t)K : (uint32_t)K / 2;
   g.row_stride = pad_to(rb, (WFMT == MOE_WFMT_FP8_PER_EXPERT) ? 64u : 16u);
@@ -592,14 +611,14 @@ TcGeom tc_geom(int K) {
   g.bias_offset = (g.sf_offset + sf + 15u) / 16u * 16u;
   g.stage_bytes = (g.bias_offset + kTcRows * 2 + 127u) / 128u * 128u;
   g.x_stride = pad_to(2u * (uint32_t)K, (WFMT == MOE_WFMT_FP8_PER_EXPERT) ? 16u : 64u);
-  const size_t fixed = (size_t)kTcTok * g.x_stride + 2 * kTcConsumers * 128 * sizeof(float) +
+  const size_t fixed = xcols * g.x_stride + 2 * kTcConsumers * 128 * sizeof(float) +
                        2 * kTcMaxStages * sizeof(uint64_t);
   g.nst = 0;
   if (fixed < kTcSmemMax) {
     const size_t n = (kTcSmemMax - fixed) / g.stage_bytes;
     g.nst = (int)(n < (size_t)kTcMaxStages ? n : (size_t)kTcMaxStages);
   }
-  g.smem = (size_t)kTcTok * g.x_stride + 2 * kTcConsumers * 128 * sizeof(float) + (size_t)g.nst * g.stage_bytes +
+  g.smem = xcols * g.x_stride + 2 * kTcConsumers * 128 * sizeof(float) + (size_t)g.nst * g.stage_bytes +
            2 * (size_t)g.nst * sizeof(uint64_t);
   return g;
 }
@@ -609,12 +628,12 @@ TcGeom tc_geom(int K) {
 // at least two stages.
 template <int WFMT>
 bool tc_ok(int T, int k, int N, int K) {
-  return T <= kTcTok && T * k <= kTcMaxSlots && N % kTcRows == 0 && K % 64 == 0 && tc_geom<WFMT>(K).nst >= 2;
+  return T <= kTcTok && T * k <= kTcMaxSlots && N % kTcRows == 0 && K % 64 == 0 && tc_geom<WFMT>(K, T).nst >= 2;
 }
 
 template <int WFMT>
 cudaError_t launch_tc(TcArgs s, int num_sms, cudaStream_t st, bool pdl) {
-  const TcGeom g = tc_geom<WFMT>(s.K);
+  const TcGeom g = tc_geom<WFMT>(s.K, s.T);
   s.nst = g.nst;
   s.stage_bytes = g.stage_bytes;
   s.row_stride = g.row_stride;
@@ -656,7 +675,7 @@ cudaError_t launch_decode_tc(const moe_decode_args& a, const float* gu_scale, co
   s.limit = a.glu_limit;
   s.y = a.y1;
   s.act = a.act;
-  cudaError_t ce = launch_tc<WFMT>(s, num_sms, st, false);
+  cudaError_t ce = launch_tc<WFMT>(s, num_sms, st, true);
   if (ce != cudaSuccess) return ce;
   // GEMV 2
   s.x = a.act;
