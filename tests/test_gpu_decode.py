@@ -1,5 +1,5 @@
 """Sparse decode path on the GPU against the oracle: FP8-per-expert and MXFP4
-weights; the mma.sync path (T in {1, 2, 4, 8}, no workspace) and the tcgen05
+weights; the mma.sync path (T in {1, ..., 8}, no workspace) and the tcgen05
 path (workspace given, T up to 128); non-local slots never written and
 skipped."""
 import numpy as np
@@ -76,6 +76,22 @@ def test_decode_gpt_oss_shape(ctx, orc, wfmt, T, ws):
     H = I = synth.DECODE_H
     y1, act, y2, out, loc = run_decode(ctx, d, ids, w, wfmt, H, I, 0, synth.DECODE_E, ws=ws)
     check_decode_stages(orc, d.x, ids, w, loc, wfmt, H, I, (y1, act, y2, out), split=ws)
+
+
+@WFMTS
+@pytest.mark.parametrize("layout", [B.MOE_GLU_INTERLEAVED, B.MOE_GLU_HALVES], ids=["interleaved", "halves"])
+@pytest.mark.parametrize("T", [3, 5, 7])
+def test_decode_mma_sync_odd_token_counts(ctx, orc, wfmt, layout, T):
+    """The mma.sync path stages min(T, 8) token columns; the MMA's columns
+    beyond T read column T - 1 and their outputs are never written. Odd T in
+    both GLU layouts, the path forced."""
+    d = inputs(T, seed=33)
+    ids, w = orc.route_softmax_topk(d.logits, synth.DECODE_K)
+    H = I = synth.DECODE_H
+    y1, act, y2, out, loc = run_decode(ctx, d, ids, w, wfmt, H, I, 0, synth.DECODE_E, glu_layout=layout,
+                                       path=B.MOE_DECODE_MMA_SYNC)
+    check_decode_stages(orc, d.x, ids, w, loc, wfmt, H, I, (y1, act, y2, out),
+                        interleaved=layout == B.MOE_GLU_INTERLEAVED)
 
 
 @WFMTS
