@@ -184,14 +184,21 @@ __global__ void weighted_sum_kernel(const uint16_t* __restrict__ y2, const int32
 // K: each converts its weight slices in registers (e4m3x2 / e2m1x2 -> f16x2,
 // exact) and runs mma.sync m16n8k16 (f16 x f16 -> f32) against the token
 // columns, staged as f16 scaled per token by a power of two so that no bf16
-// value overflows or loses bits in f16. The sixteen partial tiles are summed
-// in warp order, scaled back, and written to every (token, slot) that
-// selected the expert; the first launch applies the GLU to its gate/up row
-// pairs on the way out.
+// value overflows or loses bits in f16, and leaves its partial tile in one of
+// two reduction buffers. Warps 17-20 sum the sixteen partial tiles in warp
+// order, scale them back and write every (token, slot) that selected the
+// expert (the first launch applies the GLU to its gate/up row pairs on the
+// way out) while the compute warps go on with the next tile. Each buffer b
+// is handed over through its own pair of named barriers, 2 + b (partials
+// written: the compute warps arrive, the epilogue warps wait) and 4 + b
+// (buffer free again: the other way round), so a barrier never has two
+// generations in flight.
 constexpr int kTcRows = 16;       // MMA M: weight rows per tile / stage
 constexpr int kTcTok = 8;         // MMA N: token columns
 constexpr int kTcConsumers = 16;  // warps splitting K
-constexpr int kTcThreads = (kTcConsumers + 1) * 32;
+constexpr int kTcEpiWarps = 4;    // warps summing the partial tiles and storing the outputs
+constexpr int kTcThreads = (kTcConsumers + 1 + kTcEpiWarps) * 32;
+constexpr int kTcBarThreads = (kTcConsumers + kTcEpiWarps) * 32;  // compute + epilogue warps
 constexpr int kTcMaxStages = 8;
 constexpr int kTcMaxSlots = 256;  // T * k
 // dynamic shared memory: 227 KB per block less the kernel's static arrays
@@ -268,7 +275,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
   __shared__ int n_uniq;
   __shared__ int warp_cnt[kTcThreads / 32];
   __shared__ int xexp[kTcTok];
-  __shared__ float wmax[kTcThreads / 32][kTcTok];  // per-warp max |x| of each column
+  __shared__ float wmax[kTcConsumers][kTcTok];  // per-compute-warp max |x| of each column
+  __shared__ float tile_sc[2][kTcTok];          // per reduction buffer: column scales 2^xexp * weight scale
+  __shared__ uint16_t tile_bias[2][kTcRows];    // per reduction buffer: the tile's bias, source order
   __shared__ float wsc;
   __shared__ int abort_flag;
   volatile int* abort_v = &abort_flag;
@@ -415,6 +424,55 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
     return;
   }
 
+  if (warp > kTcConsumers) {
+    // ------------------------------------------------------------ epilogue
+    // Thread i < nout owns one output pair (GLU: the gate and up row of one
+    // intermediate index, one column) or one output (row, column) of the
+    // 16 x 8 tile.
+    const int et = (int)threadIdx.x - (kTcConsumers + 1) * 32;
+    const int nout = a.glu ? 64 : 128;
+    const int o_l = a.glu ? (et >> 1) : (et >> 2);
+    const int o_c = a.glu ? (et & 1) : (et & 3);
+    const int gl = o_l >> 2;
+    const int col = 2 * (o_l & 3) + (o_c & 1);
+    const int r_out = a.glu ? gl : gl + 8 * (o_c >> 1);  // stage row of the (first) output
+    int n = 0;
+    for (int tile = t_begin; tile < t_end; ++tile, ++n) {
+      const int b = n & 1, u = tile / tps, q = tile % tps;
+      named_barrier(2 + b, kTcBarThreads);  // the compute warps have written tile n's buffer
+      const float* rb = red + (size_t)b * kTcConsumers * 128;
+      const int j = (et < nout && col < a.T) ? slot_tab[u][col] : -1;
+      if (j >= 0 && !*abort_v) {
+        const int sl = col * a.k + j;
+        const float sc = tile_sc[b][col];
+        const float bias0 = bf16_to_f32(tile_bias[b][tc_blk_row(a, r_out)]);
+        if (a.glu) {
+          const float bias1 = bf16_to_f32(tile_bias[b][tc_blk_row(a, gl + 8)]);
+          float v0 = 0.0f, v1 = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kTcConsumers; ++w) {
+            v0 += rb[w * 128 + o_l * 4 + o_c];
+            v1 += rb[w * 128 + o_l * 4 + 2 + o_c];
+          }
+          const int r0 = tc_src_row(a, q, gl), r1 = tc_src_row(a, q, gl + 8);
+          const uint16_t y0 = (uint16_t)f32_to_bf16_bits(fmaf(v0, sc, bias0));
+          const uint16_t y1 = (uint16_t)f32_to_bf16_bits(fmaf(v1, sc, bias1));
+          a.y[(size_t)sl * N + r0] = y0;
+          a.y[(size_t)sl * N + r1] = y1;
+          a.act[(size_t)sl * a.I + 8 * q + gl] =
+              (uint16_t)f32_to_bf16_bits(glu_value(bf16_to_f32(y0), bf16_to_f32(y1), a.alpha, a.beta, a.limit));
+        } else {
+          float v = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kTcConsumers; ++w) v += rb[w * 128 + o_l * 4 + o_c];
+          a.y[(size_t)sl * N + tc_src_row(a, q, r_out)] = (uint16_t)f32_to_bf16_bits(fmaf(v, sc, bias0));
+        }
+      }
+      named_barrier_arrive(4 + b, kTcBarThreads);  // buffer b is free again
+    }
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   constexpr int kCT = kTcConsumers * 32;
   // slot table: token t's slot j (if any) that chose expert u
@@ -440,12 +498,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
   bool ok = true;
   int n = 0;
   for (int tile = t_begin; tile < t_end; ++tile, ++n) {
-    const int u = tile / tps, q = tile % tps;
+    const int u = tile / tps;
     const int lid = uniq[u];
     if (u != cur_u) {
       // New expert: the f16 token columns (once, or per expert when the
       // columns are the slots' own activation rows) with their exponents.
-      named_barrier(1, kCT);  // the previous tile's epilogue is done
+      named_barrier(1, kCT);  // every compute warp is done with the previous expert's columns
       if (a.per_slot) {
         // the columns are the activation rows of the slots that chose the
         // expert: the previous kernel's output
@@ -510,61 +568,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
         }
       }
     }
-    // Sum the K slices in warp order, then the epilogue.
-    float* rb = red + (size_t)(n & 1) * kTcConsumers * 128;
-    *reinterpret_cast<float4*>(rb + warp * 128 + lane * 4) = make_float4(d[0], d[1], d[2], d[3]);
-    // the bias of the tile, read from the stage before it is released
-    const uint16_t* bst = reinterpret_cast<const uint16_t*>(st + a.bias_offset);
-    const int nout = a.glu ? 64 : 128;
-    float bias0 = 0.0f, bias1 = 0.0f;
-    int o_l = 0, o_c = 0;
-    if (threadIdx.x < nout) {
-      o_l = a.glu ? (int)(threadIdx.x >> 1) : (int)(threadIdx.x >> 2);
-      o_c = a.glu ? (int)(threadIdx.x & 1) : (int)(threadIdx.x & 3);
-      const int gl = o_l >> 2;
-      const int r0 = a.glu ? gl : gl + 8 * (o_c >> 1);
-      if (ok) {
-        bias0 = bf16_to_f32(bst[tc_blk_row(a, r0)]);
-        if (a.glu) bias1 = bf16_to_f32(bst[tc_blk_row(a, gl + 8)]);
-      }
-    }
-    // The bias values above are read from the stage (generic proxy) but used
-    // only after its release; the next bulk copy (async proxy) may refill the
-    // stage as soon as the empty barrier completes, so fence the reads first.
+    // Warp 0 takes the tile's bias out of the stage; the stage is released
+    // once every compute warp is done with it (generic-proxy reads of the
+    // stage are fenced before the next bulk copy refills it).
+    uint16_t bias_v = 0;
+    if (warp == 0 && lane < kTcRows && ok) bias_v = reinterpret_cast<const uint16_t*>(st + a.bias_offset)[lane];
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     named_barrier(1, kCT);
     if (threadIdx.x == 0 && ok) pipe_mbar_arrive(smem_addr(bars + nst + s));
-    if (ok && threadIdx.x < nout) {
-      const int gl = o_l >> 2;
-      const int col = 2 * (o_l & 3) + (o_c & 1);
-      const int j = (col < a.T) ? slot_tab[u][col] : -1;
-      if (j >= 0) {
-        const int sl = col * a.k + j;
-        const float sc = pow2_f32(xexp[col]) * wsc;
-        if (a.glu) {
-          float v0 = 0.0f, v1 = 0.0f;
-#pragma unroll
-          for (int w = 0; w < kTcConsumers; ++w) {
-            v0 += rb[w * 128 + o_l * 4 + o_c];
-            v1 += rb[w * 128 + o_l * 4 + 2 + o_c];
-          }
-          const int r0 = tc_src_row(a, q, gl), r1 = tc_src_row(a, q, gl + 8);
-          const uint16_t y0 = (uint16_t)f32_to_bf16_bits(fmaf(v0, sc, bias0));
-          const uint16_t y1 = (uint16_t)f32_to_bf16_bits(fmaf(v1, sc, bias1));
-          a.y[(size_t)sl * N + r0] = y0;
-          a.y[(size_t)sl * N + r1] = y1;
-          a.act[(size_t)sl * a.I + 8 * q + gl] =
-              (uint16_t)f32_to_bf16_bits(glu_value(bf16_to_f32(y0), bf16_to_f32(y1), a.alpha, a.beta, a.limit));
-        } else {
-          float v = 0.0f;
-#pragma unroll
-          for (int w = 0; w < kTcConsumers; ++w) v += rb[w * 128 + o_l * 4 + o_c];
-          const int r = tc_src_row(a, q, gl + 8 * (o_c >> 1));
-          a.y[(size_t)sl * N + r] = (uint16_t)f32_to_bf16_bits(fmaf(v, sc, bias0));
-        }
-      }
+    // The partial tile, the bias and the column scales into reduction buffer
+    // b, free once the epilogue warps are done with tile n - 2.
+    const int b = n & 1;
+    if (n >= 2) named_barrier(4 + b, kTcBarThreads);
+    float* rb = red + (size_t)b * kTcConsumers * 128;
+    *reinterpret_cast<float4*>(rb + warp * 128 + lane * 4) = make_float4(d[0], d[1], d[2], d[3]);
+    if (warp == 0) {
+      if (lane < kTcRows) tile_bias[b][lane] = bias_v;
+      if (lane < kTcTok) tile_sc[b][lane] = lane < a.T ? pow2_f32(xexp[lane]) * wsc : 0.0f;
     }
+    named_barrier_arrive(2 + b, kTcBarThreads);  // tile n to the epilogue warps
   }
+  // the epilogue warps' releases of the last two buffers
+  for (int m = (n > 2 ? n - 2 : 0); m < n; ++m) named_barrier(4 + (m & 1), kTcBarThreads);
 }
 
 template <int WFMT>

@@ -82,6 +82,12 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Arrival on a named barrier without waiting for it (the producer side of a
+// producer / consumer hand-over; the consumers bar.sync on the same id).
+__device__ __forceinline__ void named_barrier_arrive(int id, int threads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // Launch, optionally with programmatic stream serialization (the kernel may
 // start before the previous kernel of the stream has finished).
 template <typename... KArgs, typename... Args>
