@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
       abort_flag = 0;
       for (int s2 = 0; s2 < nst; ++s2) {
         pipe_mbar_init(smem_addr(bars + s2), 1);
-        pipe_mbar_init(smem_addr(bars + nst + s2), 1);
+        pipe_mbar_init(smem_addr(bars + nst + s2), kTcConsumers);  // one arrive per compute warp
       }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -568,14 +568,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
         }
       }
     }
-    // Warp 0 takes the tile's bias out of the stage; the stage is released
-    // once every compute warp is done with it (generic-proxy reads of the
-    // stage are fenced before the next bulk copy refills it).
+    // Warp 0 takes the tile's bias out of the stage; each compute warp
+    // releases the stage when it is done with it (its generic-proxy reads
+    // fenced before the next bulk copy refills the stage): the stage's empty
+    // barrier completes once all sixteen have.
     uint16_t bias_v = 0;
     if (warp == 0 && lane < kTcRows && ok) bias_v = reinterpret_cast<const uint16_t*>(st + a.bias_offset)[lane];
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    named_barrier(1, kCT);
-    if (threadIdx.x == 0 && ok) pipe_mbar_arrive(smem_addr(bars + nst + s));
+    __syncwarp();
+    if (lane == 0 && ok) pipe_mbar_arrive(smem_addr(bars + nst + s));
     // The partial tile, the bias and the column scales into reduction buffer
     // b, free once the epilogue warps are done with tile n - 2.
     const int b = n & 1;
