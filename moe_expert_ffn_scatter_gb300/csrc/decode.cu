@@ -185,12 +185,12 @@ __global__ void weighted_sum_kernel(const uint16_t* __restrict__ y2, const int32
 // exact) and runs mma.sync m16n8k16 (f16 x f16 -> f32) against the token
 // columns, staged as f16 scaled per token by a power of two so that no bf16
 // value overflows or loses bits in f16, and leaves its partial tile in one of
-// two reduction buffers. Warps 17-20 sum the sixteen partial tiles in warp
+// kTcRedBufs reduction buffers. Warps 17-20 sum the sixteen partial tiles in warp
 // order, scale them back and write every (token, slot) that selected the
 // expert (the first launch applies the GLU to its gate/up row pairs on the
 // way out) while the compute warps go on with the next tile. Each buffer b
 // is handed over through its own pair of named barriers, 2 + b (partials
-// written: the compute warps arrive, the epilogue warps wait) and 4 + b
+// written: the compute warps arrive, the epilogue warps wait) and 2 + R + b
 // (buffer free again: the other way round), so a barrier never has two
 // generations in flight.
 constexpr int kTcRows = 16;       // MMA M: weight rows per tile / stage
@@ -199,6 +199,7 @@ constexpr int kTcConsumers = 16;  // warps splitting K
 constexpr int kTcEpiWarps = 4;    // warps summing the partial tiles and storing the outputs
 constexpr int kTcThreads = (kTcConsumers + 1 + kTcEpiWarps) * 32;
 constexpr int kTcBarThreads = (kTcConsumers + kTcEpiWarps) * 32;  // compute + epilogue warps
+constexpr int kTcRedBufs = 3;     // reduction buffers between the compute and epilogue warps
 constexpr int kTcMaxStages = 8;
 constexpr int kTcMaxSlots = 256;  // T * k
 // dynamic shared memory: 227 KB per block less the kernel's static arrays
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
   const int xcols = a.T < kTcTok ? a.T : kTcTok;
   uint8_t* xs = smem;                                                      // [xcols][x_stride] f16 columns
   float* red = reinterpret_cast<float*>(smem + (size_t)xcols * a.x_stride);  // [2][warps][128]
-  uint8_t* stages = reinterpret_cast<uint8_t*>(red + 2 * kTcConsumers * 128);
+  uint8_t* stages = reinterpret_cast<uint8_t*>(red + kTcRedBufs * kTcConsumers * 128);
   uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (size_t)nst * a.stage_bytes);  // full[nst], empty[nst]
   __shared__ int uniq[kTcMaxSlots];
   __shared__ int ids_s[kTcMaxSlots];
@@ -276,8 +277,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
   __shared__ int warp_cnt[kTcThreads / 32];
   __shared__ int xexp[kTcTok];
   __shared__ float wmax[kTcConsumers][kTcTok];  // per-compute-warp max |x| of each column
-  __shared__ float tile_sc[2][kTcTok];          // per reduction buffer: column scales 2^xexp * weight scale
-  __shared__ uint16_t tile_bias[2][kTcRows];    // per reduction buffer: the tile's bias, source order
+  __shared__ float tile_sc[kTcRedBufs][kTcTok];          // per reduction buffer: column scales 2^xexp * weight scale
+  __shared__ uint16_t tile_bias[kTcRedBufs][kTcRows];    // per reduction buffer: the tile's bias, source order
   __shared__ float wsc;
   __shared__ int abort_flag;
   volatile int* abort_v = &abort_flag;
@@ -438,7 +439,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
     const int r_out = a.glu ? gl : gl + 8 * (o_c >> 1);  // stage row of the (first) output
     int n = 0;
     for (int tile = t_begin; tile < t_end; ++tile, ++n) {
-      const int b = n & 1, u = tile / tps, q = tile % tps;
+      const int b = n % kTcRedBufs, u = tile / tps, q = tile % tps;
       named_barrier(2 + b, kTcBarThreads);  // the compute warps have written tile n's buffer
       const float* rb = red + (size_t)b * kTcConsumers * 128;
       const int j = (et < nout && col < a.T) ? slot_tab[u][col] : -1;
@@ -468,7 +469,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
           a.y[(size_t)sl * N + tc_src_row(a, q, r_out)] = (uint16_t)f32_to_bf16_bits(fmaf(v, sc, bias0));
         }
       }
-      named_barrier_arrive(4 + b, kTcBarThreads);  // buffer b is free again
+      named_barrier_arrive(2 + kTcRedBufs + b, kTcBarThreads);  // buffer b is free again
     }
     return;
   }
@@ -578,9 +579,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
     __syncwarp();
     if (lane == 0 && ok) pipe_mbar_arrive(smem_addr(bars + nst + s));
     // The partial tile, the bias and the column scales into reduction buffer
-    // b, free once the epilogue warps are done with tile n - 2.
-    const int b = n & 1;
-    if (n >= 2) named_barrier(4 + b, kTcBarThreads);
+    // b, free once the epilogue warps are done with tile n - kTcRedBufs.
+    const int b = n % kTcRedBufs;
+    if (n >= kTcRedBufs) named_barrier(2 + kTcRedBufs + b, kTcBarThreads);
     float* rb = red + (size_t)b * kTcConsumers * 128;
     *reinterpret_cast<float4*>(rb + warp * 128 + lane * 4) = make_float4(d[0], d[1], d[2], d[3]);
     if (warp == 0) {
@@ -589,8 +590,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
     }
     named_barrier_arrive(2 + b, kTcBarThreads);  // tile n to the epilogue warps
   }
-  // the epilogue warps' releases of the last two buffers
-  for (int m = (n > 2 ? n - 2 : 0); m < n; ++m) named_barrier(4 + (m & 1), kTcBarThreads);
+  // the epilogue warps' releases of the last buffers
+  for (int m = (n > kTcRedBufs ? n - kTcRedBufs : 0); m < n; ++m)
+    named_barrier(2 + kTcRedBufs + m % kTcRedBufs, kTcBarThreads);
 }
 
 template <int WFMT>
@@ -637,14 +639,14 @@ TcGeom tc_geom(int K, int T) {
   g.bias_offset = (g.sf_offset + sf + 15u) / 16u * 16u;
   g.stage_bytes = (g.bias_offset + kTcRows * 2 + 127u) / 128u * 128u;
   g.x_stride = pad_to(2u * (uint32_t)K, (WFMT == MOE_WFMT_FP8_PER_EXPERT) ? 16u : 64u);
-  const size_t fixed = xcols * g.x_stride + 2 * kTcConsumers * 128 * sizeof(float) +
+  const size_t fixed = xcols * g.x_stride + kTcRedBufs * kTcConsumers * 128 * sizeof(float) +
                        2 * kTcMaxStages * sizeof(uint64_t);
   g.nst = 0;
   if (fixed < kTcSmemMax) {
     const size_t n = (kTcSmemMax - fixed) / g.stage_bytes;
     g.nst = (int)(n < (size_t)kTcMaxStages ? n : (size_t)kTcMaxStages);
   }
-  g.smem = xcols * g.x_stride + 2 * kTcConsumers * 128 * sizeof(float) + (size_t)g.nst * g.stage_bytes +
+  g.smem = xcols * g.x_stride + kTcRedBufs * kTcConsumers * 128 * sizeof(float) + (size_t)g.nst * g.stage_bytes +
            2 * (size_t)g.nst * sizeof(uint64_t);
   return g;
 }
