@@ -530,6 +530,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
       const uint8_t* xg = xs + (size_t)(g < xcols ? g : xcols - 1) * a.x_stride;
       if (WFMT == MOE_WFMT_FP8_PER_EXPERT) {
         float d2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 2  // two k-blocks' loads and conversions in flight: 3-4% faster than one
         for (int kb = warp; kb < K / 64; kb += kTcConsumers) {
           const int k0 = kb * 64 + 16 * tig;
           const uint4 wa = *reinterpret_cast<const uint4*>(rowA + k0);
@@ -551,6 +552,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
         const uint8_t* sfs = st + a.sf_offset;
         const uint8_t* sfA = sfs + (size_t)tc_blk_row(a, g) * sf_row;
         const uint8_t* sfB = sfs + (size_t)tc_blk_row(a, g + 8) * sf_row;
+#pragma unroll 3  // three groups in flight (1-2% faster than one or two)
         for (int grp = warp; grp < sf_row; grp += kTcConsumers) {
           const uint32_t wa = *reinterpret_cast<const uint32_t*>(rowA + 16 * grp + 4 * tig);
           const uint32_t wb = *reinterpret_cast<const uint32_t*>(rowB + 16 * grp + 4 * tig);
