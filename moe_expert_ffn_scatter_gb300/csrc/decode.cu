@@ -185,14 +185,14 @@ __global__ void weighted_sum_kernel(const uint16_t* __restrict__ y2, const int32
 // exact) and runs mma.sync m16n8k16 (f16 x f16 -> f32) against the token
 // columns, staged as f16 scaled per token by a power of two so that no bf16
 // value overflows or loses bits in f16, and leaves its partial tile in one of
-// kTcRedBufs reduction buffers. Warps 17-20 sum the sixteen partial tiles in warp
-// order, scale them back and write every (token, slot) that selected the
+// kTcRedBufs reduction buffers. Warps 17-20 sum the sixteen partial tiles in
+// warp order, scale them back and write every (token, slot) that selected the
 // expert (the first launch applies the GLU to its gate/up row pairs on the
 // way out) while the compute warps go on with the next tile. Each buffer b
 // is handed over through its own pair of named barriers, 2 + b (partials
-// written: the compute warps arrive, the epilogue warps wait) and 2 + R + b
-// (buffer free again: the other way round), so a barrier never has two
-// generations in flight.
+// written: the compute warps arrive, the epilogue warps wait) and
+// 2 + kTcRedBufs + b (buffer free again: the other way round), so a barrier
+// never has two generations in flight.
 constexpr int kTcRows = 16;       // MMA M: weight rows per tile / stage
 constexpr int kTcTok = 8;         // MMA N: token columns
 constexpr int kTcConsumers = 16;  // warps splitting K
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemv_kernel(const __grid_con
   // (their outputs are never written), so the buffer is sized by T
   const int xcols = a.T < kTcTok ? a.T : kTcTok;
   uint8_t* xs = smem;                                                      // [xcols][x_stride] f16 columns
-  float* red = reinterpret_cast<float*>(smem + (size_t)xcols * a.x_stride);  // [2][warps][128]
+  float* red = reinterpret_cast<float*>(smem + (size_t)xcols * a.x_stride);  // [kTcRedBufs][warps][128]
   uint8_t* stages = reinterpret_cast<uint8_t*>(red + kTcRedBufs * kTcConsumers * 128);
   uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (size_t)nst * a.stage_bytes);  // full[nst], empty[nst]
   __shared__ int uniq[kTcMaxSlots];
