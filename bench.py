@@ -530,8 +530,8 @@ def run_ours(args):
         "eager_us_per_layer": 1e3 * eager_ms / args.steps,
     }
     roofline = {"bound": "tensor",
-                "kernel": "gemm1_act (grouped_gemm_kernel: tcgen05 mxf8f6f4 block-scaled GEMM1 with SiLU*mul + "
-                          "e4m3/UE8M0 quantisation in its epilogue)",
+                "kernel": "gemm1_act (grouped_gemm_pair_kernel on this layer: CTA-pair tcgen05 mxf8f6f4 "
+                          "block-scaled GEMM1 with SiLU*mul + e4m3/UE8M0 quantisation in its epilogue)",
                 "achieved": g1_tf, "peak": fp8_peak, "unit": "TFLOP/s", "frac": g1_tf / fp8_peak,
                 "traffic": recorded_traffic("gemm1_act"),
                 "peak_note": "%s burst bf16 x 2 (the dense FP8/FP6/FP4-in-mxf8f6f4 rate is twice bf16): %.1f TFLOP/s "
